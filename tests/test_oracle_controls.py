@@ -1,0 +1,86 @@
+"""Planted controls: copies of the oracle with one mistake each must fail the
+pins. The pages' kernel contract plants four such controls (PR #1377 "LFM2:
+shared-round decode", commit "kernel contract: LFM2's shared-round launches
+carry recorded M1/M2 limits and four planted controls": a tie to the highest
+id, a nonfinite logit not flagged, every stream reading or writing the first
+stream's conv state or KV cache); the rest guard the readings the pins fix.
+The mistakes are planted in the oracle's source, on the CPU.
+"""
+
+import inspect
+import types
+
+import pytest
+
+import oracle.step as oracle_step
+import oracle_pins as P
+
+
+def mutant(*edits):
+    src = inspect.getsource(oracle_step)
+    for old, new in edits:
+        assert src.count(old) == 1, old
+        src = src.replace(old, new)
+    mod = types.ModuleType("oracle_mutant")
+    exec(compile(src, "oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+CONTROLS = {
+    "tie_to_highest_id": (
+        [("pick[r] = int(np.argmax(row))  # first occurrence of the maximum",
+          "pick[r] = int(len(row) - 1 - np.argmax(row[::-1]))")],
+        [P.pin_argmax_golden, P.pin_argmax_brute]),
+    "nonfinite_not_flagged": (
+        [("if not np.all(np.isfinite(row)):", "if False:")],
+        [P.pin_argmax_golden]),
+    "streams_read_first_conv_state": (
+        [("short_conv_stream(bcx[off:off + rows], w, states[s], want_history)",
+          "short_conv_stream(bcx[off:off + rows], w, states[0], want_history)")],
+        [P.pin_segmented_equals_alone]),
+    "streams_write_first_conv_state": (
+        [("        new_states.append(st)\n", "        new_states[0:1] = [st]\n")],
+        [P.pin_segmented_equals_alone]),
+    "streams_read_first_kv_cache": (
+        [("attention_stream(q[off:off + rows], Ks[s], Vs[s], keys, rows)",
+          "attention_stream(q[off:off + rows], Ks[0], Vs[0], keys, rows)")],
+        [P.pin_segmented_equals_alone]),
+    "conv_taps_reversed": (
+        [("conv = (wf[:, 0] * bf16_to_f64(seq[i])", "conv = (wf[:, 2] * bf16_to_f64(seq[i])"),
+         ("+ wf[:, 2] * bf16_to_f64(seq[i + 2]))", "+ wf[:, 0] * bf16_to_f64(seq[i + 2]))")],
+        [P.pin_conv_worked]),
+    "gate_truncated": (
+        [("return (upper + up.astype(np.uint64)).astype(np.uint16)", "return upper.astype(np.uint16)")],
+        [P.pin_bf16_rounding_golden, P.pin_conv_worked, P.pin_bf16_rounding_matches_torch]),
+    "conv_slices_swapped": (
+        [("c = bf16_to_f64(bcx[i, h:2 * h])", "c = bf16_to_f64(bcx[i, 2 * h:3 * h])"),
+         ("x = bf16_to_f64(bcx[i, 2 * h:3 * h])", "x = bf16_to_f64(bcx[i, h:2 * h])")],
+        [P.pin_conv_worked, P.pin_conv_special_taps]),
+    "score_not_scaled": (
+        [("SCALE = 0.125 ", "SCALE = 1.0 ")],
+        [P.pin_attn_two_keys_scale, P.pin_attn_brute]),
+    "causal_off_by_one": (
+        [("return keys - rows + i + 1", "return keys - rows + i + 2")],
+        [P.pin_attn_one_key, P.pin_attn_causal_edge]),
+    "gqa_mapping_wrong": (
+        [("            g = h // GROUP\n", "            g = h % NKV\n")],
+        [P.pin_attn_gqa]),
+    "merge_sums_unrescaled_l": (
+        [("L = (wgt * l).sum(axis=-1)", "L = l.sum(axis=-1)")],
+        [P.pin_attn_split_merge]),
+    "accept_compares_next_pick": (
+        [("or flag[a] or int(pick[a]) != d:", "or flag[a] or int(pick[a + 1]) != d:")],
+        [P.pin_accept_cases, P.pin_accept_recipe]),
+    "rewind_one_row_early": (
+        [("return np.stack([history[a + 1], history[a + 2]])", "return np.stack([history[a], history[a + 1]])")],
+        [P.pin_rewind]),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CONTROLS))
+def test_planted_control_goes_red(name):
+    edits, pins = CONTROLS[name]
+    mod = mutant(*edits)
+    for pin in pins:
+        with pytest.raises(Exception):
+            pin(mod)
