@@ -1,0 +1,449 @@
+"""Benchmark of the segmented speculative-verify step on GB300.
+
+One "step" is the whole verify path over one batch: 30 conv layers
+(tf_conv_rows), 10 attention layers (tf_attn_partials + tf_attn_merge), the
+greedy pick (tf_argmax_rows) and the accept step (tf_accept), captured in one
+CUDA graph. Metric: verified rows per second (rows of every stream's window,
+all ranks) and the achieved HBM bandwidth.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5] [--impl tf|reference]
+
+Default workload: 16 streams of one row, 30 conv + 10 attention layers, key
+counts uniform in [256, 4096] (the plain shared round). The other workloads
+(1, 3, 4, 5) are selectable. ``--impl reference`` times the float64 CPU oracle
+on the host cores on a bounded sample of the same workload.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified rows/s per segmented verify step"
+UNIT = "rows/s"
+L2_FLUSH_BYTES = 256 << 20      # > 129 MB L2
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="tf", choices=["tf", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(x, world, device="cpu"):
+    """Max of a float over ranks (identity on one rank)."""
+    if world == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append(dict(ts=ts, sm=float(parts[1]), smax=float(parts[2]), util=float(parts[4]),
+                                 hw=parts[6], hwt=parts[7], swt=parts[8], pcap=parts[9]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        window = [r for r in rows if t0 - 0.25 <= r["ts"] <= t1 + 0.25]
+        loaded = [r for r in window if r["util"] > 0] or window or rows
+        reasons = set()
+        for r in loaded:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in loaded), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(loaded)}
+
+
+# ----------------------------------------------------------- helpers
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    with open(os.path.join(ROOT, "stream_speculative_decode_gb300", "csrc", "attn.cu"), "rb") as f:
+        h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload_index):
+    """Per-launch DRAM bytes of the partials kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "attn_partials_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if rec.get("source_sha256_16") != kernel_source_hash():
+        return None
+    ent = rec.get("per_workload", {}).get(str(workload_index))
+    return None if ent is None else float(ent["dram_bytes_per_launch"])
+
+
+def oracle_child(workload_index, n_streams, attn_rows, repeats):
+    """(Child process.) Time the oracle on a bounded sample of the workload and
+    scale it to one whole step: one conv layer over the first ``n_streams``
+    streams, one attention layer over the first ``attn_rows`` window rows of
+    the first stream (all 32 heads), and the greedy pick plus accept over the
+    sampled streams' rows. Each part is scaled by its work: conv and pick by
+    rows, attention by visible keys summed over rows; then times the layer
+    counts of the workload. Prints JSON with the per-repeat step estimates."""
+    import json as _json
+    from stream_speculative_decode_gb300 import inputs as I
+    from oracle import step as O
+    w = I.workload(workload_index)
+    sub = I.Workload("sample", w.rows[:n_streams], w.keys[:n_streams], 1, 1, vocab=w.vocab,
+                     drafts=w.drafts, tie_rows=min(w.tie_rows, 1), nan_rows=min(w.nan_rows, 1),
+                     inf_frac=w.inf_frac, seed=w.seed)
+    inp = I.make_inputs(sub, backend="numpy")
+    R_full = sum(w.rows)
+    R_s = sum(sub.rows)
+    vis = lambda k, r, i: k - r + i + 1
+    A_full = sum(vis(k, r, i) for r, k in zip(w.rows, w.keys) for i in range(r))
+    r0, k0 = w.rows[0], w.keys[0]
+    ar = min(attn_rows, r0)
+    A_s = sum(vis(k0, r0, i) for i in range(ar))
+    est = []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        O.conv_layer(inp.streams, inp.bcx[0], inp.w[0], inp.state[0])
+        t1 = time.perf_counter()
+        for i in range(ar):
+            O.attention_stream(inp.q[0][i:i + 1], inp.K[0][0], inp.V[0][0], vis(k0, r0, i), 1)
+        t2 = time.perf_counter()
+        pick, flag = O.argmax_rows(inp.logits)
+        O.accept_all(inp.streams, inp.ids, pick, flag, w.vocab)
+        t3 = time.perf_counter()
+        est.append(w.n_conv * (t1 - t0) * R_full / R_s + w.n_attn * (t2 - t1) * A_full / A_s
+                   + (t3 - t2) * R_full / R_s)
+    print(_json.dumps(dict(step_s=est, rows=R_full)))
+
+
+def oracle_sample(workload_index, repeats):
+    """Run ``oracle_child`` in a child process with one BLAS thread."""
+    n, ar = SAMPLE[workload_index]
+    code = (f"import sys; sys.path.insert(0, {ROOT!r}); import bench; "
+            f"bench.oracle_child({workload_index}, {n}, {ar}, {repeats})")
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[v] = "1"
+    r = subprocess.run([sys.executable, "-c", code], env=env, stdout=subprocess.PIPE,
+                       stderr=subprocess.PIPE, text=True, timeout=3600)
+    if r.returncode != 0:
+        raise RuntimeError("oracle sample failed: " + r.stderr[-2000:])
+    out = json.loads(r.stdout.strip().splitlines()[-1])
+    return out["step_s"], out["rows"]
+
+
+# streams in the conv / pick sample, window rows in the attention sample
+SAMPLE = {1: (1, 4), 2: (4, 1), 3: (2, 2), 4: (1, 1), 5: (2, 2)}
+
+
+def sample_desc(w, index):
+    n, ar = SAMPLE[index]
+    return (f"float64 numpy oracle, 1 BLAS thread: one conv layer over the first {n} of {len(w.rows)} "
+            f"streams, one attention layer over {min(ar, w.rows[0])} window row(s) of stream 0 "
+            f"({w.keys[0]} keys, 32 heads), pick + accept over the sampled rows; each part scaled "
+            f"to the whole step ({w.n_conv} conv + {w.n_attn} attention layers, {sum(w.rows)} rows) "
+            f"by rows or by visible keys")
+
+
+# -------------------------------------------------------------- arms
+
+def run_reference(args, rank, world):
+    from stream_speculative_decode_gb300 import inputs as I
+    if rank != 0:
+        return 0
+    w = I.workload(args.workload)
+    times, rows = oracle_sample(args.workload, args.warmup + args.steps)
+    timed = times[args.warmup:]
+    sec = sum(timed) / max(len(timed), 1)
+    value = rows / sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample_desc(w, args.workload)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": w.name, "streams": len(w.rows), "rows": sum(w.rows), "keys_total": sum(w.keys),
+            "conv_layers": w.n_conv, "attn_layers": w.n_attn, "vocab": w.vocab,
+            "widths": "H=2048, conv in 6144 (B,C,x), kw=3, 32 q / 8 kv heads, d=64"}
+
+
+def run_tf(args, rank, world):
+    import numpy as np
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from stream_speculative_decode_gb300 import inputs as I
+    from stream_speculative_decode_gb300 import tf
+    from stream_speculative_decode_gb300.step import DeviceStep, algorithmic_bytes
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    dist_init(world, "nccl")
+    w = I.workload(args.workload)
+    inp = I.make_inputs(w, backend="torch", device=dev)
+    d = DeviceStep(inp, device=dev)
+    ab = algorithmic_bytes(inp.streams, w.n_conv, w.n_attn, w.vocab)
+    R = inp.R
+
+    # per-launch timing of the dominant kernel, recorded inside the graph
+    try:
+        evs = {"attn_partials": [(torch.cuda.Event(enable_timing=True, external=True),
+                                  torch.cuda.Event(enable_timing=True, external=True))
+                                 for _ in range(w.n_attn)]}
+        graph_events = True
+    except TypeError:
+        evs, graph_events = None, False
+    # warm the kernels once outside capture
+    d.run()
+    torch.cuda.synchronize()
+    d.capture(events=evs)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    for _ in range(args.warmup):
+        flush.zero_()
+        d.graph.replay()
+    torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    part_ms = []
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    for k in range(args.steps):
+        flush.zero_()                       # L2 flushed between timed steps (outside the events)
+        ev[k][0].record(stream)
+        d.graph.replay()
+        ev[k][1].record(stream)
+        if graph_events:                    # read this replay's per-launch events
+            ev[k][1].synchronize()
+            part_ms.extend(a.elapsed_time(b) for a, b in evs["attn_partials"])
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    dist_barrier(world)
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    clocks_sum = clocks.summary(t_wall0, t_wall1)
+    ms = sum(step_ms) / len(step_ms)
+    ms_max = dist_max(ms, world, device=dev)
+
+    if not graph_events:
+        # no event nodes in graphs on this PyTorch: time eager launches of the same kernel
+        for _ in range(min(args.steps, 20)):
+            for l in range(w.n_attn):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                tf.tf_attn_partials(d.seg, l, d.q[l], d.partials)
+                b.record(stream)
+                torch.cuda.synchronize()
+                part_ms.append(a.elapsed_time(b))
+    clocks.stop()
+
+    peak, peak_kind = measured_peaks()
+    attn_alg = sum(k for _, _, k in inp.streams) * 8 * 64 * 2 * 2 + R * 32 * 64 * 2
+    part_avg_ms = sum(part_ms) / len(part_ms) if part_ms else float("nan")
+    achieved = attn_alg / (part_avg_ms * 1e-3) / 1e9
+    traffic = recorded_traffic(args.workload)
+
+    # end to end through the C ABI with host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(d, args, stream, flush)
+
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0 and world == 1:
+        times, rows = oracle_sample(args.workload, 3)
+        sec = sum(times) / len(times)
+        cpu = {"value": rows / sec, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": sample_desc(w, args.workload) + "; mean of 3 samples"}
+
+    step_gbs = ab["total"] / (ms_max * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": R * world / (ms_max * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(workload_config(w), l2="flushed: 256 MB written between timed steps, outside the events",
+                       graph="one CUDA graph per step", parallelism=f"replicas x{world}"),
+        "hbm": {"step_algorithmic_bytes": ab["total"], "achieved_gbs": step_gbs, "peak_gbs": peak,
+                "frac": step_gbs / peak, "peak_kind": peak_kind},
+        "roofline": {"kernel": "tf_attn_partials", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": attn_alg, "avg_launch_ms": part_avg_ms,
+                     "launches_timed": len(part_ms), "peak_kind": peak_kind,
+                     "timing": "CUDA events around each launch inside the graph, every timed step"
+                     if graph_events else "CUDA events around eager launches after the timed region"},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": d.launches_per_step() * args.steps,
+        "clocks": clocks_sum,
+        "wall_s_timed": t_wall1 - t_wall0,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    d.free()
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(d, args, stream, flush):
+    """Same metric through the public API with host buffers: every step copies
+    its inputs (conv inputs, queries, logits, ids) from pinned host memory and
+    reads back the picks, flags and per-stream accept results."""
+    import torch
+    host_in = [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)) for t in
+               d.bcx + d.q + [d.logits, d.ids]]
+    outs = [d.pick, d.flag, d.accept_len, d.next_token, d.new_keys, d.sflag]
+    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+    h2d = sum(h.numel() * h.element_size() for _, h in host_in)
+    d2h = sum(h.numel() * h.element_size() for h in host_out)
+    steps = max(3, min(args.steps, 50))
+
+    def one():
+        for dv, hv in host_in:
+            dv.copy_(hv, non_blocking=True)
+        d.graph.replay()
+        for dv, hv in zip(outs, host_out):
+            hv.copy_(dv, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        one()
+        b.record(stream)
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    ms = sum(ts) / len(ts)
+    return {"value": d.R / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": ms, "steps": steps}
+
+
+def main():
+    args = parse()
+    rank, world, _ = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_tf(args, rank, world)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

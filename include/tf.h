@@ -1,0 +1,224 @@
+/*
+ * tf.h -- C ABI of the segmented speculative-verify step (LFM2 shared-round
+ * decode with drafts) for NVIDIA GB300 (sm_103a).
+ *
+ * What the step computes comes from the TensorFold pages:
+ *   [SRD]   PR #1377 "LFM2: shared-round decode"
+ *           - commit "a shared round runs each layer's conv and attention once
+ *             over all its streams" (segment table of cache addresses, row
+ *             offsets and key counts; one launch per layer over every row;
+ *             per-stream attention partials; float64 attention and a host
+ *             replay of the conv steps as the checks);
+ *           - commit "a verify's greedy rows take the GPU's pick of their
+ *             logits" (first largest logit, ties to the lower id, nonfinite
+ *             rows flagged);
+ *           - commit "the conv, qk, attention and merge kernels' bodies as
+ *             inline functions" (qk, attention, merge);
+ *           - section "Failures the tests catch" (a scratch too small for
+ *             per-stream partials; a table reaching memory it did not declare).
+ *   [DSP]   PR #1391 "lfm2: draft with LiquidAI's DSpark drafter (--drafter)":
+ *           the lane core verifies every draft; the target's attention keeps
+ *           its causal count.
+ *
+ * Conventions for every call:
+ *   - All tensors are dense, row-major, in DEVICE memory owned by the caller,
+ *     and start on a 16-byte boundary. bf16 tensors are passed as `void*`.
+ *   - Every call is asynchronous on the caller's CUDA stream `stream` (a
+ *     cudaStream_t; NULL is the legacy default stream) and never synchronises.
+ *   - Every call returns a tf_status. Invalid arguments are refused on the host
+ *     before anything is launched; nothing aborts. A nonfinite logit is data,
+ *     reported in the flags, never an error.
+ *   - Model widths are fixed (LFM2.5-24B-A2B): TF_H conv channels, conv input
+ *     TF_CIN = 3*TF_H as the consecutive slices (B, C, x), kernel width TF_KW,
+ *     TF_NQ query heads sharing TF_NKV KV heads of width TF_D.
+ */
+#ifndef TF_H_INCLUDED
+#define TF_H_INCLUDED
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TF_H        2048
+#define TF_CIN      6144
+#define TF_KW       3
+#define TF_NQ       32
+#define TF_NKV      8
+#define TF_D        64
+#define TF_MAX_ROWS 16          /* window rows per stream (1 + drafts) */
+#define TF_MAX_KEYS (1 << 22)   /* cache rows per stream */
+#define TF_MAX_STREAMS 65536
+
+typedef enum {
+    TF_OK = 0,
+    TF_EINVAL = 1,   /* null pointer, bad shape, unpacked rows, aliasing, misalignment */
+    TF_ERANGE = 2,   /* a size beyond the limits above */
+    TF_ENOMEM = 3,   /* the library's own table allocation failed */
+    TF_ECUDA = 4     /* a CUDA call or launch failed (see tf_last_cuda_error) */
+} tf_status;
+
+struct CUstream_st;                       /* cudaStream_t is struct CUstream_st* */
+typedef struct CUstream_st* tf_cuda_stream;
+
+/* One stream of a shared round ([SRD] "a table of the streams' cache
+ * addresses, row offsets and key counts").
+ *   rows        window rows r_s = 1 + drafts, 1..TF_MAX_ROWS
+ *   row_offset  first row of the stream in every [R][...] tensor; streams are
+ *               packed in order: row_offset_0 = 0, row_offset_{s+1} =
+ *               row_offset_s + rows_s
+ *   keys        k_s, cache entries INCLUDING the window's own rows (their K/V
+ *               are already written); window row i sees keys
+ *               [0, keys - rows + i + 1) (causal, [DSP]); rows <= keys
+ *   kv_capacity cache rows allocated per KV head, keys <= kv_capacity */
+typedef struct {
+    int32_t rows;
+    int32_t row_offset;
+    int32_t keys;
+    int32_t kv_capacity;
+} tf_stream;
+
+/* Host-side sizes of a table, from tf_segments_plan (no GPU needed). */
+typedef struct {
+    int32_t n_streams;
+    int32_t n_rows;           /* R = sum of rows */
+    int32_t max_rows;
+    int32_t n_conv_tiles;     /* 8-row conv tiles ([SRD] "8-row tiles") */
+    int32_t n_attn_items;     /* (stream, key chunk) work items per KV head */
+    int32_t reserved;
+    int64_t n_partials;       /* partial records: sum_s rows_s * 32 * chunks_s */
+    int64_t partials_bytes;   /* scratch tf_attn_partials needs (see below) */
+} tf_plan;
+
+/* The library's own device copy of a segment table. Immutable once built. */
+typedef struct tf_segments tf_segments;
+
+/* Split-K chunk of a stream: keys [c*chunk, (c+1)*chunk). The chunk length is
+ * 256 * rows keys; it depends on the stream alone, so a stream's results do
+ * not depend on which other streams share the round. */
+int32_t tf_chunk_keys(int32_t rows);
+
+/* Validate `streams` and compute the table's sizes. Host only; touches no GPU.
+ * Errors: TF_EINVAL (null, rows < 1, unpacked offsets, keys < rows,
+ * keys > kv_capacity), TF_ERANGE (beyond TF_MAX_*). n_streams == 0 is an
+ * empty round (every call on its table is a no-op). */
+int tf_segments_plan(const tf_stream* streams, int n_streams, tf_plan* out);
+
+/* Build the segment table on the device ([SRD] segments.zig).
+ *   streams      host array [n_streams]
+ *   conv_state   host array [n_conv][n_streams] of device pointers, each to a
+ *                bf16 [2][TF_H] rolling conv state (oldest row first), read
+ *                and rewritten in place by tf_conv_rows / tf_accept
+ *   conv_hist    NULL, or host array [n_conv][n_streams] of device pointers,
+ *                each to a bf16 [rows+2][TF_H] history written by
+ *                tf_conv_rows (the state before the window, then every row's
+ *                gate); entries of one-row streams may be NULL. NULL disables
+ *                the conv rewind in tf_accept.
+ *   k_cache, v_cache  host arrays [n_attn][n_streams] of device pointers, each
+ *                to a bf16 [TF_NKV][kv_capacity][TF_D] cache (head-major)
+ * Refuses (TF_EINVAL) null or misaligned pointers and any two buffers of the
+ * table that overlap (conv states and histories across every stream and
+ * layer; K and V caches likewise) -- the bug class of [SRD]'s planted controls
+ * "every stream reading or writing the first stream's conv state or kv cache".
+ * The table is copied to the device on `stream` before the call returns; the
+ * host arrays may be freed at once. *out is owned by the caller and released
+ * with tf_segments_free. */
+int tf_segments_build(const tf_stream* streams, int n_streams,
+                      const void* const* conv_state, const void* const* conv_hist,
+                      const void* const* k_cache, const void* const* v_cache,
+                      int n_conv, int n_attn, tf_cuda_stream stream,
+                      tf_segments** out);
+
+/* Free a table (synchronises the device through cudaFree). NULL is a no-op. */
+int tf_segments_free(tf_segments* seg);
+
+/* Sizes of a built table (same as tf_segments_plan's). */
+int tf_segments_query(const tf_segments* seg, tf_plan* out);
+
+/* Bytes of partial scratch tf_attn_partials writes and tf_attn_merge reads
+ * ([SRD] "the scratch's attention partials now hold each stream's apart").
+ * Layout: float o[n_partials][TF_D], then float2 ml[n_partials] (m, l).
+ * 0 for a NULL table. */
+size_t tf_partials_bytes(const tf_segments* seg);
+
+/* a1. LFM2 gated short conv of one conv layer over every row of every stream
+ * ([SRD]: "short conv (30 layers)", run once a layer over every row).
+ *   bcx  bf16 [R][TF_CIN], row = (B, C, x)
+ *   w    bf16 [TF_H][TF_KW] depthwise taps; w[c][0] multiplies the oldest row
+ *   y    float [R][TF_H] output, y = C * conv
+ * Per stream, row by row: bx = bf16_rne(B*x); seq = [state0, state1, bx_0..];
+ * conv_i = w0*seq[i] + w1*seq[i+1] + w2*seq[i+2] (fp32). Afterwards the
+ * stream's state holds the last two entries of seq and its history (if any)
+ * all of them; both are bit-exact. Errors: TF_EINVAL (null/misaligned,
+ * conv_layer out of range). */
+int tf_conv_rows(const tf_segments* seg, int conv_layer, const void* bcx,
+                 const void* w, float* y, tf_cuda_stream stream);
+
+/* a2. Causal GQA attention partials of one attention layer: for every stream,
+ * KV head, key chunk, window row and query head, (m, l, o) over the chunk's
+ * visible keys ([SRD] "qk, attention and merge (10 layers)").
+ *   q         bf16 [R][TF_NQ][TF_D]
+ *   partials  device scratch of tf_partials_bytes(seg) bytes. Record of
+ *             stream s, chunk c, KV head g, row i, head 4g+hh:
+ *             pbase_s + ((c*8 + g)*rows_s + i)*4 + hh, pbase_s = sum over
+ *             earlier streams of rows * 32 * chunks.
+ *             m = (largest score) * log2(e), l = sum 2^(s*log2(e) - m),
+ *             o[d] = sum 2^(s*log2(e) - m) * v[d]; a chunk without a visible
+ *             key has m = -inf, l = 0, o = 0.
+ * Score = (q . k) / 8; query head h reads KV head h / 4. Errors: TF_EINVAL. */
+int tf_attn_partials(const tf_segments* seg, int attn_layer, const void* q,
+                     void* partials, tf_cuda_stream stream);
+
+/* a3. Log-sum-exp merge of the partials into the attention output
+ * ([SRD] lfm2_merge_row): out = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c,
+ * M = max_c m_c, empty chunks skipped.
+ *   out  float [R][TF_NQ][TF_D]. Errors: TF_EINVAL. */
+int tf_attn_merge(const tf_segments* seg, const void* partials, float* out,
+                  tf_cuda_stream stream);
+
+/* a4. Greedy pick of each row of bf16 logits ([SRD] lfm2_argmax: "the first
+ * largest logit ... ties to the lower id, nonfinite rows flagged").
+ *   logits      bf16, row r at logits + r*row_stride (elements), V per row
+ *   pick        int32 [R]: lowest id holding the row's largest value (-0 and
+ *               +0 are equal); -1 when the row is flagged
+ *   flag        uint8 [R]: 1 if the row holds a NaN, +Inf or -Inf, else 0
+ * Needs no table. R == 0 is a no-op. Errors: TF_EINVAL (null, V < 1,
+ * row_stride < V), TF_ERANGE (V > 2^30, R > 2^24). Rows are read with 16-byte
+ * vector loads when logits and row_stride allow it. */
+int tf_argmax_rows(const void* logits, int R, int V, int64_t row_stride,
+                   int32_t* pick, uint8_t* flag, tf_cuda_stream stream);
+
+/* a5. Greedy verify of every stream: the accepted-draft prefix length
+ * ([DSP] "the lane core verifies every draft"; [SRD] verifyFn takes the pick
+ * for greedy rows, flagged rows are drawn on the host).
+ *   ids         int32 [R]: row 0 of a window is the pending token, rows 1..
+ *               the drafts
+ *   pick, flag  from tf_argmax_rows
+ *   vocab       draft ids outside [0, vocab) never match
+ *   accept_len  int32 [S]: a = leading drafts j+1 with pick[j] == ids[j+1]
+ *               and row j unflagged (0 <= a <= rows-1)
+ *   next_token  int32 [S]: pick of row a, or -1 when row a is flagged
+ *   new_keys    int32 [S]: keys - rows + a + 1
+ *   sflag       uint8 [S]: bit 0 row a flagged (host draws), bit 1 a draft id
+ *               of the window lies outside [0, vocab)
+ *   rewind_conv nonzero: rewrite every conv layer's state of every stream with
+ *               rows > 1 to history rows a+1, a+2 (the state after row a);
+ *               needs the table's conv_hist
+ * Errors: TF_EINVAL (null outputs; rewind without histories). */
+int tf_accept(const tf_segments* seg, const int32_t* ids, const int32_t* pick,
+              const uint8_t* flag, int vocab, int32_t* accept_len,
+              int32_t* next_token, int32_t* new_keys, uint8_t* sflag,
+              int rewind_conv, tf_cuda_stream stream);
+
+/* Name of a status code. */
+const char* tf_strerror(int status);
+
+/* The CUDA error code behind the last TF_ECUDA of this thread (0 if none). */
+int tf_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TF_H_INCLUDED */

@@ -1,0 +1,413 @@
+// a2/a3: causal GQA attention of every window row against its stream's KV
+// cache, as split-K partials and a log-sum-exp merge, one launch each a layer.
+//
+// PR #1377 "LFM2: shared-round decode": commit "the conv, qk, attention and
+// merge kernels' bodies as inline functions" (qk, attention, merge) and commit
+// "a shared round runs each layer's conv and attention once over all its
+// streams" (one launch a layer over every row from the segment table; the
+// scratch's attention partials hold each stream's apart). PR #1391: the
+// target's attention keeps its causal count.
+//
+// Partials kernel: one CTA per (work item = stream key chunk, KV head). The
+// chunk length depends on the stream alone (256 * rows keys), so a stream's
+// partials do not depend on the other streams of the round. The CTA streams
+// the chunk's K and V (64 keys a stage, 4-stage cp.async pipeline into
+// XOR-swizzled shared memory) once, for all 4*rows query rows of the KV head
+// (GQA: query head h reads KV head h/4) -- the whole window shares one read of
+// the cache. Four warps split each stage's keys (16 each); every warp keeps an
+// online softmax over its keys for all query rows; the warps are combined at
+// the end. q.k runs on bf16 tensor-core MMAs with fp32 accumulation (exact
+// products); P.V runs with P and V in fp16 (V's bf16 values convert exactly
+// within fp16's range) and fp32 accumulation.
+//
+// HBM bound: 256 bytes of K+V per key per KV head; the window's queries ride
+// along. Arithmetic intensity 4*rows flops per byte for each of q.k and P.V.
+#include "tf_internal.cuh"
+
+namespace tf {
+namespace {
+
+constexpr int kKT = 64;                 // keys per stage
+constexpr int kStages = 4;
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRowB = TF_D * 2;         // 128 bytes per cache row
+constexpr int kStageB = 2 * kKT * kRowB;  // K then V: 16 KB
+constexpr int kOStride = 68;            // floats per row of the warp-combine buffer
+constexpr float kLog2e8 = 0.18033688011112042f;   // log2(e) / sqrt(64)
+
+__host__ __device__ constexpr int smem_bytes(int mt) { return kStages * kStageB + 16 * mt * kRowB; }
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    const int sz = valid ? 16 : 0;   // 0: fill the 16 bytes with zeros
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(sz));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
+__device__ __forceinline__ void ldsm_x4(uint32_t r[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t r[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_f16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+// two bf16 -> two fp16 (exact for |v| in fp16's normal range)
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) {
+    return pack_h2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+// byte offset of 16-byte chunk `ch` of row `r` in a swizzled 128-byte-row tile
+__device__ __forceinline__ uint32_t swz(int r, int ch) { return uint32_t(r * kRowB + ((ch ^ (r & 7)) << 4)); }
+
+template <int MT>
+__global__ void __launch_bounds__(kThreads)
+attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
+                     float* __restrict__ part_o, float2* __restrict__ part_ml) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr bool kQReg = MT <= 2;
+    const int item_idx = blockIdx.x / TF_NKV;
+    const int g = blockIdx.x % TF_NKV;
+    const AttnItem item = t.items[item_idx];
+    const SegStream st = t.streams[item.stream];
+    const int nq = st.rows * 4;
+    const int c0 = item.chunk * st.chunk_keys;
+    const int nkeys = min(st.chunk_keys, st.keys - c0);
+    const int nst = (nkeys + kKT - 1) / kKT;
+    const size_t slot = size_t(layer) * t.S + item.stream;
+    const uint16_t* Kg = static_cast<const uint16_t*>(t.k_cache[slot]) + (size_t(g) * st.cap + c0) * TF_D;
+    const uint16_t* Vg = static_cast<const uint16_t*>(t.v_cache[slot]) + (size_t(g) * st.cap + c0) * TF_D;
+    unsigned char* sKV = smem;
+    unsigned char* sQ = smem + kStages * kStageB;
+    const uint32_t sKV32 = smem_u32(sKV), sQ32 = smem_u32(sQ);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // query rows qi = 4*i + hh (window row i, head 4g + hh); rows past nq are zero
+    for (int idx = tid; idx < 16 * MT * 8; idx += kThreads) {
+        const int qi = idx >> 3, ch = idx & 7;
+        const bool valid = qi < nq;
+        const uint16_t* src = q + ((size_t(st.row_offset + (qi >> 2)) * TF_NQ + 4 * g + (qi & 3)) * TF_D + ch * 8);
+        cp_async16(sQ32 + swz(qi, ch), valid ? src : q, valid);
+    }
+    auto issue = [&](int s) {
+        const uint32_t buf = sKV32 + (s % kStages) * kStageB;
+        const int key0 = s * kKT;
+#pragma unroll
+        for (int k = 0; k < (kKT * 8) / kThreads; ++k) {
+            const int idx = tid + k * kThreads;
+            const int r = idx >> 3, ch = idx & 7;
+            const bool valid = key0 + r < nkeys;
+            const size_t off = size_t(key0 + r) * TF_D + ch * 8;
+            cp_async16(buf + swz(r, ch), valid ? Kg + off : Kg, valid);
+            cp_async16(buf + kKT * kRowB + swz(r, ch), valid ? Vg + off : Vg, valid);
+        }
+    };
+#pragma unroll
+    for (int s = 0; s < kStages - 1; ++s) {
+        if (s < nst) issue(s);
+        cp_async_commit();
+    }
+
+    const int g8 = lane >> 2, t4 = lane & 3;
+    float o[MT][8][4];
+    float m[MT][2], l[MT][2];
+    int lim[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+        for (int dt = 0; dt < 8; ++dt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[mt][dt][e] = 0.f;
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            m[mt][r] = -INFINITY;
+            l[mt][r] = 0.f;
+            const int qi = mt * 16 + g8 + 8 * r;
+            // chunk-local bound of the keys row qi/4 sees (causal), 0 for padding rows
+            const int vis = st.keys - st.rows + (qi >> 2) + 1 - c0;
+            lim[mt][r] = qi < nq ? max(0, min(vis, nkeys)) : 0;
+        }
+    }
+    uint32_t qf[kQReg ? MT : 1][4][4];
+
+    for (int it = 0; it < nst; ++it) {
+        if (it + kStages - 1 < nst) issue(it + kStages - 1);
+        cp_async_commit();
+        cp_async_wait<kStages - 1>();
+        __syncthreads();
+        if (kQReg && it == 0) {
+#pragma unroll
+            for (int mt = 0; mt < (kQReg ? MT : 0); ++mt)
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const int mi = lane >> 3;
+                    const int row = mt * 16 + (mi & 1) * 8 + (lane & 7);
+                    ldsm_x4(qf[mt][ks], sQ32 + swz(row, ks * 2 + (mi >> 1)));
+                }
+        }
+        const int kw0 = it * kKT + warp * 16;   // chunk-local first key of this warp
+        if (kw0 < nkeys) {
+            const uint32_t bufK = sKV32 + (it % kStages) * kStageB;
+            const uint32_t bufV = bufK + kKT * kRowB;
+            uint32_t kb[4][4];
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+                const int mi = lane >> 3;
+                const int r = warp * 16 + (mi >> 1) * 8 + (lane & 7);
+                ldsm_x4(kb[ks], bufK + swz(r, ks * 2 + (mi & 1)));
+            }
+            uint32_t vb[8][2];
+#pragma unroll
+            for (int dp = 0; dp < 4; ++dp) {
+                const int mi = lane >> 3;
+                const int r = warp * 16 + (mi & 1) * 8 + (lane & 7);
+                uint32_t x[4];
+                ldsm_x4_t(x, bufV + swz(r, dp * 2 + (mi >> 1)));
+                vb[2 * dp][0] = bf2_to_h2(x[0]);
+                vb[2 * dp][1] = bf2_to_h2(x[1]);
+                vb[2 * dp + 1][0] = bf2_to_h2(x[2]);
+                vb[2 * dp + 1][1] = bf2_to_h2(x[3]);
+            }
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+                if (mt * 16 < nq) {
+                    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks) {
+                        uint32_t a[4];
+                        if (kQReg) {
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) a[k] = qf[kQReg ? mt : 0][ks][k];
+                        } else {
+                            const int mi = lane >> 3;
+                            const int row = mt * 16 + (mi & 1) * 8 + (lane & 7);
+                            ldsm_x4(a, sQ32 + swz(row, ks * 2 + (mi >> 1)));
+                        }
+                        mma_bf16(s[0], a, kb[ks][0], kb[ks][1]);
+                        mma_bf16(s[1], a, kb[ks][2], kb[ks][3]);
+                    }
+                    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int key = kw0 + nt * 8 + 2 * t4 + (e & 1);
+                            float x = s[nt][e] * kLog2e8;
+                            if (key >= lim[mt][e >> 1]) x = -INFINITY;
+                            s[nt][e] = x;
+                            mx[e >> 1] = fmaxf(mx[e >> 1], x);
+                        }
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], 1));
+                        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], 2));
+                    }
+                    float alpha[2], muse[2];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const float mn = fmaxf(m[mt][r], mx[r]);
+                        alpha[r] = (mn == -INFINITY) ? 1.f : ex2(m[mt][r] - mn);
+                        muse[r] = (mn == -INFINITY) ? 0.f : mn;
+                        m[mt][r] = mn;
+                    }
+                    float ps[2] = {0.f, 0.f};
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float p = ex2(s[nt][e] - muse[e >> 1]);
+                            s[nt][e] = p;
+                            ps[e >> 1] += p;
+                        }
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) l[mt][r] = l[mt][r] * alpha[r] + ps[r];
+#pragma unroll
+                    for (int dt = 0; dt < 8; ++dt) {
+                        o[mt][dt][0] *= alpha[0];
+                        o[mt][dt][1] *= alpha[0];
+                        o[mt][dt][2] *= alpha[1];
+                        o[mt][dt][3] *= alpha[1];
+                    }
+                    uint32_t pa[4];
+                    pa[0] = pack_h2(s[0][0], s[0][1]);
+                    pa[1] = pack_h2(s[0][2], s[0][3]);
+                    pa[2] = pack_h2(s[1][0], s[1][1]);
+                    pa[3] = pack_h2(s[1][2], s[1][3]);
+#pragma unroll
+                    for (int dt = 0; dt < 8; ++dt) mma_f16(o[mt][dt], pa, vb[dt][0], vb[dt][1]);
+                }
+            }
+        }
+        __syncthreads();
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // ---- combine the four warps (shared memory reused)
+    float* sO = reinterpret_cast<float*>(smem);                     // [4][16*MT][kOStride]
+    float* sM = sO + kWarps * 16 * MT * kOStride;                    // [4][16*MT]
+    float* sL = sM + kWarps * 16 * MT;                               // [4][16*MT]
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            float lr = l[mt][r];
+            lr += __shfl_xor_sync(0xFFFFFFFFu, lr, 1);
+            lr += __shfl_xor_sync(0xFFFFFFFFu, lr, 2);
+            const int qi = mt * 16 + g8 + 8 * r;
+            if (t4 == 0) {
+                sM[warp * 16 * MT + qi] = m[mt][r];
+                sL[warp * 16 * MT + qi] = lr;
+            }
+            float* row = sO + (size_t(warp) * 16 * MT + qi) * kOStride;
+#pragma unroll
+            for (int dt = 0; dt < 8; ++dt)
+                *reinterpret_cast<float2*>(row + dt * 8 + 2 * t4) =
+                    make_float2(o[mt][dt][2 * r], o[mt][dt][2 * r + 1]);
+        }
+    }
+    __syncthreads();
+    const int64_t rec0 = st.pbase + (int64_t(item.chunk) * TF_NKV + g) * nq;
+    for (int idx = tid; idx < nq * (TF_D / 4); idx += kThreads) {
+        const int qi = idx >> 4, d4 = (idx & 15) * 4;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sM[w * 16 * MT + qi]);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        float L = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float mw = sM[w * 16 * MT + qi];
+                const float wt = (mw == -INFINITY) ? 0.f : ex2(mw - M);
+                L += wt * sL[w * 16 * MT + qi];
+                const float4 v = *reinterpret_cast<const float4*>(sO + (size_t(w) * 16 * MT + qi) * kOStride + d4);
+                acc.x += wt * v.x;
+                acc.y += wt * v.y;
+                acc.z += wt * v.z;
+                acc.w += wt * v.w;
+            }
+        }
+        *reinterpret_cast<float4*>(part_o + (rec0 + qi) * TF_D + d4) = acc;
+        if (d4 == 0) part_ml[rec0 + qi] = make_float2(M, L);
+    }
+}
+
+constexpr int kMergeThreads = 256;
+
+__global__ void __launch_bounds__(kMergeThreads)
+attn_merge_kernel(SegTable t, const float* __restrict__ part_o, const float2* __restrict__ part_ml,
+                  float* __restrict__ out) {
+    const int row = blockIdx.x;
+    const int s = t.row_stream[row];
+    const SegStream st = t.streams[s];
+    const int i = row - st.row_offset;
+    const int nq = st.rows * 4;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t stride = int64_t(TF_NKV) * nq;   // records between chunks
+    for (int h = warp; h < TF_NQ; h += kMergeThreads / 32) {
+        const int g = h >> 2, hh = h & 3;
+        const int64_t base = st.pbase + int64_t(g) * nq + i * 4 + hh;
+        float M = -INFINITY;
+        for (int c = lane; c < st.n_chunks; c += 32) {
+            const float2 ml = part_ml[base + c * stride];
+            if (ml.y > 0.f) M = fmaxf(M, ml.x);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+        float2 acc = make_float2(0.f, 0.f);
+        float L = 0.f;
+        for (int c = 0; c < st.n_chunks; ++c) {
+            const int64_t rec = base + c * stride;
+            const float2 ml = part_ml[rec];
+            if (ml.y > 0.f) {
+                const float w = ex2(ml.x - M);
+                const float2 v = *reinterpret_cast<const float2*>(part_o + rec * TF_D + 2 * lane);
+                L += w * ml.y;
+                acc.x += w * v.x;
+                acc.y += w * v.y;
+            }
+        }
+        const float inv = 1.f / L;
+        *reinterpret_cast<float2*>(out + (size_t(row) * TF_NQ + h) * TF_D + 2 * lane) =
+            make_float2(acc.x * inv, acc.y * inv);
+    }
+}
+
+template <int MT>
+int prepare_one() {
+    cudaError_t e = cudaFuncSetAttribute(attn_partials_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         smem_bytes(MT));
+    return e == cudaSuccess ? TF_OK : cuda_fail(e);
+}
+
+}  // namespace
+
+int attn_prepare() {
+    int rc;
+    if ((rc = prepare_one<1>()) != TF_OK) return rc;
+    if ((rc = prepare_one<2>()) != TF_OK) return rc;
+    if ((rc = prepare_one<3>()) != TF_OK) return rc;
+    return prepare_one<4>();
+}
+
+}  // namespace tf
+
+extern "C" int tf_attn_partials(const tf_segments* seg, int attn_layer, const void* q, void* partials,
+                                tf_cuda_stream stream) {
+    using namespace tf;
+    if (!seg) return TF_EINVAL;
+    const SegTable& t = seg->dev;
+    if (attn_layer < 0 || attn_layer >= t.n_attn) return TF_EINVAL;
+    if (t.R == 0) return TF_OK;
+    if (!q || !partials || !aligned16(q) || !aligned16(partials)) return TF_EINVAL;
+    float* po = static_cast<float*>(partials);
+    float2* pml = reinterpret_cast<float2*>(po + t.n_partials * TF_D);
+    const int mt = (t.max_rows + 3) / 4;
+    const dim3 grid(t.n_items * TF_NKV);
+    const uint16_t* qq = static_cast<const uint16_t*>(q);
+    switch (mt) {
+        case 1: attn_partials_kernel<1><<<grid, kThreads, smem_bytes(1), stream>>>(t, attn_layer, qq, po, pml); break;
+        case 2: attn_partials_kernel<2><<<grid, kThreads, smem_bytes(2), stream>>>(t, attn_layer, qq, po, pml); break;
+        case 3: attn_partials_kernel<3><<<grid, kThreads, smem_bytes(3), stream>>>(t, attn_layer, qq, po, pml); break;
+        default: attn_partials_kernel<4><<<grid, kThreads, smem_bytes(4), stream>>>(t, attn_layer, qq, po, pml); break;
+    }
+    return launch_status();
+}
+
+extern "C" int tf_attn_merge(const tf_segments* seg, const void* partials, float* out, tf_cuda_stream stream) {
+    using namespace tf;
+    if (!seg) return TF_EINVAL;
+    const SegTable& t = seg->dev;
+    if (t.R == 0) return TF_OK;
+    if (!partials || !out || !aligned16(partials) || !aligned16(out)) return TF_EINVAL;
+    const float* po = static_cast<const float*>(partials);
+    const float2* pml = reinterpret_cast<const float2*>(po + t.n_partials * TF_D);
+    attn_merge_kernel<<<t.R, kMergeThreads, 0, stream>>>(t, po, pml, out);
+    return launch_status();
+}

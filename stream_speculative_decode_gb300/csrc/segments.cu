@@ -1,0 +1,288 @@
+// Segment table: host validation, sizing and the device copy.
+//
+// PR #1377 "LFM2: shared-round decode", commit "a shared round runs each
+// layer's conv and attention once over all its streams": the kernels run once
+// a layer over every row "from a table of the streams' cache addresses, row
+// offsets and key counts"; a stream of more than 8 rows is folded into 8-row
+// tiles; the attention partials hold each stream's apart. The same commit's
+// residency concern (a table reaching buffers nobody declared) becomes here a
+// host check that the table's buffers are valid, aligned and never overlap.
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "tf_internal.cuh"
+
+namespace tf {
+
+static thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = static_cast<int>(e);
+    return TF_ECUDA;
+}
+
+int sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 152;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+int attn_prepare();   // attn.cu: kernel attributes
+
+namespace {
+
+struct Interval {
+    uintptr_t lo, hi;
+};
+
+// True when two of the intervals overlap (empty intervals are ignored).
+bool any_overlap(std::vector<Interval>& v) {
+    std::sort(v.begin(), v.end(), [](const Interval& a, const Interval& b) { return a.lo < b.lo; });
+    for (size_t i = 1; i < v.size(); ++i)
+        if (v[i].lo < v[i - 1].hi) return true;
+    return false;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace
+}  // namespace tf
+
+extern "C" {
+
+int32_t tf_chunk_keys(int32_t rows) { return 256 * (rows < 1 ? 1 : rows); }
+
+int tf_segments_plan(const tf_stream* streams, int n_streams, tf_plan* out) {
+    if (!out) return TF_EINVAL;
+    std::memset(out, 0, sizeof(*out));
+    if (n_streams < 0) return TF_EINVAL;
+    if (n_streams > TF_MAX_STREAMS) return TF_ERANGE;
+    if (n_streams > 0 && !streams) return TF_EINVAL;
+    int64_t R = 0, parts = 0, items = 0, tiles = 0;
+    int max_rows = 0;
+    for (int s = 0; s < n_streams; ++s) {
+        const tf_stream& st = streams[s];
+        if (st.rows < 1 || st.keys < 1 || st.kv_capacity < 1) return TF_EINVAL;
+        if (st.rows > TF_MAX_ROWS || st.kv_capacity > TF_MAX_KEYS) return TF_ERANGE;
+        if (st.row_offset != R) return TF_EINVAL;          // packed, in order
+        if (st.keys < st.rows || st.keys > st.kv_capacity) return TF_EINVAL;
+        int64_t chunk = tf_chunk_keys(st.rows);
+        int64_t nch = (st.keys + chunk - 1) / chunk;
+        R += st.rows;
+        parts += int64_t(st.rows) * TF_NQ * nch;
+        items += nch;
+        tiles += (st.rows + tf::kConvTileRows - 1) / tf::kConvTileRows;
+        max_rows = std::max(max_rows, int(st.rows));
+    }
+    if (R > (1 << 24)) return TF_ERANGE;
+    out->n_streams = n_streams;
+    out->n_rows = int32_t(R);
+    out->max_rows = max_rows;
+    out->n_conv_tiles = int32_t(tiles);
+    out->n_attn_items = int32_t(items);
+    out->n_partials = parts;
+    out->partials_bytes = parts * TF_D * 4 + parts * 8;
+    return TF_OK;
+}
+
+int tf_segments_build(const tf_stream* streams, int n_streams,
+                      const void* const* conv_state, const void* const* conv_hist,
+                      const void* const* k_cache, const void* const* v_cache,
+                      int n_conv, int n_attn, tf_cuda_stream stream, tf_segments** out) {
+    using namespace tf;
+    if (!out) return TF_EINVAL;
+    *out = nullptr;
+    if (n_conv < 0 || n_attn < 0 || n_conv > 4096 || n_attn > 4096) return TF_EINVAL;
+    tf_plan plan;
+    int rc = tf_segments_plan(streams, n_streams, &plan);
+    if (rc != TF_OK) return rc;
+    const int S = n_streams;
+    if (S > 0 && n_conv > 0 && !conv_state) return TF_EINVAL;
+    if (S > 0 && n_attn > 0 && (!k_cache || !v_cache)) return TF_EINVAL;
+
+    // ---- pointer checks: non-null, 16-byte aligned, no two buffers overlap
+    std::vector<Interval> conv_iv, kv_iv;
+    for (int l = 0; l < n_conv; ++l) {
+        for (int s = 0; s < S; ++s) {
+            const void* p = conv_state[size_t(l) * S + s];
+            if (!p || !aligned16(p)) return TF_EINVAL;
+            uintptr_t a = reinterpret_cast<uintptr_t>(p);
+            conv_iv.push_back({a, a + size_t(2) * TF_H * 2});
+            if (conv_hist) {
+                const void* h = conv_hist[size_t(l) * S + s];
+                if (!h) {
+                    if (streams[s].rows > 1) return TF_EINVAL;
+                    continue;
+                }
+                if (!aligned16(h)) return TF_EINVAL;
+                uintptr_t b = reinterpret_cast<uintptr_t>(h);
+                conv_iv.push_back({b, b + size_t(streams[s].rows + 2) * TF_H * 2});
+            }
+        }
+    }
+    for (int l = 0; l < n_attn; ++l) {
+        for (int s = 0; s < S; ++s) {
+            const void* k = k_cache[size_t(l) * S + s];
+            const void* v = v_cache[size_t(l) * S + s];
+            if (!k || !v || !aligned16(k) || !aligned16(v)) return TF_EINVAL;
+            size_t bytes = size_t(TF_NKV) * streams[s].kv_capacity * TF_D * 2;
+            uintptr_t a = reinterpret_cast<uintptr_t>(k), b = reinterpret_cast<uintptr_t>(v);
+            kv_iv.push_back({a, a + bytes});
+            kv_iv.push_back({b, b + bytes});
+        }
+    }
+    if (any_overlap(conv_iv) || any_overlap(kv_iv)) return TF_EINVAL;
+
+    tf_segments* seg = new (std::nothrow) tf_segments();
+    if (!seg) return TF_ENOMEM;
+    seg->plan = plan;
+    const int R = plan.n_rows;
+
+    // ---- host image: streams | row_stream | tiles | items | pointer arrays
+    std::vector<SegStream> ss(S);
+    std::vector<int32_t> row_stream(R);
+    std::vector<ConvTile> tiles;
+    std::vector<AttnItem> items;
+    int64_t pbase = 0;
+    for (int s = 0; s < S; ++s) {
+        const tf_stream& st = streams[s];
+        SegStream& d = ss[s];
+        d.rows = st.rows;
+        d.row_offset = st.row_offset;
+        d.keys = st.keys;
+        d.cap = st.kv_capacity;
+        d.chunk_keys = tf_chunk_keys(st.rows);
+        d.n_chunks = (st.keys + d.chunk_keys - 1) / d.chunk_keys;
+        d.pbase = pbase;
+        pbase += int64_t(st.rows) * TF_NQ * d.n_chunks;
+        for (int i = 0; i < st.rows; ++i) row_stream[st.row_offset + i] = s;
+        for (int r0 = 0; r0 < st.rows; r0 += kConvTileRows)
+            tiles.push_back({s, r0, std::min(kConvTileRows, st.rows - r0), 0});
+        for (int c = 0; c < d.n_chunks; ++c) items.push_back({s, c});
+    }
+    // largest chunks first, so the long work starts early in the grid
+    std::stable_sort(items.begin(), items.end(), [&](const AttnItem& a, const AttnItem& b) {
+        auto len = [&](const AttnItem& it) {
+            const SegStream& d = ss[it.stream];
+            int lo = it.chunk * d.chunk_keys;
+            int len_keys = std::min(d.keys, lo + d.chunk_keys) - lo;
+            return int64_t(len_keys) * ((d.rows + 3) / 4 + 1);
+        };
+        return len(a) > len(b);
+    });
+
+    size_t off = 0;
+    const size_t o_streams = off;  off = align_up(off + sizeof(SegStream) * S, 256);
+    const size_t o_rows = off;     off = align_up(off + sizeof(int32_t) * R, 256);
+    const size_t o_tiles = off;    off = align_up(off + sizeof(ConvTile) * tiles.size(), 256);
+    const size_t o_items = off;    off = align_up(off + sizeof(AttnItem) * items.size(), 256);
+    const size_t n_cp = size_t(n_conv) * S, n_ap = size_t(n_attn) * S;
+    const size_t o_cs = off;       off = align_up(off + sizeof(void*) * n_cp, 256);
+    const size_t o_ch = off;       off = align_up(off + (conv_hist ? sizeof(void*) * n_cp : 0), 256);
+    const size_t o_k = off;        off = align_up(off + sizeof(void*) * n_ap, 256);
+    const size_t o_v = off;        off = align_up(off + sizeof(void*) * n_ap, 256);
+    const size_t total = off;
+
+    seg->host.assign(total, 0);
+    unsigned char* h = seg->host.data();
+    if (S) std::memcpy(h + o_streams, ss.data(), sizeof(SegStream) * S);
+    if (R) std::memcpy(h + o_rows, row_stream.data(), sizeof(int32_t) * R);
+    if (!tiles.empty()) std::memcpy(h + o_tiles, tiles.data(), sizeof(ConvTile) * tiles.size());
+    if (!items.empty()) std::memcpy(h + o_items, items.data(), sizeof(AttnItem) * items.size());
+    if (n_cp) std::memcpy(h + o_cs, conv_state, sizeof(void*) * n_cp);
+    if (n_cp && conv_hist) std::memcpy(h + o_ch, conv_hist, sizeof(void*) * n_cp);
+    if (n_ap) {
+        std::memcpy(h + o_k, k_cache, sizeof(void*) * n_ap);
+        std::memcpy(h + o_v, v_cache, sizeof(void*) * n_ap);
+    }
+    seg->streams = ss;
+
+    SegTable& t = seg->dev;
+    std::memset(&t, 0, sizeof(t));
+    t.S = S;
+    t.R = R;
+    t.n_tiles = int32_t(tiles.size());
+    t.n_items = int32_t(items.size());
+    t.n_conv = n_conv;
+    t.n_attn = n_attn;
+    t.max_rows = plan.max_rows;
+    t.has_hist = conv_hist ? 1 : 0;
+    t.n_partials = plan.n_partials;
+
+    if (total > 0 && S > 0) {
+        cudaError_t e = cudaMalloc(&seg->blob, total);
+        if (e != cudaSuccess) {
+            delete seg;
+            cuda_fail(e);
+            return e == cudaErrorMemoryAllocation ? TF_ENOMEM : TF_ECUDA;
+        }
+        e = cudaMemcpyAsync(seg->blob, h, total, cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) {
+            cudaFree(seg->blob);
+            delete seg;
+            return cuda_fail(e);
+        }
+        unsigned char* b = static_cast<unsigned char*>(seg->blob);
+        t.streams = reinterpret_cast<const SegStream*>(b + o_streams);
+        t.row_stream = reinterpret_cast<const int32_t*>(b + o_rows);
+        t.tiles = reinterpret_cast<const ConvTile*>(b + o_tiles);
+        t.items = reinterpret_cast<const AttnItem*>(b + o_items);
+        t.conv_state = reinterpret_cast<void* const*>(b + o_cs);
+        t.conv_hist = conv_hist ? reinterpret_cast<void* const*>(b + o_ch) : nullptr;
+        t.k_cache = reinterpret_cast<const void* const*>(b + o_k);
+        t.v_cache = reinterpret_cast<const void* const*>(b + o_v);
+        rc = attn_prepare();
+        if (rc != TF_OK) {
+            cudaFree(seg->blob);
+            delete seg;
+            return rc;
+        }
+    }
+    *out = seg;
+    return TF_OK;
+}
+
+int tf_segments_free(tf_segments* seg) {
+    if (!seg) return TF_OK;
+    int rc = TF_OK;
+    if (seg->blob) {
+        cudaError_t e = cudaFree(seg->blob);
+        if (e != cudaSuccess) rc = tf::cuda_fail(e);
+    }
+    delete seg;
+    return rc;
+}
+
+int tf_segments_query(const tf_segments* seg, tf_plan* out) {
+    if (!seg || !out) return TF_EINVAL;
+    *out = seg->plan;
+    return TF_OK;
+}
+
+size_t tf_partials_bytes(const tf_segments* seg) {
+    return seg ? size_t(seg->plan.partials_bytes) : 0;
+}
+
+const char* tf_strerror(int status) {
+    switch (status) {
+        case TF_OK: return "TF_OK: success";
+        case TF_EINVAL: return "TF_EINVAL: invalid argument (null, shape, packing, alignment or aliasing)";
+        case TF_ERANGE: return "TF_ERANGE: size out of the supported range";
+        case TF_ENOMEM: return "TF_ENOMEM: device allocation of the segment table failed";
+        case TF_ECUDA: return "TF_ECUDA: a CUDA call or kernel launch failed";
+        default: return "unknown tf status";
+    }
+}
+
+int tf_last_cuda_error(void) { return tf::g_last_cuda_error; }
+
+}  // extern "C"

@@ -1,0 +1,219 @@
+"""Python binding of libtf.so, the segmented speculative-verify step for GB300.
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels. Functions carry the C names. Tensor arguments may be torch tensors
+(their device pointers are passed) or integer device addresses. Importing this
+package without a built ``libtf.so`` raises ImportError: there is no fallback.
+
+Build the library with ``python -m stream_speculative_decode_gb300.build`` (or
+``__graft_entry__.build()``).
+"""
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libtf.so")
+
+TF_H, TF_CIN, TF_KW, TF_NQ, TF_NKV, TF_D = 2048, 6144, 3, 32, 8, 64
+TF_MAX_ROWS = 16
+TF_OK, TF_EINVAL, TF_ERANGE, TF_ENOMEM, TF_ECUDA = 0, 1, 2, 3, 4
+
+# every symbol include/tf.h declares
+EXPORTS = ("tf_chunk_keys", "tf_segments_plan", "tf_segments_build", "tf_segments_free",
+           "tf_segments_query", "tf_partials_bytes", "tf_conv_rows", "tf_attn_partials",
+           "tf_attn_merge", "tf_argmax_rows", "tf_accept", "tf_strerror", "tf_last_cuda_error")
+
+
+class TFError(RuntimeError):
+    def __init__(self, fn, status):
+        msg = _lib.tf_strerror(status).decode()
+        if status == TF_ECUDA:
+            msg += f" (cudaError {_lib.tf_last_cuda_error()})"
+        super().__init__(f"{fn}: {msg}")
+        self.status = status
+
+
+class tf_stream(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int32), ("row_offset", ctypes.c_int32),
+                ("keys", ctypes.c_int32), ("kv_capacity", ctypes.c_int32)]
+
+
+class tf_plan(ctypes.Structure):
+    _fields_ = [("n_streams", ctypes.c_int32), ("n_rows", ctypes.c_int32),
+                ("max_rows", ctypes.c_int32), ("n_conv_tiles", ctypes.c_int32),
+                ("n_attn_items", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("n_partials", ctypes.c_int64), ("partials_bytes", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_ if f != "reserved"}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libtf.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    P = ctypes.POINTER
+    sig = {
+        "tf_chunk_keys": (ctypes.c_int32, [ctypes.c_int32]),
+        "tf_segments_plan": (i32, [P(tf_stream), i32, P(tf_plan)]),
+        "tf_segments_build": (i32, [P(tf_stream), i32, P(vp), P(vp), P(vp), P(vp), i32, i32, vp, P(vp)]),
+        "tf_segments_free": (i32, [vp]),
+        "tf_segments_query": (i32, [vp, P(tf_plan)]),
+        "tf_partials_bytes": (sz, [vp]),
+        "tf_conv_rows": (i32, [vp, i32, vp, vp, vp, vp]),
+        "tf_attn_partials": (i32, [vp, i32, vp, vp, vp]),
+        "tf_attn_merge": (i32, [vp, vp, vp, vp]),
+        "tf_argmax_rows": (i32, [vp, i32, i32, i64, vp, vp, vp]),
+        "tf_accept": (i32, [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, vp]),
+        "tf_strerror": (ctypes.c_char_p, [i32]),
+        "tf_last_cuda_error": (i32, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def lib():
+    """The loaded ctypes library."""
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(fn, rc):
+    if rc != TF_OK:
+        raise TFError(fn, rc)
+
+
+def _streams_array(streams):
+    arr = (tf_stream * max(len(streams), 1))()
+    for i, st in enumerate(streams):
+        rows, off, keys, cap = st
+        arr[i] = tf_stream(rows, off, keys, cap)
+    return arr
+
+
+def tf_chunk_keys(rows):
+    return _lib.tf_chunk_keys(rows)
+
+
+def tf_segments_plan(streams):
+    """Host-only sizes of a table; ``streams`` = [(rows, row_offset, keys, cap)]."""
+    plan = tf_plan()
+    _check("tf_segments_plan", _lib.tf_segments_plan(_streams_array(streams), len(streams), ctypes.byref(plan)))
+    return plan.as_dict()
+
+
+def tf_segments_plan_status(streams):
+    """The raw status of tf_segments_plan (for refusal tests)."""
+    plan = tf_plan()
+    return _lib.tf_segments_plan(_streams_array(streams), len(streams), ctypes.byref(plan))
+
+
+class Segments:
+    """Owner of a tf_segments handle."""
+
+    def __init__(self, handle):
+        self.handle = handle
+        plan = tf_plan()
+        _check("tf_segments_query", _lib.tf_segments_query(handle, ctypes.byref(plan)))
+        self.plan = plan.as_dict()
+        self.partials_bytes = int(_lib.tf_partials_bytes(handle))
+
+    def free(self):
+        if self.handle:
+            _check("tf_segments_free", _lib.tf_segments_free(self.handle))
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+def _ptr_array(ptrs):
+    if ptrs is None:
+        return None
+    arr = (ctypes.c_void_p * max(len(ptrs), 1))()
+    for i, p in enumerate(ptrs):
+        arr[i] = _ptr(p)
+    return arr
+
+
+def tf_segments_build_status(streams, conv_state, conv_hist, k_cache, v_cache, n_conv, n_attn, stream=None):
+    """Raw status and handle of tf_segments_build; pointer lists are flat [layer][stream]."""
+    out = ctypes.c_void_p()
+    rc = _lib.tf_segments_build(_streams_array(streams), len(streams), _ptr_array(conv_state),
+                                _ptr_array(conv_hist), _ptr_array(k_cache), _ptr_array(v_cache),
+                                n_conv, n_attn, _stream(stream), ctypes.byref(out))
+    return rc, out.value
+
+
+def tf_segments_build(streams, conv_state, conv_hist, k_cache, v_cache, n_conv, n_attn, stream=None):
+    rc, handle = tf_segments_build_status(streams, conv_state, conv_hist, k_cache, v_cache,
+                                          n_conv, n_attn, stream)
+    _check("tf_segments_build", rc)
+    return Segments(handle)
+
+
+def tf_segments_free(seg):
+    seg.free()
+
+
+def tf_partials_bytes(seg):
+    return int(_lib.tf_partials_bytes(seg.handle if isinstance(seg, Segments) else seg))
+
+
+def _h(seg):
+    return seg.handle if isinstance(seg, Segments) else seg
+
+
+def tf_conv_rows(seg, conv_layer, bcx, w, y, stream=None):
+    _check("tf_conv_rows", _lib.tf_conv_rows(_h(seg), conv_layer, _ptr(bcx), _ptr(w), _ptr(y), _stream(stream)))
+
+
+def tf_attn_partials(seg, attn_layer, q, partials, stream=None):
+    _check("tf_attn_partials", _lib.tf_attn_partials(_h(seg), attn_layer, _ptr(q), _ptr(partials), _stream(stream)))
+
+
+def tf_attn_merge(seg, partials, out, stream=None):
+    _check("tf_attn_merge", _lib.tf_attn_merge(_h(seg), _ptr(partials), _ptr(out), _stream(stream)))
+
+
+def tf_argmax_rows(logits, R, V, row_stride, pick, flag, stream=None):
+    _check("tf_argmax_rows", _lib.tf_argmax_rows(_ptr(logits), R, V, row_stride, _ptr(pick), _ptr(flag),
+                                                 _stream(stream)))
+
+
+def tf_accept(seg, ids, pick, flag, vocab, accept_len, next_token, new_keys, sflag, rewind_conv=True,
+              stream=None):
+    _check("tf_accept", _lib.tf_accept(_h(seg), _ptr(ids), _ptr(pick), _ptr(flag), vocab, _ptr(accept_len),
+                                       _ptr(next_token), _ptr(new_keys), _ptr(sflag), 1 if rewind_conv else 0,
+                                       _stream(stream)))
+
+
+def tf_strerror(status):
+    return _lib.tf_strerror(status).decode()
