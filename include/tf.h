@@ -178,6 +178,25 @@ int tf_attn_partials(const tf_segments* seg, int attn_layer, const void* q,
 int tf_attn_merge(const tf_segments* seg, const void* partials, float* out,
                   tf_cuda_stream stream);
 
+/* Attention of one layer (tf_attn_partials then tf_attn_merge) that allocates
+ * nothing: the partial scratch is a fixed array of TF_STATIC_SCRATCH_BYTES
+ * compiled into the library (no counterpart on the pages; it exists for
+ * callers that cannot call cudaMalloc or any allocating routine, such as code
+ * under a strict memory budget or an allocator it does not own).
+ *   q    bf16 [R][TF_NQ][TF_D], out float [R][TF_NQ][TF_D], as above.
+ * Every GPU that loads the library holds the array until the process exits.
+ * The first call on a device looks the array's device address up (with that
+ * device current); make that first call before any stream capture. Calls
+ * share the one array: calls whose launches overlap on the GPU (different
+ * streams at once) race and give wrong results. Nothing in the array has to
+ * start at zero; each call writes every record it reads.
+ * Errors: TF_ERANGE when tf_partials_bytes(seg) > TF_STATIC_SCRATCH_BYTES
+ * (nothing is launched), TF_EINVAL as tf_attn_partials. Calls no cudaMalloc,
+ * cudaFree or other allocating routine. */
+#define TF_STATIC_SCRATCH_BYTES (16u << 20)
+int tf_attn_static(const tf_segments* seg, int attn_layer, const void* q, float* out,
+                   tf_cuda_stream stream);
+
 /* a4. Greedy pick of each row of bf16 logits ([SRD] lfm2_argmax: "the first
  * largest logit ... ties to the lower id, nonfinite rows flagged").
  *   logits      bf16, row r at logits + r*row_stride (elements), V per row

@@ -376,6 +376,26 @@ int attn_prepare() {
     return prepare_one<4>();
 }
 
+// Launchers for other translation units: the partials and the merge of one
+// attention layer with the partial records at `po` (o) and `pml` (m, l).
+int launch_attn_partials(const SegTable& t, int layer, const uint16_t* q, float* po, float2* pml,
+                         cudaStream_t stream) {
+    const int mt = (t.max_rows + 3) / 4;
+    const dim3 grid(t.n_items * TF_NKV);
+    switch (mt) {
+        case 1: attn_partials_kernel<1><<<grid, kThreads, smem_bytes(1), stream>>>(t, layer, q, po, pml); break;
+        case 2: attn_partials_kernel<2><<<grid, kThreads, smem_bytes(2), stream>>>(t, layer, q, po, pml); break;
+        case 3: attn_partials_kernel<3><<<grid, kThreads, smem_bytes(3), stream>>>(t, layer, q, po, pml); break;
+        default: attn_partials_kernel<4><<<grid, kThreads, smem_bytes(4), stream>>>(t, layer, q, po, pml); break;
+    }
+    return launch_status();
+}
+
+int launch_attn_merge(const SegTable& t, const float* po, const float2* pml, float* out, cudaStream_t stream) {
+    attn_merge_kernel<<<t.R, kMergeThreads, 0, stream>>>(t, po, pml, out);
+    return launch_status();
+}
+
 }  // namespace tf
 
 extern "C" int tf_attn_partials(const tf_segments* seg, int attn_layer, const void* q, void* partials,

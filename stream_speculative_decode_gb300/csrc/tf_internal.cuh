@@ -72,4 +72,9 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// attn.cu: one attention layer's partials and merge with the records at po/pml.
+int launch_attn_partials(const SegTable& t, int layer, const uint16_t* q, float* po, float2* pml,
+                         cudaStream_t stream);
+int launch_attn_merge(const SegTable& t, const float* po, const float2* pml, float* out, cudaStream_t stream);
+
 }  // namespace tf

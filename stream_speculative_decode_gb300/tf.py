@@ -22,7 +22,9 @@ TF_OK, TF_EINVAL, TF_ERANGE, TF_ENOMEM, TF_ECUDA = 0, 1, 2, 3, 4
 # every symbol include/tf.h declares
 EXPORTS = ("tf_chunk_keys", "tf_segments_plan", "tf_segments_build", "tf_segments_free",
            "tf_segments_query", "tf_partials_bytes", "tf_conv_rows", "tf_attn_partials",
-           "tf_attn_merge", "tf_argmax_rows", "tf_accept", "tf_strerror", "tf_last_cuda_error")
+           "tf_attn_merge", "tf_attn_static", "tf_argmax_rows", "tf_accept", "tf_strerror",
+           "tf_last_cuda_error")
+TF_STATIC_SCRATCH_BYTES = 16 << 20
 
 
 class TFError(RuntimeError):
@@ -65,6 +67,7 @@ def _load():
         "tf_conv_rows": (i32, [vp, i32, vp, vp, vp, vp]),
         "tf_attn_partials": (i32, [vp, i32, vp, vp, vp]),
         "tf_attn_merge": (i32, [vp, vp, vp, vp]),
+        "tf_attn_static": (i32, [vp, i32, vp, vp, vp]),
         "tf_argmax_rows": (i32, [vp, i32, i32, i64, vp, vp, vp]),
         "tf_accept": (i32, [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, vp]),
         "tf_strerror": (ctypes.c_char_p, [i32]),
@@ -201,6 +204,12 @@ def tf_attn_partials(seg, attn_layer, q, partials, stream=None):
 
 def tf_attn_merge(seg, partials, out, stream=None):
     _check("tf_attn_merge", _lib.tf_attn_merge(_h(seg), _ptr(partials), _ptr(out), _stream(stream)))
+
+
+def tf_attn_static(seg, attn_layer, q, out, stream=None):
+    """One attention layer with the library's fixed partial scratch (allocates
+    nothing; see include/tf.h)."""
+    _check("tf_attn_static", _lib.tf_attn_static(_h(seg), attn_layer, _ptr(q), _ptr(out), _stream(stream)))
 
 
 def tf_argmax_rows(logits, R, V, row_stride, pick, flag, stream=None):
