@@ -35,6 +35,7 @@ constexpr int kRowB = TF_D * 2;         // 128 bytes per cache row
 constexpr int kStageB = 2 * kKT * kRowB;  // K then V: 16 KB
 constexpr int kOStride = 68;            // floats per row of the warp-combine buffer
 constexpr float kLog2e8 = 0.18033688011112042f;   // log2(e) / sqrt(64)
+constexpr float kTau = 8.f;             // lazy-rescale threshold, log2 units
 
 __host__ __device__ constexpr int smem_bytes(int mt) { return kStages * kStageB + 16 * mt * kRowB; }
 
@@ -135,8 +136,9 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
 
     const int g8 = lane >> 2, t4 = lane & 3;
     float o[MT][8][4];
-    float m[MT][2], l[MT][2];
+    float m[MT][2], l[MT][2], mtrue[MT][2];   // m: reference max; mtrue: running max
     int lim[MT][2];
+    const int lim_all = st.keys - st.rows + 1 - c0;   // keys every real row sees (chunk-local)
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
@@ -146,6 +148,7 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             m[mt][r] = -INFINITY;
+            mtrue[mt][r] = -INFINITY;
             l[mt][r] = 0.f;
             const int qi = mt * 16 + g8 + 8 * r;
             // chunk-local bound of the keys row qi/4 sees (causal), 0 for padding rows
@@ -211,48 +214,64 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
                         mma_bf16(s[0], a, kb[ks][0], kb[ks][1]);
                         mma_bf16(s[1], a, kb[ks][2], kb[ks][3]);
                     }
+                    // scores of row 0 and every later row are all visible up to
+                    // lim_all; past it (the causal edge, the chunk's end) mask
+                    if (kw0 + 16 > lim_all) {
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int key = kw0 + nt * 8 + 2 * t4 + (e & 1);
+                                if (key >= lim[mt][e >> 1]) s[nt][e] = -INFINITY;
+                            }
+                    }
                     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int key = kw0 + nt * 8 + 2 * t4 + (e & 1);
-                            float x = s[nt][e] * kLog2e8;
-                            if (key >= lim[mt][e >> 1]) x = -INFINITY;
-                            s[nt][e] = x;
-                            mx[e >> 1] = fmaxf(mx[e >> 1], x);
-                        }
+                        for (int e = 0; e < 4; ++e) mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
                         mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], 1));
                         mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], 2));
                     }
-                    float alpha[2], muse[2];
+                    // lazy rescale: the reference max moves only when a row's max
+                    // rises more than kTau (log2 units) above it, so p <= 2^kTau
+                    float alpha[2] = {1.f, 1.f}, muse[2];
+                    bool resc = false;
 #pragma unroll
                     for (int r = 0; r < 2; ++r) {
-                        const float mn = fmaxf(m[mt][r], mx[r]);
-                        alpha[r] = (mn == -INFINITY) ? 1.f : ex2(m[mt][r] - mn);
-                        muse[r] = (mn == -INFINITY) ? 0.f : mn;
-                        m[mt][r] = mn;
+                        const float mxs = mx[r] * kLog2e8;
+                        mtrue[mt][r] = fmaxf(mtrue[mt][r], mxs);
+                        if (mxs > m[mt][r] + kTau) {
+                            alpha[r] = ex2(m[mt][r] - mxs);
+                            m[mt][r] = mxs;
+                            resc = true;
+                        }
+                        muse[r] = (m[mt][r] == -INFINITY) ? 0.f : m[mt][r];
+                    }
+                    if (__any_sync(0xFFFFFFFFu, resc)) {
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) l[mt][r] *= alpha[r];
+#pragma unroll
+                        for (int dt = 0; dt < 8; ++dt) {
+                            o[mt][dt][0] *= alpha[0];
+                            o[mt][dt][1] *= alpha[0];
+                            o[mt][dt][2] *= alpha[1];
+                            o[mt][dt][3] *= alpha[1];
+                        }
                     }
                     float ps[2] = {0.f, 0.f};
 #pragma unroll
                     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const float p = ex2(s[nt][e] - muse[e >> 1]);
+                            const float p = ex2(fmaf(s[nt][e], kLog2e8, -muse[e >> 1]));
                             s[nt][e] = p;
                             ps[e >> 1] += p;
                         }
 #pragma unroll
-                    for (int r = 0; r < 2; ++r) l[mt][r] = l[mt][r] * alpha[r] + ps[r];
-#pragma unroll
-                    for (int dt = 0; dt < 8; ++dt) {
-                        o[mt][dt][0] *= alpha[0];
-                        o[mt][dt][1] *= alpha[0];
-                        o[mt][dt][2] *= alpha[1];
-                        o[mt][dt][3] *= alpha[1];
-                    }
+                    for (int r = 0; r < 2; ++r) l[mt][r] += ps[r];
                     uint32_t pa[4];
                     pa[0] = pack_h2(s[0][0], s[0][1]);
                     pa[1] = pack_h2(s[0][2], s[0][3]);
@@ -267,6 +286,23 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
     }
     cp_async_wait<0>();
     __syncthreads();
+
+    // renormalise each row to its true running max (exact partial format)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            if (mtrue[mt][r] > m[mt][r]) {
+                const float f = ex2(m[mt][r] - mtrue[mt][r]);
+                l[mt][r] *= f;
+#pragma unroll
+                for (int dt = 0; dt < 8; ++dt) {
+                    o[mt][dt][2 * r] *= f;
+                    o[mt][dt][2 * r + 1] *= f;
+                }
+            }
+            m[mt][r] = mtrue[mt][r];
+        }
 
     // ---- combine the four warps (shared memory reused)
     float* sO = reinterpret_cast<float*>(smem);                     // [4][16*MT][kOStride]
@@ -318,45 +354,72 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
     }
 }
 
-constexpr int kMergeThreads = 256;
+constexpr int kMergeWarps = 8;
+constexpr int kMergeThreads = kMergeWarps * 32;
+constexpr int kMergeUnroll = 8;
 
+// One warp per (row, query head); a CTA covers 8 heads of one row. Lanes read
+// the chunks' (m, l) in parallel; the o records are then read kMergeUnroll at a
+// time with independent loads, lane j holding dimensions 2j and 2j+1.
 __global__ void __launch_bounds__(kMergeThreads)
 attn_merge_kernel(SegTable t, const float* __restrict__ part_o, const float2* __restrict__ part_ml,
                   float* __restrict__ out) {
-    const int row = blockIdx.x;
+    const int row = blockIdx.x >> 2;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int h = (blockIdx.x & 3) * kMergeWarps + warp;
     const int s = t.row_stream[row];
     const SegStream st = t.streams[s];
     const int i = row - st.row_offset;
     const int nq = st.rows * 4;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = h >> 2, hh = h & 3;
     const int64_t stride = int64_t(TF_NKV) * nq;   // records between chunks
-    for (int h = warp; h < TF_NQ; h += kMergeThreads / 32) {
-        const int g = h >> 2, hh = h & 3;
-        const int64_t base = st.pbase + int64_t(g) * nq + i * 4 + hh;
-        float M = -INFINITY;
-        for (int c = lane; c < st.n_chunks; c += 32) {
-            const float2 ml = part_ml[base + c * stride];
-            if (ml.y > 0.f) M = fmaxf(M, ml.x);
-        }
+    const int64_t base = st.pbase + int64_t(g) * nq + i * 4 + hh;
+    const int C = st.n_chunks;
+
+    float M = -INFINITY;
+    for (int c = lane; c < C; c += 32) {
+        const float2 ml = part_ml[base + c * stride];
+        if (ml.y > 0.f) M = fmaxf(M, ml.x);
+    }
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-        float2 acc = make_float2(0.f, 0.f);
-        float L = 0.f;
-        for (int c = 0; c < st.n_chunks; ++c) {
-            const int64_t rec = base + c * stride;
-            const float2 ml = part_ml[rec];
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+
+    float2 acc = make_float2(0.f, 0.f);
+    float lsum = 0.f;
+    for (int c0 = 0; c0 < C; c0 += 32) {
+        float wj = 0.f;
+        if (c0 + lane < C) {
+            const float2 ml = part_ml[base + (c0 + lane) * stride];
             if (ml.y > 0.f) {
-                const float w = ex2(ml.x - M);
-                const float2 v = *reinterpret_cast<const float2*>(part_o + rec * TF_D + 2 * lane);
-                L += w * ml.y;
-                acc.x += w * v.x;
-                acc.y += w * v.y;
+                wj = ex2(ml.x - M);
+                lsum += wj * ml.y;
             }
         }
-        const float inv = 1.f / L;
-        *reinterpret_cast<float2*>(out + (size_t(row) * TF_NQ + h) * TF_D + 2 * lane) =
-            make_float2(acc.x * inv, acc.y * inv);
+        const int n = min(32, C - c0);
+        for (int j = 0; j < n; j += kMergeUnroll) {
+            float2 v[kMergeUnroll];
+            float wk[kMergeUnroll];
+#pragma unroll
+            for (int k = 0; k < kMergeUnroll; ++k) {
+                wk[k] = __shfl_sync(0xFFFFFFFFu, wj, (j + k) & 31);
+                v[k] = make_float2(0.f, 0.f);
+                if (j + k < n)
+                    v[k] = *reinterpret_cast<const float2*>(part_o + (base + (c0 + j + k) * stride) * TF_D + 2 * lane);
+            }
+#pragma unroll
+            for (int k = 0; k < kMergeUnroll; ++k) {
+                if (j + k < n) {
+                    acc.x += wk[k] * v[k].x;
+                    acc.y += wk[k] * v[k].y;
+                }
+            }
+        }
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
+    const float inv = 1.f / lsum;
+    *reinterpret_cast<float2*>(out + (size_t(row) * TF_NQ + h) * TF_D + 2 * lane) =
+        make_float2(acc.x * inv, acc.y * inv);
 }
 
 template <int MT>
@@ -392,7 +455,7 @@ int launch_attn_partials(const SegTable& t, int layer, const uint16_t* q, float*
 }
 
 int launch_attn_merge(const SegTable& t, const float* po, const float2* pml, float* out, cudaStream_t stream) {
-    attn_merge_kernel<<<t.R, kMergeThreads, 0, stream>>>(t, po, pml, out);
+    attn_merge_kernel<<<t.R * 4, kMergeThreads, 0, stream>>>(t, po, pml, out);
     return launch_status();
 }
 
@@ -428,6 +491,6 @@ extern "C" int tf_attn_merge(const tf_segments* seg, const void* partials, float
     if (!partials || !out || !aligned16(partials) || !aligned16(out)) return TF_EINVAL;
     const float* po = static_cast<const float*>(partials);
     const float2* pml = reinterpret_cast<const float2*>(po + t.n_partials * TF_D);
-    attn_merge_kernel<<<t.R, kMergeThreads, 0, stream>>>(t, po, pml, out);
+    attn_merge_kernel<<<t.R * 4, kMergeThreads, 0, stream>>>(t, po, pml, out);
     return launch_status();
 }
