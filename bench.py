@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--impl", default="tf", choices=["tf", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--conv-layers", type=int, default=None, help="override (small profiling runs)")
+    ap.add_argument("--attn-layers", type=int, default=None, help="override (small profiling runs)")
     return ap.parse_args()
 
 
@@ -159,9 +161,12 @@ def measured_peaks():
 
 
 def kernel_source_hash():
+    """Hash of the attention kernels' sources (a recorded ncu traffic figure is
+    reported only while it matches)."""
     h = hashlib.sha256()
-    with open(os.path.join(ROOT, "stream_speculative_decode_gb300", "csrc", "attn.cu"), "rb") as f:
-        h.update(f.read())
+    for name in ("attn.cu", "attn_tc.cu", "tf_internal.cuh"):
+        with open(os.path.join(ROOT, "stream_speculative_decode_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
@@ -290,7 +295,7 @@ def run_tf(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
     torch.cuda.set_device(dev)
     dist_init(world, "nccl")
-    w = I.workload(args.workload)
+    w = I.workload(args.workload, n_conv=args.conv_layers, n_attn=args.attn_layers)
     inp = I.make_inputs(w, backend="torch", device=dev)
     d = DeviceStep(inp, device=dev)
     ab = algorithmic_bytes(inp.streams, w.n_conv, w.n_attn, w.vocab)
@@ -298,7 +303,7 @@ def run_tf(args, rank, world):
 
     # per-launch timing of the dominant kernel, recorded inside the graph
     try:
-        evs = {"attn_partials": [(torch.cuda.Event(enable_timing=True, external=True),
+        evs = {"attn": [(torch.cuda.Event(enable_timing=True, external=True),
                                   torch.cuda.Event(enable_timing=True, external=True))
                                  for _ in range(w.n_attn)]}
         graph_events = True
@@ -330,7 +335,7 @@ def run_tf(args, rank, world):
         ev[k][1].record(stream)
         if graph_events:                    # read this replay's per-launch events
             ev[k][1].synchronize()
-            part_ms.extend(a.elapsed_time(b) for a, b in evs["attn_partials"])
+            part_ms.extend(a.elapsed_time(b) for a, b in evs["attn"])
     torch.cuda.synchronize()
     t_wall1 = time.time()
     dist_barrier(world)
@@ -346,14 +351,15 @@ def run_tf(args, rank, world):
                 flush.zero_()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
-                tf.tf_attn_partials(d.seg, l, d.q[l], d.partials)
+                d.attn(l)
                 b.record(stream)
                 torch.cuda.synchronize()
                 part_ms.append(a.elapsed_time(b))
     clocks.stop()
 
     peak, peak_kind = measured_peaks()
-    attn_alg = sum(k for _, _, k in inp.streams) * 8 * 64 * 2 * 2 + R * 32 * 64 * 2
+    # one attention call: every stream's K and V (bf16), the queries in (bf16), the output out (fp32)
+    attn_alg = sum(k for _, _, k in inp.streams) * 8 * 64 * 2 * 2 + R * 32 * 64 * (2 + 4)
     part_avg_ms = sum(part_ms) / len(part_ms) if part_ms else float("nan")
     achieved = attn_alg / (part_avg_ms * 1e-3) / 1e9
     traffic = recorded_traffic(args.workload)
@@ -379,9 +385,11 @@ def run_tf(args, rank, world):
                        graph="one CUDA graph per step", parallelism=f"replicas x{world}"),
         "hbm": {"step_algorithmic_bytes": ab["total"], "achieved_gbs": step_gbs, "peak_gbs": peak,
                 "frac": step_gbs / peak, "peak_kind": peak_kind},
-        "roofline": {"kernel": "tf_attn_partials", "bound": "hbm", "achieved": achieved, "peak": peak,
+        "roofline": {"kernel": "tf_attn (attention partials with the merge folded in)", "bound": "hbm",
+                     "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": attn_alg, "avg_launch_ms": part_avg_ms,
+                     "launches_per_call": d.seg.plan["attn_kernels"] + d.seg.plan["attn_merge_launch"],
                      "launches_timed": len(part_ms), "peak_kind": peak_kind,
                      "timing": "CUDA events around each launch inside the graph, every timed step"
                      if graph_events else "CUDA events around eager launches after the timed region"},

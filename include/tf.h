@@ -87,6 +87,8 @@ typedef struct {
     int32_t max_rows;
     int32_t n_conv_tiles;     /* 8-row conv tiles ([SRD] "8-row tiles") */
     int32_t n_attn_items;     /* (stream, key chunk) work items per KV head */
+    int32_t attn_kernels;     /* partial-kernel launches per attention layer (1 or 2) */
+    int32_t attn_merge_launch;/* 1 if tf_attn also launches the merge kernel */
     int32_t reserved;
     int64_t n_partials;       /* partial records: sum_s rows_s * 32 * chunks_s */
     int64_t partials_bytes;   /* scratch tf_attn_partials needs (see below) */
@@ -158,7 +160,14 @@ int tf_conv_rows(const tf_segments* seg, int conv_layer, const void* bcx,
 
 /* a2. Causal GQA attention partials of one attention layer: for every stream,
  * KV head, key chunk, window row and query head, (m, l, o) over the chunk's
- * visible keys ([SRD] "qk, attention and merge (10 layers)").
+ * visible keys ([SRD] "qk, attention and merge (10 layers)"). Streams with
+ * windows of 3 rows or more run on the tcgen05 tensor-core kernel, the others
+ * on the mma.sync kernel; the choice depends on the stream alone (so a
+ * stream's bits do not depend on its round), and a round holding both kinds
+ * makes one launch of each (tf_plan.attn_kernels). The environment variable
+ * TF_ATTN_PATH=mma|tc, read by tf_segments_build, forces one kernel for every
+ * stream. Values of V must lie within fp16's range (|v| < 65504): P.V runs in
+ * fp16 with fp32 accumulation.
  *   q         bf16 [R][TF_NQ][TF_D]
  *   partials  device scratch of tf_partials_bytes(seg) bytes. Record of
  *             stream s, chunk c, KV head g, row i, head 4g+hh:
@@ -170,6 +179,19 @@ int tf_conv_rows(const tf_segments* seg, int conv_layer, const void* bcx,
  * Score = (q . k) / 8; query head h reads KV head h / 4. Errors: TF_EINVAL. */
 int tf_attn_partials(const tf_segments* seg, int attn_layer, const void* q,
                      void* partials, tf_cuda_stream stream);
+
+/* a2+a3 in one call: the attention output of one layer. One launch of the
+ * partials kernel(s) in which a stream with a single key chunk writes its
+ * output directly and a stream with few partial records (4 * rows * chunks
+ * <= 512) is merged by the last CTA to finish each of its KV heads (counted
+ * by per-layer counters in the table that reset themselves); streams with
+ * more records are merged by one merge launch. ([SRD]: "one launch a layer
+ * over every row".) Same arguments as tf_attn_partials plus `out`
+ * (float [R][TF_NQ][TF_D]); `partials` is the scratch of tf_partials_bytes.
+ * Calls on the same table and layer must not overlap on the GPU.
+ * Errors: TF_EINVAL. */
+int tf_attn(const tf_segments* seg, int attn_layer, const void* q, void* partials, float* out,
+            tf_cuda_stream stream);
 
 /* a3. Log-sum-exp merge of the partials into the attention output
  * ([SRD] lfm2_merge_row): out = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c,

@@ -29,6 +29,8 @@ accept_kernel(SegTable t, const int32_t* __restrict__ ids, const int32_t* __rest
     const int layer = blockIdx.y;
     const SegStream st = t.streams[s];
     const int o = st.row_offset;
+    pdl_wait();
+    pdl_trigger();
 
     int sf = 0;
     for (int j = 1; j < st.rows; ++j) {
@@ -79,7 +81,6 @@ extern "C" int tf_accept(const tf_segments* seg, const int32_t* ids, const int32
     if (rewind_conv && need_hist && t.n_conv > 0 && !t.has_hist) return TF_EINVAL;
     const int ly = (rewind_conv && t.n_conv > 0) ? t.n_conv : 1;
     dim3 grid(t.S, ly);
-    accept_kernel<<<grid, kThreads, 0, stream>>>(t, ids, pick, flag, vocab, accept_len, next_token,
-                                                 new_keys, sflag, rewind_conv ? 1 : 0);
-    return launch_status();
+    return launch_pdl(accept_kernel, grid, dim3(kThreads), 0, stream, t, ids, pick, flag, vocab, accept_len,
+                      next_token, new_keys, sflag, rewind_conv ? 1 : 0);
 }

@@ -89,6 +89,7 @@ argmax_rows_kernel(const uint16_t* __restrict__ logits, int V, int64_t stride, i
     float best = -INFINITY;
     int bid = 0x7FFFFFFF;
     uint32_t nf = 0;
+    pdl_wait();
 
     if (kVec) {
         // vector part: [begin, vend), begin and chunk are multiples of 8
@@ -108,6 +109,7 @@ argmax_rows_kernel(const uint16_t* __restrict__ logits, int V, int64_t stride, i
     } else {
         for (int j = begin + threadIdx.x; j < end; j += kThreads) scan_one(p[j], j, best, bid, nf);
     }
+    pdl_trigger();
     if (best == 0.0f) best = 0.0f;   // -0 -> +0 so keys compare as values
     bool bad = (nf & 0x80008000u) != 0;
 
@@ -186,13 +188,15 @@ extern "C" int tf_argmax_rows(const void* logits, int R, int V, int64_t row_stri
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = cl;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // see tf_internal.cuh
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     const uint16_t* lg = static_cast<const uint16_t*>(logits);
     cudaError_t e = vec ? cudaLaunchKernelEx(&cfg, argmax_rows_kernel<true>, lg, V, row_stride, chunk, pick, flag)
                         : cudaLaunchKernelEx(&cfg, argmax_rows_kernel<false>, lg, V, row_stride, chunk, pick, flag);

@@ -89,7 +89,7 @@ __device__ __forceinline__ uint32_t swz(int r, int ch) { return uint32_t(r * kRo
 template <int MT>
 __global__ void __launch_bounds__(kThreads)
 attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
-                     float* __restrict__ part_o, float2* __restrict__ part_ml) {
+                     float* __restrict__ part_o, float2* __restrict__ part_ml, float* __restrict__ out) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr bool kQReg = MT <= 2;
     const int item_idx = blockIdx.x / TF_NKV;
@@ -107,6 +107,7 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
     unsigned char* sQ = smem + kStages * kStageB;
     const uint32_t sKV32 = smem_u32(sKV), sQ32 = smem_u32(sQ);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    pdl_wait();   // the table above; queries and caches below
 
     // query rows qi = 4*i + hh (window row i, head 4g + hh); rows past nq are zero
     for (int idx = tid; idx < 16 * MT * 8; idx += kThreads) {
@@ -286,6 +287,7 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
     }
     cp_async_wait<0>();
     __syncthreads();
+    pdl_trigger();
 
     // renormalise each row to its true running max (exact partial format)
 #pragma unroll
@@ -328,6 +330,7 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
         }
     }
     __syncthreads();
+    const int mode = out ? st.merge_mode : kMergeKernel;   // records only in the two-call form
     const int64_t rec0 = st.pbase + (int64_t(item.chunk) * TF_NKV + g) * nq;
     for (int idx = tid; idx < nq * (TF_D / 4); idx += kThreads) {
         const int qi = idx >> 4, d4 = (idx & 15) * 4;
@@ -349,8 +352,18 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
                 acc.w += wt * v.w;
             }
         }
-        *reinterpret_cast<float4*>(part_o + (rec0 + qi) * TF_D + d4) = acc;
-        if (d4 == 0) part_ml[rec0 + qi] = make_float2(M, L);
+        if (mode == kMergeDirect) {   // the stream's only chunk: the output itself
+            const float inv = 1.f / L;
+            *reinterpret_cast<float4*>(out_row(out, st, g, qi) + d4) =
+                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        } else {
+            *reinterpret_cast<float4*>(part_o + (rec0 + qi) * TF_D + d4) = acc;
+            if (d4 == 0) part_ml[rec0 + qi] = make_float2(M, L);
+        }
+    }
+    if (mode == kMergeLastCta) {
+        __shared__ int last_flag;
+        finish_last_cta(t, layer, item.stream, st, g, part_o, part_ml, out, &last_flag);
     }
 }
 
@@ -363,18 +376,23 @@ constexpr int kMergeUnroll = 8;
 // time with independent loads, lane j holding dimensions 2j and 2j+1.
 __global__ void __launch_bounds__(kMergeThreads)
 attn_merge_kernel(SegTable t, const float* __restrict__ part_o, const float2* __restrict__ part_ml,
-                  float* __restrict__ out) {
+                  float* __restrict__ out, int kernel_mode_only) {
     const int row = blockIdx.x >> 2;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int h = (blockIdx.x & 3) * kMergeWarps + warp;
     const int s = t.row_stream[row];
     const SegStream st = t.streams[s];
+    if (kernel_mode_only && st.merge_mode != kMergeKernel) {   // finished by the partials kernel
+        pdl_trigger();
+        return;
+    }
     const int i = row - st.row_offset;
     const int nq = st.rows * 4;
     const int g = h >> 2, hh = h & 3;
     const int64_t stride = int64_t(TF_NKV) * nq;   // records between chunks
     const int64_t base = st.pbase + int64_t(g) * nq + i * 4 + hh;
     const int C = st.n_chunks;
+    pdl_wait();
 
     float M = -INFINITY;
     for (int c = lane; c < C; c += 32) {
@@ -417,6 +435,7 @@ attn_merge_kernel(SegTable t, const float* __restrict__ part_o, const float2* __
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
+    pdl_trigger();
     const float inv = 1.f / lsum;
     *reinterpret_cast<float2*>(out + (size_t(row) * TF_NQ + h) * TF_D + 2 * lane) =
         make_float2(acc.x * inv, acc.y * inv);
@@ -442,21 +461,26 @@ int attn_prepare() {
 // Launchers for other translation units: the partials and the merge of one
 // attention layer with the partial records at `po` (o) and `pml` (m, l).
 int launch_attn_partials(const SegTable& t, int layer, const uint16_t* q, float* po, float2* pml,
-                         cudaStream_t stream) {
-    const int mt = (t.max_rows + 3) / 4;
-    const dim3 grid(t.n_items * TF_NKV);
-    switch (mt) {
-        case 1: attn_partials_kernel<1><<<grid, kThreads, smem_bytes(1), stream>>>(t, layer, q, po, pml); break;
-        case 2: attn_partials_kernel<2><<<grid, kThreads, smem_bytes(2), stream>>>(t, layer, q, po, pml); break;
-        case 3: attn_partials_kernel<3><<<grid, kThreads, smem_bytes(3), stream>>>(t, layer, q, po, pml); break;
-        default: attn_partials_kernel<4><<<grid, kThreads, smem_bytes(4), stream>>>(t, layer, q, po, pml); break;
+                         cudaStream_t stream, float* out) {
+    if (t.n_items_mma > 0) {
+        const dim3 grid(t.n_items_mma * TF_NKV);
+        int rc;
+        switch (t.mma_mt) {
+            case 1: rc = launch_pdl(attn_partials_kernel<1>, grid, dim3(kThreads), smem_bytes(1), stream, t, layer, q, po, pml, out); break;
+            case 2: rc = launch_pdl(attn_partials_kernel<2>, grid, dim3(kThreads), smem_bytes(2), stream, t, layer, q, po, pml, out); break;
+            case 3: rc = launch_pdl(attn_partials_kernel<3>, grid, dim3(kThreads), smem_bytes(3), stream, t, layer, q, po, pml, out); break;
+            default: rc = launch_pdl(attn_partials_kernel<4>, grid, dim3(kThreads), smem_bytes(4), stream, t, layer, q, po, pml, out); break;
+        }
+        if (rc != TF_OK) return rc;
     }
-    return launch_status();
+    if (t.n_items_mma < t.n_items) return launch_attn_partials_tc(t, layer, q, po, pml, stream, out);
+    return TF_OK;
 }
 
-int launch_attn_merge(const SegTable& t, const float* po, const float2* pml, float* out, cudaStream_t stream) {
-    attn_merge_kernel<<<t.R * 4, kMergeThreads, 0, stream>>>(t, po, pml, out);
-    return launch_status();
+int launch_attn_merge(const SegTable& t, const float* po, const float2* pml, float* out, cudaStream_t stream,
+                      bool kernel_mode_only) {
+    return launch_pdl(attn_merge_kernel, dim3(t.R * 4), dim3(kMergeThreads), 0, stream, t, po, pml, out,
+                      kernel_mode_only ? 1 : 0);
 }
 
 }  // namespace tf
@@ -471,16 +495,22 @@ extern "C" int tf_attn_partials(const tf_segments* seg, int attn_layer, const vo
     if (!q || !partials || !aligned16(q) || !aligned16(partials)) return TF_EINVAL;
     float* po = static_cast<float*>(partials);
     float2* pml = reinterpret_cast<float2*>(po + t.n_partials * TF_D);
-    const int mt = (t.max_rows + 3) / 4;
-    const dim3 grid(t.n_items * TF_NKV);
-    const uint16_t* qq = static_cast<const uint16_t*>(q);
-    switch (mt) {
-        case 1: attn_partials_kernel<1><<<grid, kThreads, smem_bytes(1), stream>>>(t, attn_layer, qq, po, pml); break;
-        case 2: attn_partials_kernel<2><<<grid, kThreads, smem_bytes(2), stream>>>(t, attn_layer, qq, po, pml); break;
-        case 3: attn_partials_kernel<3><<<grid, kThreads, smem_bytes(3), stream>>>(t, attn_layer, qq, po, pml); break;
-        default: attn_partials_kernel<4><<<grid, kThreads, smem_bytes(4), stream>>>(t, attn_layer, qq, po, pml); break;
-    }
-    return launch_status();
+    return launch_attn_partials(t, attn_layer, static_cast<const uint16_t*>(q), po, pml, stream);
+}
+
+extern "C" int tf_attn(const tf_segments* seg, int attn_layer, const void* q, void* partials, float* out,
+                       tf_cuda_stream stream) {
+    using namespace tf;
+    if (!seg) return TF_EINVAL;
+    const SegTable& t = seg->dev;
+    if (attn_layer < 0 || attn_layer >= t.n_attn) return TF_EINVAL;
+    if (t.R == 0) return TF_OK;
+    if (!q || !partials || !out || !aligned16(q) || !aligned16(partials) || !aligned16(out)) return TF_EINVAL;
+    float* po = static_cast<float*>(partials);
+    float2* pml = reinterpret_cast<float2*>(po + t.n_partials * TF_D);
+    int rc = launch_attn_partials(t, attn_layer, static_cast<const uint16_t*>(q), po, pml, stream, out);
+    if (rc != TF_OK || t.n_merge_rows == 0) return rc;
+    return launch_attn_merge(t, po, pml, out, stream, true);
 }
 
 extern "C" int tf_attn_merge(const tf_segments* seg, const void* partials, float* out, tf_cuda_stream stream) {
@@ -491,6 +521,5 @@ extern "C" int tf_attn_merge(const tf_segments* seg, const void* partials, float
     if (!partials || !out || !aligned16(partials) || !aligned16(out)) return TF_EINVAL;
     const float* po = static_cast<const float*>(partials);
     const float2* pml = reinterpret_cast<const float2*>(po + t.n_partials * TF_D);
-    attn_merge_kernel<<<t.R * 4, kMergeThreads, 0, stream>>>(t, po, pml, out);
-    return launch_status();
+    return launch_attn_merge(t, po, pml, out, stream, false);
 }

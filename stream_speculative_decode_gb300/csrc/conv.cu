@@ -58,6 +58,7 @@ conv_rows_kernel(SegTable t, int layer, const uint16_t* __restrict__ bcx,
     uint16_t* hist = t.has_hist ? static_cast<uint16_t*>(t.conv_hist[slot]) : nullptr;
     const int n = tile.nrows;
     const int row_base = st.row_offset + tile.row0;
+    pdl_wait();   // the table above; the data below may come from the previous kernel
 
     // taps of channels c..c+7: 24 bf16, element (channel j, tap k) at 3*j+k
     float wt[24];
@@ -99,6 +100,7 @@ conv_rows_kernel(SegTable t, int layer, const uint16_t* __restrict__ bcx,
         s1 = gate8(*reinterpret_cast<const uint4*>(r1), *reinterpret_cast<const uint4*>(r1 + 2 * TF_H));
     }
     const uint4 old0 = s0, old1 = s1;
+    pdl_trigger();
 
     float f0[8], f1[8];
     unpack8(s0, f0);
@@ -163,7 +165,6 @@ extern "C" int tf_conv_rows(const tf_segments* seg, int conv_layer, const void* 
     if (t.R == 0) return TF_OK;
     if (!bcx || !w || !y || !aligned16(bcx) || !aligned16(w) || !aligned16(y)) return TF_EINVAL;
     dim3 grid(t.n_tiles, TF_H / kChanPerCta);
-    conv_rows_kernel<<<grid, kThreads, 0, stream>>>(t, conv_layer, static_cast<const uint16_t*>(bcx),
-                                                   static_cast<const uint16_t*>(w), y);
-    return launch_status();
+    return launch_pdl(conv_rows_kernel, grid, dim3(kThreads), 0, stream, t, conv_layer,
+                      static_cast<const uint16_t*>(bcx), static_cast<const uint16_t*>(w), y);
 }

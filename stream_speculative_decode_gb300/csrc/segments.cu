@@ -8,9 +8,12 @@
 // residency concern (a table reaching buffers nobody declared) becomes here a
 // host check that the table's buffers are valid, aligned and never overlap.
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
+
+#include <cudaTypedefs.h>   // PFN_cuTensorMapEncodeTiled
 
 #include "tf_internal.cuh"
 
@@ -37,6 +40,50 @@ int sm_count() {
 }
 
 int attn_prepare();   // attn.cu: kernel attributes
+
+namespace {
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// TMA map of one stream's K or V cache, bf16 [8][cap][64], as a 3-D tensor
+// (d, key, head) of extents (64, keys, 8): keys past `keys` read as zeros. A box
+// is 64 keys of one head, 128-byte rows, 128-byte swizzle (the layout the
+// tensor-core kernel's shared-memory descriptors describe).
+bool encode_kv_map(CUtensorMap* out, const void* base, int keys, int cap) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {cuuint64_t(TF_D), cuuint64_t(keys), cuuint64_t(TF_NKV)};
+    const cuuint64_t strides[2] = {cuuint64_t(TF_D) * 2, cuuint64_t(cap) * TF_D * 2};
+    const cuuint32_t box[3] = {cuuint32_t(TF_D), 64u, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// Attention kernel of a stream: tensor cores once its window holds 3 rows (12
+// query rows per KV head); TF_ATTN_PATH=mma|tc forces one (tests compare both).
+int attn_path_of(int rows) {
+    const char* e = std::getenv("TF_ATTN_PATH");
+    if (e && std::strcmp(e, "mma") == 0) return kAttnMma;
+    if (e && std::strcmp(e, "tc") == 0) return kAttnTc;
+    return rows >= kTcMinRows ? kAttnTc : kAttnMma;
+}
 
 namespace {
 
@@ -69,6 +116,7 @@ int tf_segments_plan(const tf_stream* streams, int n_streams, tf_plan* out) {
     if (n_streams > 0 && !streams) return TF_EINVAL;
     int64_t R = 0, parts = 0, items = 0, tiles = 0;
     int max_rows = 0;
+    bool any_mma = false, any_tc = false, any_merge = false;
     for (int s = 0; s < n_streams; ++s) {
         const tf_stream& st = streams[s];
         if (st.rows < 1 || st.keys < 1 || st.kv_capacity < 1) return TF_EINVAL;
@@ -82,6 +130,8 @@ int tf_segments_plan(const tf_stream* streams, int n_streams, tf_plan* out) {
         items += nch;
         tiles += (st.rows + tf::kConvTileRows - 1) / tf::kConvTileRows;
         max_rows = std::max(max_rows, int(st.rows));
+        (tf::attn_path_of(st.rows) == tf::kAttnTc ? any_tc : any_mma) = true;
+        if (nch > 1 && 4 * st.rows * nch > tf::kMergeLastCtaMaxRecords) any_merge = true;
     }
     if (R > (1 << 24)) return TF_ERANGE;
     out->n_streams = n_streams;
@@ -89,6 +139,8 @@ int tf_segments_plan(const tf_stream* streams, int n_streams, tf_plan* out) {
     out->max_rows = max_rows;
     out->n_conv_tiles = int32_t(tiles);
     out->n_attn_items = int32_t(items);
+    out->attn_kernels = int32_t(any_mma) + int32_t(any_tc);
+    out->attn_merge_launch = int32_t(any_merge);
     out->n_partials = parts;
     out->partials_bytes = parts * TF_D * 4 + parts * 8;
     return TF_OK;
@@ -164,13 +216,19 @@ int tf_segments_build(const tf_stream* streams, int n_streams,
         d.n_chunks = (st.keys + d.chunk_keys - 1) / d.chunk_keys;
         d.pbase = pbase;
         pbase += int64_t(st.rows) * TF_NQ * d.n_chunks;
+        d.merge_mode = d.n_chunks == 1 ? kMergeDirect
+                     : (4 * st.rows * d.n_chunks <= kMergeLastCtaMaxRecords ? kMergeLastCta : kMergeKernel);
+        d.pad_ = 0;
         for (int i = 0; i < st.rows; ++i) row_stream[st.row_offset + i] = s;
         for (int r0 = 0; r0 < st.rows; r0 += kConvTileRows)
             tiles.push_back({s, r0, std::min(kConvTileRows, st.rows - r0), 0});
         for (int c = 0; c < d.n_chunks; ++c) items.push_back({s, c});
     }
-    // largest chunks first, so the long work starts early in the grid
+    // mma.sync items first, then tensor-core items; within each, largest
+    // chunks first so the long work starts early in the grid
     std::stable_sort(items.begin(), items.end(), [&](const AttnItem& a, const AttnItem& b) {
+        const int pa = attn_path_of(ss[a.stream].rows), pb = attn_path_of(ss[b.stream].rows);
+        if (pa != pb) return pa < pb;
         auto len = [&](const AttnItem& it) {
             const SegStream& d = ss[it.stream];
             int lo = it.chunk * d.chunk_keys;
@@ -179,6 +237,12 @@ int tf_segments_build(const tf_stream* streams, int n_streams,
         };
         return len(a) > len(b);
     });
+    int n_items_mma = 0, mma_rows = 1;
+    for (const AttnItem& it : items)
+        if (attn_path_of(ss[it.stream].rows) == kAttnMma) {
+            ++n_items_mma;
+            mma_rows = std::max(mma_rows, ss[it.stream].rows);
+        }
 
     size_t off = 0;
     const size_t o_streams = off;  off = align_up(off + sizeof(SegStream) * S, 256);
@@ -190,6 +254,10 @@ int tf_segments_build(const tf_stream* streams, int n_streams,
     const size_t o_ch = off;       off = align_up(off + (conv_hist ? sizeof(void*) * n_cp : 0), 256);
     const size_t o_k = off;        off = align_up(off + sizeof(void*) * n_ap, 256);
     const size_t o_v = off;        off = align_up(off + sizeof(void*) * n_ap, 256);
+    const size_t n_maps = size_t(n_items_mma) < items.size() ? n_ap : 0;
+    const size_t o_km = off;       off = align_up(off + sizeof(CUtensorMap) * n_maps, 256);
+    const size_t o_vm = off;       off = align_up(off + sizeof(CUtensorMap) * n_maps, 256);
+    const size_t o_ctr = off;      off = align_up(off + sizeof(int32_t) * n_ap * TF_NKV, 256);
     const size_t total = off;
 
     seg->host.assign(total, 0);
@@ -204,6 +272,17 @@ int tf_segments_build(const tf_stream* streams, int n_streams,
         std::memcpy(h + o_k, k_cache, sizeof(void*) * n_ap);
         std::memcpy(h + o_v, v_cache, sizeof(void*) * n_ap);
     }
+    for (size_t i = 0; i < n_maps; ++i) {
+        const tf_stream& st = streams[i % S];
+        CUtensorMap km, vm;   // aligned locals, copied into the image
+        if (!encode_kv_map(&km, k_cache[i], st.keys, st.kv_capacity) ||
+            !encode_kv_map(&vm, v_cache[i], st.keys, st.kv_capacity)) {
+            delete seg;
+            return cuda_fail(cudaErrorInvalidValue);
+        }
+        std::memcpy(h + o_km + i * sizeof(CUtensorMap), &km, sizeof(CUtensorMap));
+        std::memcpy(h + o_vm + i * sizeof(CUtensorMap), &vm, sizeof(CUtensorMap));
+    }
     seg->streams = ss;
 
     SegTable& t = seg->dev;
@@ -217,6 +296,11 @@ int tf_segments_build(const tf_stream* streams, int n_streams,
     t.max_rows = plan.max_rows;
     t.has_hist = conv_hist ? 1 : 0;
     t.n_partials = plan.n_partials;
+    t.n_items_mma = n_items_mma;
+    t.mma_mt = (mma_rows + 3) / 4;
+    t.n_merge_rows = 0;
+    for (const SegStream& d : ss)
+        if (d.merge_mode == kMergeKernel) t.n_merge_rows += d.rows;
 
     if (total > 0 && S > 0) {
         cudaError_t e = cudaMalloc(&seg->blob, total);
@@ -240,7 +324,11 @@ int tf_segments_build(const tf_stream* streams, int n_streams,
         t.conv_hist = conv_hist ? reinterpret_cast<void* const*>(b + o_ch) : nullptr;
         t.k_cache = reinterpret_cast<const void* const*>(b + o_k);
         t.v_cache = reinterpret_cast<const void* const*>(b + o_v);
+        t.k_maps = n_maps ? reinterpret_cast<const CUtensorMap*>(b + o_km) : nullptr;
+        t.v_maps = n_maps ? reinterpret_cast<const CUtensorMap*>(b + o_vm) : nullptr;
+        t.counters = reinterpret_cast<int32_t*>(b + o_ctr);   // zero in the image
         rc = attn_prepare();
+        if (rc == TF_OK) rc = attn_tc_prepare();
         if (rc != TF_OK) {
             cudaFree(seg->blob);
             delete seg;

@@ -2,6 +2,7 @@
 // segment table, launch helpers and small device utilities.
 #pragma once
 
+#include <cuda.h>            // CUtensorMap (the type only; the encoder comes from the runtime's driver entry point)
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -17,7 +18,15 @@ struct SegStream {
     int32_t rows, row_offset, keys, cap;
     int32_t chunk_keys, n_chunks;
     int64_t pbase;            // first partial record of the stream
+    int32_t merge_mode;       // in one-call attention: kMergeDirect / kMergeLastCta / kMergeKernel
+    int32_t pad_;
 };
+
+// How the one-call attention (tf_attn) finishes a stream's chunks.
+constexpr int kMergeDirect = 0;    // one chunk: the partials kernel writes the output
+constexpr int kMergeLastCta = 1;   // few records: the last CTA of each KV head merges them
+constexpr int kMergeKernel = 2;    // many records: the merge kernel
+constexpr int kMergeLastCtaMaxRecords = 512;   // 4*rows*chunks of one KV head
 
 // A conv tile: up to 8 consecutive rows of one stream.
 struct ConvTile {
@@ -41,9 +50,24 @@ struct SegTable {
     void* const* conv_hist;           // [n_conv][S] or nullptr
     const void* const* k_cache;       // [n_attn][S]
     const void* const* v_cache;       // [n_attn][S]
+    const CUtensorMap* k_maps;        // [n_attn][S] TMA maps of the K caches (tensor-core path)
+    const CUtensorMap* v_maps;        // [n_attn][S]
     int32_t S, R, n_tiles, n_items, n_conv, n_attn, max_rows, has_hist;
+    int32_t n_items_mma;              // items [0, n_items_mma) run on the mma.sync kernel,
+                                      // [n_items_mma, n_items) on the tcgen05 kernel
+    int32_t mma_mt;                   // 16-row query tiles of the mma.sync kernel's widest stream
     int64_t n_partials;
+    int32_t* counters;                // [n_attn][S][8] arrivals per (stream, KV head), self-resetting
+    int32_t n_merge_rows;             // rows of kMergeKernel streams
+    int32_t pad2_;
 };
+
+constexpr int kAttnMma = 0;   // mma.sync flash-decode kernel (narrow windows)
+constexpr int kAttnTc = 1;    // tcgen05 + TMA kernel (windows of 3 rows or more)
+constexpr int kTcMinRows = 3;
+
+// Kernel of a stream: by its window rows, unless TF_ATTN_PATH forces one.
+int attn_path_of(int rows);
 
 }  // namespace tf
 
@@ -72,9 +96,138 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Number of SMs of the current device (cached per device).
 int sm_count();
 
+// ---- programmatic dependent launch ---------------------------------------
+// Every kernel of the library is launched with programmatic stream
+// serialization: it may start while the previous kernel of the stream is
+// finishing. Before griddepcontrol.wait a kernel reads nothing but the
+// segment table (immutable once built, uploaded before any launch that uses
+// it); after it, everything the previous kernels wrote is visible. Each kernel
+// lets its dependents launch once it has finished its main work.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+               Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return launch_status();
+}
+
 // attn.cu: one attention layer's partials and merge with the records at po/pml.
+// With out != nullptr the partials kernels also finish the streams whose
+// merge_mode is kMergeDirect or kMergeLastCta (the one-call form).
 int launch_attn_partials(const SegTable& t, int layer, const uint16_t* q, float* po, float2* pml,
-                         cudaStream_t stream);
-int launch_attn_merge(const SegTable& t, const float* po, const float2* pml, float* out, cudaStream_t stream);
+                         cudaStream_t stream, float* out = nullptr);
+int launch_attn_merge(const SegTable& t, const float* po, const float2* pml, float* out, cudaStream_t stream,
+                      bool kernel_mode_only = false);
+
+// attn_tc.cu: the tensor-core partials kernel (same records as the mma.sync kernel).
+int launch_attn_partials_tc(const SegTable& t, int layer, const uint16_t* q, float* po, float2* pml,
+                            cudaStream_t stream, float* out);   // items [n_items_mma, n_items)
+int attn_tc_prepare();
+
+}  // namespace tf
+
+namespace tf {
+
+// ---- shared device code of the attention kernels -------------------------
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Output address of query row qi (window row qi/4, head 4g + qi%4) of a stream.
+__device__ __forceinline__ float* out_row(float* out, const SegStream& st, int g, int qi) {
+    return out + (size_t(st.row_offset + (qi >> 2)) * TF_NQ + 4 * g + (qi & 3)) * TF_D;
+}
+
+// Log-sum-exp merge of the chunk records of one (stream, KV head) into the
+// output, by the threads [tid, nthreads) of one CTA, one pass over the chunks
+// eight at a time (their loads in flight together) with a running max. The
+// records were written by other CTAs: they are read through L2 (ld.global.cg).
+__device__ __forceinline__ void merge_stream_head(const SegStream& st, int g, const float* part_o,
+                                                  const float2* part_ml, float* out, int tid, int nthreads) {
+    constexpr int kB = 8;
+    const int nq = st.rows * 4;
+    const int64_t stride = int64_t(TF_NKV) * nq;
+    const int64_t base = st.pbase + int64_t(g) * nq;
+    for (int idx = tid; idx < nq * (TF_D / 4); idx += nthreads) {
+        const int qi = idx >> 4, d4 = (idx & 15) * 4;
+        float M = -INFINITY, L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c0 = 0; c0 < st.n_chunks; c0 += kB) {
+            float2 ml[kB];
+            float4 v[kB];
+#pragma unroll
+            for (int k = 0; k < kB; ++k) {
+                ml[k] = make_float2(-INFINITY, 0.f);
+                v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (c0 + k < st.n_chunks) {
+                    const int64_t rec = base + (c0 + k) * stride + qi;
+                    ml[k] = __ldcg(part_ml + rec);
+                    v[k] = __ldcg(reinterpret_cast<const float4*>(part_o + rec * TF_D + d4));
+                }
+            }
+            float Mb = M;
+#pragma unroll
+            for (int k = 0; k < kB; ++k)
+                if (ml[k].y > 0.f) Mb = fmaxf(Mb, ml[k].x);
+            if (Mb == -INFINITY) continue;
+            const float sc = (M == -INFINITY) ? 0.f : ex2_approx(M - Mb);
+            L *= sc;
+            acc.x *= sc;
+            acc.y *= sc;
+            acc.z *= sc;
+            acc.w *= sc;
+            M = Mb;
+#pragma unroll
+            for (int k = 0; k < kB; ++k) {
+                if (ml[k].y > 0.f) {
+                    const float w = ex2_approx(ml[k].x - M);
+                    L += w * ml[k].y;
+                    acc.x += w * v[k].x;
+                    acc.y += w * v[k].y;
+                    acc.z += w * v[k].z;
+                    acc.w += w * v[k].w;
+                }
+            }
+        }
+        const float inv = 1.f / L;
+        *reinterpret_cast<float4*>(out_row(out, st, g, qi) + d4) =
+            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+}
+
+// End of a partials CTA in the one-call form, for kMergeLastCta streams: every
+// CTA of (stream, KV head) counts its arrival after its records are visible;
+// the last one merges and resets the counter for the next launch. All threads
+// of the CTA call this.
+__device__ __forceinline__ void finish_last_cta(const SegTable& t, int layer, int s, const SegStream& st, int g,
+                                                const float* part_o, const float2* part_ml, float* out,
+                                                int* smem_flag) {
+    __threadfence();
+    __syncthreads();
+    int* ctr = t.counters + (size_t(layer) * t.S + s) * TF_NKV + g;
+    if (threadIdx.x == 0) *smem_flag = (atomicAdd(ctr, 1) == st.n_chunks - 1);
+    __syncthreads();
+    if (*smem_flag) {
+        __threadfence();
+        merge_stream_head(st, g, part_o, part_ml, out, threadIdx.x, blockDim.x);
+        if (threadIdx.x == 0) atomicExch(ctr, 0);
+    }
+}
 
 }  // namespace tf

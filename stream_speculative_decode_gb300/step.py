@@ -48,7 +48,7 @@ class DeviceStep:
     per-layer conv inputs, queries and the logits are the step's inputs.
     """
 
-    def __init__(self, inp: StepInputs, device="cuda", keep_history=True, stream=None):
+    def __init__(self, inp: StepInputs, device="cuda", keep_history=True, stream=None, fused_attention=True):
         self.inp = inp
         self.device = torch.device(device)
         self.S = S = len(inp.streams)
@@ -99,6 +99,7 @@ class DeviceStep:
                                         stream=stream)
         self.partials = torch.empty(max(self.seg.partials_bytes, 16), dtype=torch.uint8, device=dev)
         self.schedule = layer_schedule(n_conv, n_attn)
+        self.fused_attention = fused_attention
         self.graph = None
 
     # ---------------------------------------------------------------- running
@@ -106,8 +107,11 @@ class DeviceStep:
         tf.tf_conv_rows(self.seg, l, self.bcx[l], self.w[l], self.y[l], stream)
 
     def attn(self, l, stream=None):
-        tf.tf_attn_partials(self.seg, l, self.q[l], self.partials, stream)
-        tf.tf_attn_merge(self.seg, self.partials, self.out[l], stream)
+        if self.fused_attention:   # one call: partials with the merge folded in
+            tf.tf_attn(self.seg, l, self.q[l], self.partials, self.out[l], stream)
+        else:                      # the two-call form
+            tf.tf_attn_partials(self.seg, l, self.q[l], self.partials, stream)
+            tf.tf_attn_merge(self.seg, self.partials, self.out[l], stream)
 
     def head(self, rewind=True, stream=None):
         tf.tf_argmax_rows(self.logits, self.R, self.vocab, self.vocab, self.pick, self.flag, stream)
@@ -115,24 +119,28 @@ class DeviceStep:
                      self.new_keys, self.sflag, rewind and self.hist is not None, stream)
 
     def run(self, stream=None, rewind=True, events=None):
-        """Enqueue the whole step. ``events``: optional dict of lists of
-        (start, end) CUDA event pairs to record around each partials launch."""
+        """Enqueue the whole step. ``events``: optional dict with a list of
+        (start, end) CUDA event pairs per attention layer, recorded around
+        that layer's attention call."""
         for kind, l in self.schedule:
             if kind == "conv":
                 self.conv(l, stream)
+            elif events is not None:
+                ev0, ev1 = events["attn"][l]
+                ev0.record(stream)
+                self.attn(l, stream)
+                ev1.record(stream)
             else:
-                if events is not None:
-                    ev0, ev1 = events["attn_partials"][l]
-                    ev0.record(stream)
-                    tf.tf_attn_partials(self.seg, l, self.q[l], self.partials, stream)
-                    ev1.record(stream)
-                    tf.tf_attn_merge(self.seg, self.partials, self.out[l], stream)
-                else:
-                    self.attn(l, stream)
+                self.attn(l, stream)
         self.head(rewind, stream)
 
     def launches_per_step(self):
-        return self.n_conv + 2 * self.n_attn + 2
+        """Kernel launches of one step: a conv per conv layer, per attention
+        layer one partials launch per kernel kind in the round plus the merge,
+        then the pick and the accept."""
+        p = self.seg.plan
+        per_attn = p["attn_kernels"] + (p["attn_merge_launch"] if self.fused_attention else 1)
+        return self.n_conv + self.n_attn * per_attn + 2
 
     def capture(self, rewind=True, events=None):
         """Capture one step into a CUDA graph (on a side stream)."""

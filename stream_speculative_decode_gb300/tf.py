@@ -22,7 +22,7 @@ TF_OK, TF_EINVAL, TF_ERANGE, TF_ENOMEM, TF_ECUDA = 0, 1, 2, 3, 4
 # every symbol include/tf.h declares
 EXPORTS = ("tf_chunk_keys", "tf_segments_plan", "tf_segments_build", "tf_segments_free",
            "tf_segments_query", "tf_partials_bytes", "tf_conv_rows", "tf_attn_partials",
-           "tf_attn_merge", "tf_attn_static", "tf_argmax_rows", "tf_accept", "tf_strerror",
+           "tf_attn_merge", "tf_attn", "tf_attn_static", "tf_argmax_rows", "tf_accept", "tf_strerror",
            "tf_last_cuda_error")
 TF_STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -44,7 +44,8 @@ class tf_stream(ctypes.Structure):
 class tf_plan(ctypes.Structure):
     _fields_ = [("n_streams", ctypes.c_int32), ("n_rows", ctypes.c_int32),
                 ("max_rows", ctypes.c_int32), ("n_conv_tiles", ctypes.c_int32),
-                ("n_attn_items", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("n_attn_items", ctypes.c_int32), ("attn_kernels", ctypes.c_int32),
+                ("attn_merge_launch", ctypes.c_int32), ("reserved", ctypes.c_int32),
                 ("n_partials", ctypes.c_int64), ("partials_bytes", ctypes.c_int64)]
 
     def as_dict(self):
@@ -68,6 +69,7 @@ def _load():
         "tf_attn_partials": (i32, [vp, i32, vp, vp, vp]),
         "tf_attn_merge": (i32, [vp, vp, vp, vp]),
         "tf_attn_static": (i32, [vp, i32, vp, vp, vp]),
+        "tf_attn": (i32, [vp, i32, vp, vp, vp, vp]),
         "tf_argmax_rows": (i32, [vp, i32, i32, i64, vp, vp, vp]),
         "tf_accept": (i32, [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, vp]),
         "tf_strerror": (ctypes.c_char_p, [i32]),
@@ -204,6 +206,11 @@ def tf_attn_partials(seg, attn_layer, q, partials, stream=None):
 
 def tf_attn_merge(seg, partials, out, stream=None):
     _check("tf_attn_merge", _lib.tf_attn_merge(_h(seg), _ptr(partials), _ptr(out), _stream(stream)))
+
+
+def tf_attn(seg, attn_layer, q, partials, out, stream=None):
+    """One attention layer in one call (partials with an in-kernel merge)."""
+    _check("tf_attn", _lib.tf_attn(_h(seg), attn_layer, _ptr(q), _ptr(partials), _ptr(out), _stream(stream)))
 
 
 def tf_attn_static(seg, attn_layer, q, out, stream=None):

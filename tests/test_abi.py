@@ -167,3 +167,19 @@ def test_argmax_refusals(T):
     assert lib.tf_argmax_rows(0x1000, 2, 10, 9, 0x1000, 0x2000, None) == T.TF_EINVAL  # stride < V
     assert lib.tf_argmax_rows(0x1000, 2, 0, 10, 0x1000, 0x2000, None) == T.TF_EINVAL
     assert lib.tf_argmax_rows(0x1000, 2, (1 << 30) + 1, (1 << 30) + 1, 0x1000, 0x2000, None) == T.TF_ERANGE
+
+
+@pytest.mark.parametrize("rows,kernels", [([1], 1), ([1, 2], 1), ([3], 1), ([16, 4], 1), ([1, 3], 2), ([2, 12, 1], 2)])
+def test_attention_kernel_count(T, rows, kernels, monkeypatch):
+    """Windows of 3 rows or more go to the tensor-core kernel, narrower ones to
+    the mma.sync kernel; a round holding both makes one launch of each."""
+    monkeypatch.delenv("TF_ATTN_PATH", raising=False)
+    streams, off = [], 0
+    for r in rows:
+        streams.append((r, off, 500, 512))
+        off += r
+    assert T.tf_segments_plan(streams)["attn_kernels"] == kernels
+    monkeypatch.setenv("TF_ATTN_PATH", "mma")
+    assert T.tf_segments_plan(streams)["attn_kernels"] == 1
+    monkeypatch.setenv("TF_ATTN_PATH", "tc")
+    assert T.tf_segments_plan(streams)["attn_kernels"] == 1

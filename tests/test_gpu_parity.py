@@ -114,6 +114,37 @@ def test_step_mixed_small(mods):
     run_and_check(mods, w)
 
 
+@pytest.mark.parametrize("path", ["mma", "tc"])
+def test_step_forced_kernel(mods, path, monkeypatch):
+    """Every stream forced onto one attention kernel (the mma.sync kernel for
+    wide windows, the tensor-core kernel for one- and two-row windows)."""
+    monkeypatch.setenv("TF_ATTN_PATH", path)
+    w = small_work(mods, rows=[1, 2, 4, 9, 16], keys=[700, 33, 2500, 4200, 1900], n_conv=1, n_attn=2, seed=13)
+    run_and_check(mods, w)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_step_merge_modes(mods, fused):
+    """The one-call attention finishes single-chunk streams in the partials
+    kernel, streams with few records in the last CTA of each KV head, and the
+    rest in a merge launch; the two-call form merges everything in the merge
+    kernel. Rows/keys below cover all three modes on both attention kernels."""
+    tf, inputs, step, torch = mods
+    w = small_work(mods, rows=[1, 1, 2, 6, 6, 16, 3], keys=[200, 40000, 9000, 1500, 9300, 8000, 700],
+                   n_conv=1, n_attn=1, seed=14)
+    inp = inputs.make_inputs(w, backend="numpy")
+    d = step.DeviceStep(inp, fused_attention=fused)
+    assert d.seg.plan["attn_merge_launch"] == 1
+    d.run()
+    res = d.results()
+    ref = O.verify_step(inp)
+    check_step(res, ref, inp)
+    d.run()                       # counters reset themselves: a second step is right too
+    res2 = d.results()
+    check_attn(res2["out"][0], ref["out"][0], "second step")
+    d.free()
+
+
 def test_step_chunk_edges(mods):
     """Key counts at, just below and just above split-K chunk multiples."""
     rows = [1, 1, 1, 2, 2, 4, 4, 8]
