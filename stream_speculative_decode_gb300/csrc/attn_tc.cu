@@ -7,9 +7,11 @@
 // used when a window holds 3 rows or more, where q.K and P.V are real
 // contractions (4*rows flops per byte of K/V each).
 //
-// One CTA per (work item = one stream's key chunk, KV head), 6 warps:
-//   warp 4, lane 0   control: TMA loads of K/V tiles (64 keys = 8 KB each,
-//                    128-byte swizzle) into a 5-stage ring, and the MMAs;
+// One CTA per (work item = one stream's key chunk, KV head), 7 warps:
+//   warp 6, lane 0   TMA loads of K/V tiles (64 keys = 8 KB each, 128-byte
+//                    swizzle) into a 5-stage ring, refilling a stage as soon
+//                    as the P.V that read it completes;
+//   warp 4, lane 0   the MMAs;
 //   warp 5           converts each V tile bf16 -> fp16 in shared memory as
 //                    soon as it lands (exact within fp16's range);
 //   warps 0-3        softmax; query row qi sits on TMEM lane
@@ -46,7 +48,7 @@ constexpr int kTileB = kKT * TF_D * 2;      // 8 KB: one K or V tile
 constexpr int kStageB = 2 * kTileB;         // K then V
 constexpr int kQRows = 128;                 // MMA M
 constexpr int kQB = kQRows * TF_D * 2;      // 16 KB
-constexpr int kWarps = 6;
+constexpr int kWarps = 7;
 constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kCols = 256;             // tensor-memory columns per CTA (192 used)
 constexpr uint32_t kColS = 0;               // + 64 * (tile % 2)
@@ -435,16 +437,6 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
     if (warp == 4) {
         // ------------------------------------------------------------ control
         if (lane == 0) {
-            int issued = 0, consumed = 0;
-            auto issue = [&](int j) {
-                const int s = j % kStages;
-                const uint32_t bar = su32(&bars->kv_full[s]);
-                mbar_expect_tx(bar, kStageB);
-                tma_load_3d(sStage + s * kStageB, kmap, 0, c0 + j * kKT, g, bar);
-                tma_load_3d(sStage + s * kStageB + kTileB, vmap, 0, c0 + j * kKT, g, bar);
-                ++issued;
-            };
-            for (int j = 0; j < T && j < kStages; ++j) issue(j);
             const uint64_t dq = sdesc(sQ, 16, 1024);
             bool ok = true;
             for (int j = 0; j <= T && ok; ++j) {
@@ -452,7 +444,6 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                     const int s = j % kStages, b = j & 1;
                     ok = mbar_wait(su32(&bars->kv_full[s]), (j / kStages) & 1, abortp);
                     if (!ok) break;
-                    consumed = j + 1;
                     if (j >= 2) {   // P.V(j-2) has released S buffer b
                         ok = mbar_wait(su32(&bars->o_done[b]), ((j - 2) >> 1) & 1, abortp);
                         if (!ok) break;
@@ -482,21 +473,30 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                     tc_commit(su32(&bars->o_done[b]));
                     tc_commit(su32(&bars->kv_empty[s]));
                 }
-                if (j >= 2 && j - 2 + kStages < T) {   // refill the stage of tile j-2 (its P.V is long done)
-                    const int jr = j - 2;
-                    ok = mbar_wait(su32(&bars->kv_empty[jr % kStages]), (jr / kStages) & 1, abortp);
-                    if (!ok) break;
-                    issue(jr + kStages);
-                }
             }
-            if (ok) {
-                mbar_wait(su32(&bars->kv_empty[(T - 1) % kStages]), ((T - 1) / kStages) & 1, abortp);
-            } else {
-                for (int j = consumed; j < issued; ++j)
-                    mbar_drain(su32(&bars->kv_full[j % kStages]), (j / kStages) & 1);
-            }
-            tc_commit(su32(&bars->drain));
+            if (ok) mbar_wait(su32(&bars->kv_empty[(T - 1) % kStages]), ((T - 1) / kStages) & 1, abortp);
+            tc_commit(su32(&bars->drain));   // every MMA issued so far
             mbar_drain(su32(&bars->drain), 0);
+        }
+        __syncwarp();
+    } else if (warp == 6) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int j = 0; j < T; ++j) {
+                const int s = j % kStages;
+                if (j >= kStages &&   // the stage is free once the P.V of tile j - kStages completed
+                    !mbar_wait(su32(&bars->kv_empty[s]), ((j - kStages) / kStages) & 1, abortp))
+                    break;
+                const uint32_t bar = su32(&bars->kv_full[s]);
+                mbar_expect_tx(bar, kStageB);
+                tma_load_3d(sStage + s * kStageB, kmap, 0, c0 + j * kKT, g, bar);
+                tma_load_3d(sStage + s * kStageB + kTileB, vmap, 0, c0 + j * kKT, g, bar);
+                ++issued;
+            }
+            if (*abortp)   // let the copies in flight land before the CTA exits
+                for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
+                    mbar_drain(su32(&bars->kv_full[j % kStages]), (j / kStages) & 1);
         }
         __syncwarp();
     } else if (warp < 4) {

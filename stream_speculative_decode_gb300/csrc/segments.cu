@@ -106,7 +106,7 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 extern "C" {
 
-int32_t tf_chunk_keys(int32_t rows) { return 256 * (rows < 1 ? 1 : rows); }
+int32_t tf_chunk_keys(int32_t rows) { return 256 * (rows < 4 ? 4 : rows); }
 
 int tf_segments_plan(const tf_stream* streams, int n_streams, tf_plan* out) {
     if (!out) return TF_EINVAL;

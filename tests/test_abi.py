@@ -39,14 +39,14 @@ def test_strerror(T):
 
 def test_chunk_rule(T):
     for r in range(1, 17):
-        assert T.tf_chunk_keys(r) == 256 * r
+        assert T.tf_chunk_keys(r) == 256 * max(r, 4)
 
 
 def _plan_expect(streams):
     """The partial count from the documented rule: rows * 32 * chunks."""
     n = 0
     for rows, _, keys, _ in streams:
-        chunk = 256 * rows
+        chunk = 256 * max(rows, 4)
         n += rows * 32 * (-(-keys // chunk))
     return n
 
@@ -72,7 +72,7 @@ def test_partial_count(T, total_rows):
 
 
 def test_partial_count_beyond_32_bits(T):
-    streams = [(1, i, 1 << 22, 1 << 22) for i in range(8200)]
+    streams = [(1, i, 1 << 22, 1 << 22) for i in range(32800)]
     plan = T.tf_segments_plan(streams)
     assert plan["n_partials"] == _plan_expect(streams) > 2 ** 32
 

@@ -130,7 +130,7 @@ def test_step_merge_modes(mods, fused):
     rest in a merge launch; the two-call form merges everything in the merge
     kernel. Rows/keys below cover all three modes on both attention kernels."""
     tf, inputs, step, torch = mods
-    w = small_work(mods, rows=[1, 1, 2, 6, 6, 16, 3], keys=[200, 40000, 9000, 1500, 9300, 8000, 700],
+    w = small_work(mods, rows=[1, 1, 2, 6, 6, 16, 3], keys=[200, 5000, 9000, 1500, 33000, 8000, 700],
                    n_conv=1, n_attn=1, seed=14)
     inp = inputs.make_inputs(w, backend="numpy")
     d = step.DeviceStep(inp, fused_attention=fused)
@@ -147,8 +147,8 @@ def test_step_merge_modes(mods, fused):
 
 def test_step_chunk_edges(mods):
     """Key counts at, just below and just above split-K chunk multiples."""
-    rows = [1, 1, 1, 2, 2, 4, 4, 8]
-    keys = [256, 255, 257, 512, 513, 1024, 1023, 2049]
+    rows = [1, 1, 1, 2, 2, 4, 4, 8, 6]
+    keys = [1024, 1023, 1025, 2048, 2049, 1024, 1023, 2049, 1537]
     run_and_check(mods, small_work(mods, rows, keys, n_conv=1, n_attn=1, seed=6))
 
 

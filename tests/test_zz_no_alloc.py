@@ -71,14 +71,14 @@ def test_static_scratch_refuses_oversized_table(mods):
     """A table whose partials exceed the fixed array is refused with TF_ERANGE
     before anything is launched."""
     tf, inputs, step, torch = mods
-    keys = 640_000            # one 1-row stream: 2,500 chunks of 256 keys -> 20.6 MB of partials
+    rows, keys = 16, 520_000  # one 16-row stream: 127 chunks of 4,096 keys -> 17.2 MB of partials
     cap = inputs.kv_capacity(keys)
     K = torch.zeros((8, cap, 64), dtype=torch.bfloat16, device="cuda")
     V = torch.zeros((8, cap, 64), dtype=torch.bfloat16, device="cuda")
-    seg = tf.tf_segments_build([(1, 0, keys, cap)], [], None, [K.data_ptr()], [V.data_ptr()], 0, 1)
+    seg = tf.tf_segments_build([(rows, 0, keys, cap)], [], None, [K.data_ptr()], [V.data_ptr()], 0, 1)
     assert seg.partials_bytes > tf.TF_STATIC_SCRATCH_BYTES
-    q = torch.zeros((1, 32, 64), dtype=torch.bfloat16, device="cuda")
-    out = torch.zeros((1, 32, 64), dtype=torch.float32, device="cuda")
+    q = torch.zeros((rows, 32, 64), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((rows, 32, 64), dtype=torch.float32, device="cuda")
     rc = tf.lib().tf_attn_static(seg.handle, 0, q.data_ptr(), out.data_ptr(),
                                  torch.cuda.current_stream().cuda_stream)
     assert rc == tf.TF_ERANGE
