@@ -18,7 +18,7 @@
 //                    32*(qi / per) + qi % per (per = ceil(4*rows / 4)), so the
 //                    rows spread over the four lane quadrants and all four
 //                    SM sub-partitions share the softmax.
-// Per key tile j (TMEM columns: S/P double-buffered at 64*(j%2), O at 128):
+// Per key tile j (TMEM columns: S/P of tile j at 64*(j%3), O at 192):
 //   S = Q K^T      M = 128 lanes (4*rows real rows, the rest zero), N = 64
 //                  keys, K = 64: A = Q (bf16, smem), B = K tile (bf16, smem);
 //                  issued while the softmax still works on tile j-1;
@@ -27,9 +27,9 @@
 //                  more than 2^8), p = 2^(s*log2e/8 - m) packed to fp16 in
 //                  place of S;
 //   O += P V       A = P (fp16, tensor memory), B = V tile (fp16, smem,
-//                  MN-major), fp32 accumulate;
-//   l += P ones    the row sums on the tensor core too (B = a 64x16 matrix of
-//                  fp16 ones), so l sums exactly the fp16 P that P.V used.
+//                  MN-major), fp32 accumulate.
+// S/P has three buffers, so the q.K of tile j waits only for the P.V of
+// tile j-3 and is ready before the softmax reaches it.
 // At the end (m, l, O) is renormalised to the true running max and written
 // as the chunk's partial records.
 //
@@ -50,11 +50,10 @@ constexpr int kQRows = 128;                 // MMA M
 constexpr int kQB = kQRows * TF_D * 2;      // 16 KB
 constexpr int kWarps = 7;
 constexpr int kThreads = kWarps * 32;
-constexpr uint32_t kCols = 256;             // tensor-memory columns per CTA (192 used)
-constexpr uint32_t kColS = 0;               // + 64 * (tile % 2)
-constexpr uint32_t kColO = 128;             // O: 64 columns
-constexpr uint32_t kColL = 192;             // l = P . ones: 16 equal columns
-constexpr int kOnesB = 16 * kKT * 2;        // ones matrix [16][64] fp16, 2 KB
+constexpr uint32_t kCols = 256;             // tensor-memory columns per CTA
+constexpr int kSBuf = 3;                    // S/P buffers: tile j uses buffer j % 3
+constexpr uint32_t kColS = 0;               // + 64 * (tile % 3)
+constexpr uint32_t kColO = 192;             // O: 64 columns
 constexpr float kLog2e8 = 0.18033688011112042f;   // log2(e) / sqrt(64)
 constexpr float kTau = 8.f;
 constexpr unsigned long long kTimeoutNs = 2000000000ull;
@@ -64,14 +63,14 @@ struct Bars {
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
     uint64_t v_ready[kStages];   // the stage's V tile is converted to fp16
-    uint64_t s_full[2];          // per S buffer
-    uint64_t p_full[2];          // per S buffer
-    uint64_t o_done[2];          // P.V of a tile using S buffer b completed
+    uint64_t s_full[kSBuf];      // per S buffer
+    uint64_t p_full[kSBuf];      // per S buffer
+    uint64_t o_done[kSBuf];      // P.V of a tile using S buffer b completed
     uint64_t drain;
     uint32_t tmem_base;
     uint32_t abort_flag;
 };
-constexpr int kSmemBytes = 1024 + kQB + kStages * kStageB + kOnesB + int(sizeof(Bars));
+constexpr int kSmemBytes = 1024 + kQB + kStages * kStageB + int(sizeof(Bars));
 
 // Instruction descriptors, kind::f16, fp32 accumulate, M = 128, N = 64.
 //   bits 4-5 D format (1 = f32), 7-9 A format, 10-12 B format (0 = f16, 1 = bf16),
@@ -79,8 +78,6 @@ constexpr int kSmemBytes = 1024 + kQB + kStages * kStageB + kOnesB + int(sizeof(
 constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(64 >> 3) << 17) |
                               (uint32_t(128 >> 4) << 24);
 constexpr uint32_t kIdescPV = (1u << 4) | (1u << 16) | (uint32_t(64 >> 3) << 17) | (uint32_t(128 >> 4) << 24);
-// row sums of P on the tensor core: A = P (f16, tensor memory), B = ones (f16, K-major), N = 16
-constexpr uint32_t kIdescL = (1u << 4) | (uint32_t(16 >> 3) << 17) | (uint32_t(128 >> 4) << 24);
 
 // Shared-memory matrix descriptor: start address, leading / stride byte
 // offsets (16-byte units), descriptor version 1, 128-byte swizzle (layout 2).
@@ -270,6 +267,7 @@ struct SoftState {
     int T, lim, lim_all;
     bool wact;           // the warp holds at least one real query row
     float mref, mtrue;   // reference (lazy) and true running max, log2 units
+    float l;             // sum of 2^(s*log2e/8 - mref) over the keys so far
 };
 
 template <int KC>
@@ -277,9 +275,9 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
     const int lane = threadIdx.x & 31;
     Bars* bars = st.bars;
     for (int j = 0; j < st.T; ++j) {
-        const int b = j & 1;
+        const int b = j % kSBuf;
         const uint32_t colS = kColS + 64 * b;
-        if (!mbar_wait(su32(&bars->s_full[b]), (j >> 1) & 1, st.abortp)) break;
+        if (!mbar_wait(su32(&bars->s_full[b]), (j / kSBuf) & 1, st.abortp)) break;
         tc_fence_after();
         if (st.wact) {
             const int k0 = j * kKT;                  // chunk-local first key of the tile
@@ -309,15 +307,18 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
             st.mtrue = fmaxf(st.mtrue, mxs);
             const bool resc = mxs > st.mref + kTau;
             if (__any_sync(0xFFFFFFFFu, resc)) {
-                // O and l hold P.V of tiles < j; the last of them (j-1) must be done
-                if (j >= 1 && !mbar_wait(su32(&bars->o_done[(j - 1) & 1]), ((j - 1) >> 1) & 1, st.abortp))
+                // O holds P.V of tiles < j; the last of them (j-1) must be done
+                if (j >= 1 && !mbar_wait(su32(&bars->o_done[(j - 1) % kSBuf]), ((j - 1) / kSBuf) & 1, st.abortp))
                     break;
                 tc_fence_after();
                 const float alpha = resc ? ex2(st.mref - mxs) : 1.f;
-                if (resc) st.mref = mxs;
+                if (resc) {
+                    st.mref = mxs;
+                    st.l *= alpha;
+                }
                 if (j >= 1) {
 #pragma unroll 1
-                    for (int h = 0; h < 5; ++h) {   // O (64 columns) and l (16)
+                    for (int h = 0; h < 4; ++h) {   // O (64 columns)
                         uint32_t o16[16];
                         tc_ld16(st.trow + kColO + 16 * h, o16);
                         tc_wait_ld();
@@ -335,10 +336,16 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
             }
             const float mu = (st.mref == -INFINITY) ? 0.f : st.mref;
             uint32_t own[KC / 2];
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};   // four independent sums
 #pragma unroll
-            for (int c = 0; c < KC / 2; ++c)
-                own[c] = pack_h2(ex2(fmaf(v[2 * c], kLog2e8, -mu)), ex2(fmaf(v[2 * c + 1], kLog2e8, -mu)));
+            for (int c = 0; c < KC / 2; ++c) {
+                const float p0 = ex2(fmaf(v[2 * c], kLog2e8, -mu));
+                const float p1 = ex2(fmaf(v[2 * c + 1], kLog2e8, -mu));
+                s4[c & 3] += p0 + p1;
+                own[c] = pack_h2(p0, p1);
+            }
             tc_st_n<KC / 2>(st.trow + colS, own);   // P (fp16 pairs) over the first KC/2 columns of S
+            st.l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
             tc_wait_st();
         }
         tc_fence_before();
@@ -356,8 +363,7 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
     unsigned char* gbase = smem_raw + (base - raw);
     const uint32_t sQ = base;
     const uint32_t sStage = base + kQB;
-    const uint32_t sOnes = base + kQB + kStages * kStageB;   // 1 KB aligned
-    Bars* bars = reinterpret_cast<Bars*>(gbase + kQB + kStages * kStageB + kOnesB);
+    Bars* bars = reinterpret_cast<Bars*>(gbase + kQB + kStages * kStageB);
     volatile uint32_t* abortp = &bars->abort_flag;
 
     const int item_idx = t.n_items_mma + blockIdx.x / TF_NKV;   // tensor-core items follow the mma.sync ones
@@ -383,7 +389,7 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
             mbar_init(su32(&bars->kv_empty[s]), 1);
             mbar_init(su32(&bars->v_ready[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < kSBuf; ++b) {
             mbar_init(su32(&bars->s_full[b]), 1);
             mbar_init(su32(&bars->p_full[b]), 4);   // the 4 softmax warps
             mbar_init(su32(&bars->o_done[b]), 1);
@@ -409,8 +415,6 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                     q + ((size_t(st.row_offset + (qq >> 2)) * TF_NQ + 4 * g + (qq & 3)) * TF_D + ch * 8));
             sts128(sQ + L * 128 + ((ch ^ (L & 7)) << 4), v);
         }
-        for (int idx = tid; idx < kOnesB / 16; idx += 128)   // fp16 1.0 = 0x3C00 everywhere
-            sts128(sOnes + idx * 16, make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u));
         fence_async_smem();
     }
     tc_fence_before();
@@ -433,6 +437,7 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
     ss.wact = wact;
     ss.mref = -INFINITY;
     ss.mtrue = -INFINITY;
+    ss.l = 0.f;
 
     if (warp == 4) {
         // ------------------------------------------------------------ control
@@ -441,11 +446,11 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
             bool ok = true;
             for (int j = 0; j <= T && ok; ++j) {
                 if (j < T) {
-                    const int s = j % kStages, b = j & 1;
+                    const int s = j % kStages, b = j % kSBuf;
                     ok = mbar_wait(su32(&bars->kv_full[s]), (j / kStages) & 1, abortp);
                     if (!ok) break;
-                    if (j >= 2) {   // P.V(j-2) has released S buffer b
-                        ok = mbar_wait(su32(&bars->o_done[b]), ((j - 2) >> 1) & 1, abortp);
+                    if (j >= kSBuf) {   // P.V(j-3) has released S buffer b
+                        ok = mbar_wait(su32(&bars->o_done[b]), ((j - kSBuf) / kSBuf) & 1, abortp);
                         if (!ok) break;
                     }
                     tc_fence_after();
@@ -456,20 +461,17 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                     tc_commit(su32(&bars->s_full[b]));
                 }
                 if (j >= 1) {
-                    const int jj = j - 1, s = jj % kStages, b = jj & 1;
-                    ok = mbar_wait(su32(&bars->p_full[b]), (jj >> 1) & 1, abortp);
+                    const int jj = j - 1, s = jj % kStages, b = jj % kSBuf;
+                    ok = mbar_wait(su32(&bars->p_full[b]), (jj / kSBuf) & 1, abortp);
                     if (!ok) break;
                     ok = mbar_wait(su32(&bars->v_ready[s]), (jj / kStages) & 1, abortp);
                     if (!ok) break;
                     tc_fence_after();
                     const uint64_t dv = sdesc(sStage + s * kStageB + kTileB, kTileB, 1024);
-                    const uint64_t dl = sdesc(sOnes, 16, 1024);
 #pragma unroll
-                    for (int k = 0; k < kKT / 16; ++k) {   // 64 keys: 4 steps of 16 (2 KB of V rows)
-                        const uint32_t acc = (jj > 0 || k > 0) ? 1u : 0u;
-                        tc_mma_ts(tmem + kColO, tmem + kColS + 64 * b + 8 * k, dv + 128 * k, kIdescPV, acc);
-                        tc_mma_ts(tmem + kColL, tmem + kColS + 64 * b + 8 * k, dl + 2 * k, kIdescL, acc);
-                    }
+                    for (int k = 0; k < kKT / 16; ++k)   // 64 keys: 4 steps of 16 (2 KB of V rows)
+                        tc_mma_ts(tmem + kColO, tmem + kColS + 64 * b + 8 * k, dv + 128 * k, kIdescPV,
+                                  (jj > 0 || k > 0) ? 1u : 0u);
                     tc_commit(su32(&bars->o_done[b]));
                     tc_commit(su32(&bars->kv_empty[s]));
                 }
@@ -502,7 +504,7 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
     } else if (warp < 4) {
         // ------------------------------------------------------------ softmax
         softmax_tiles<kKT>(ss);
-        if (!*abortp) mbar_wait(su32(&bars->o_done[(T - 1) & 1]), ((T - 1) >> 1) & 1, abortp);
+        if (!*abortp) mbar_wait(su32(&bars->o_done[(T - 1) % kSBuf]), ((T - 1) / kSBuf) & 1, abortp);
     } else {
         // ------------------------------------------------------------ V tiles bf16 -> fp16
         for (int j = 0; j < T; ++j) {
@@ -536,11 +538,10 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
         const bool aborted = *abortp != 0;
         float f = 1.f;
         if (ss.mtrue > ss.mref && ss.mref != -INFINITY) f = ex2(ss.mref - ss.mtrue);
-        uint32_t ro[64], rl[16];
+        uint32_t ro[64];
         tc_ld64(trow + kColO, ro);
-        tc_ld16(trow + kColL, rl);
         tc_wait_ld();
-        const float lsum = __uint_as_float(rl[0]);
+        const float lsum = ss.l;
         float o[64];
 #pragma unroll
         for (int d = 0; d < 64; ++d) o[d] = __uint_as_float(ro[d]);
