@@ -13,6 +13,8 @@ Sources (web pages about the TensorFold project):
     "kernel contract: ... four planted controls".
   * PR #1391 "lfm2: draft with LiquidAI's DSpark drafter (--drafter)": "The lane
     core verifies every draft"; the target keeps its causal count.
+  * The same PR's drafter side (``oracle/draft.py``): the Markov head's pick
+    and the copy of the drafter's picks into the verify's ids.
   * Issue #1374 "LFM2.5-24B-A2B on Metal: drafts with LiquidAI's DSpark drafter
     (proposal and gate)", section "What": a drafted reply equals its plain one.
 
@@ -32,4 +34,8 @@ from .step import (  # noqa: F401
     attention_stream, attention_partials_stream, merge_partials, attention_layer,
     argmax_rows, accept_stream, accept_all, rewind_state,
     verify_step,
+)
+from .draft import (  # noqa: F401
+    f64_to_bf16_rne_any, markov_step, markov_chain, markov_all,
+    DFLAG_BAD_PENDING, DFLAG_BAD_DRAFT, draft_ids_all,
 )

@@ -130,7 +130,7 @@ def conv_layer(streams, bcx, w, states, want_history=True):
 
 # ------------------------------------------------------- a2/a3: attention
 
-def _visible(keys, rows, i):
+def _visible(keys, rows, i, full=False):
     """Keys row i of a window of ``rows`` rows sees: [0, keys - rows + i + 1).
 
     Reading: ``keys`` counts the cache entries INCLUDING the window's own rows
@@ -138,12 +138,21 @@ def _visible(keys, rows, i):
     ``keys - rows + i`` and attends causally to itself and every earlier key.
     Source: PR #1391 "lfm2: draft with LiquidAI's DSpark drafter": the target's
     attention instantiations "keep their causal count".
+
+    ``full``: the drafter's block attention (same PR: the attention and merge
+    kernels "with a FULL template flag", every block row seeing the keys
+    ``[0, len + 1)``). Reading: ``len + 1`` is the key count including the
+    block's own rows, so every row sees all ``keys`` keys -- what the block's
+    last row sees under the causal count.
     """
+    if full:
+        return keys
     return keys - rows + i + 1
 
 
-def attention_stream(q, K, V, keys, rows):
-    """Causal GQA attention of one stream's window rows, in float64.
+def attention_stream(q, K, V, keys, rows, full=False):
+    """Causal (or, with ``full``, non-causal block) GQA attention of one
+    stream's window rows, in float64.
 
     Source: PR #1377 "LFM2: shared-round decode", commit "a shared round runs
     each layer's conv and attention once over all its streams": the stream
@@ -161,7 +170,7 @@ def attention_stream(q, K, V, keys, rows):
     Vf = [bf16_to_f64(V[g, :keys]) for g in range(NKV)]
     qf = bf16_to_f64(q)
     for i in range(rows):
-        n = _visible(keys, rows, i)
+        n = _visible(keys, rows, i, full)
         for h in range(NQ):
             g = h // GROUP
             s = (Kf[g][:n] @ qf[i, h]) * SCALE
@@ -171,7 +180,7 @@ def attention_stream(q, K, V, keys, rows):
     return out
 
 
-def attention_partials_stream(q, K, V, keys, rows, chunk):
+def attention_partials_stream(q, K, V, keys, rows, chunk, full=False):
     """Split-K partials of one stream: per row, head and key chunk (m, l, o).
 
     Chunk c covers keys [c*chunk, (c+1)*chunk) intersected with the row's
@@ -197,7 +206,7 @@ def attention_partials_stream(q, K, V, keys, rows, chunk):
         Kg = bf16_to_f64(K[g, :keys])
         Vg = bf16_to_f64(V[g, :keys])
         for i in range(rows):
-            n = _visible(keys, rows, i)
+            n = _visible(keys, rows, i, full)
             for c in range(n_chunks):
                 lo, hi = c * chunk, min((c + 1) * chunk, n)
                 if lo >= hi:
@@ -231,8 +240,9 @@ def merge_partials(m, l, o):
     return (wgt[..., None] * o).sum(axis=-2) / L[..., None]
 
 
-def attention_layer(streams, q, Ks, Vs):
-    """One attention layer over every row of every stream, stream by stream.
+def attention_layer(streams, q, Ks, Vs, full=False):
+    """One attention layer over every row of every stream, stream by stream
+    (``full``: the non-causal block form of ``_visible``).
 
     ``q`` holds all R rows packed stream after stream; ``Ks[s]``, ``Vs[s]`` are
     stream s's caches. Returns out float64 [R][NQ][D].
@@ -240,7 +250,7 @@ def attention_layer(streams, q, Ks, Vs):
     R = q.shape[0]
     out = np.empty((R, NQ, D), dtype=np.float64)
     for s, (rows, off, keys) in enumerate(streams):
-        out[off:off + rows] = attention_stream(q[off:off + rows], Ks[s], Vs[s], keys, rows)
+        out[off:off + rows] = attention_stream(q[off:off + rows], Ks[s], Vs[s], keys, rows, full)
     return out
 
 

@@ -304,6 +304,75 @@ def pin_attn_brute(impl):
                 assert abs(out[i, h, d] - want) <= 1e-12 * (1 + abs(want))
 
 
+# ------------------------------------------------------ block (FULL) attention
+
+def pin_attn_full_q_zero(impl):
+    """FULL block attention with q = 0: every row's scores are equal, so every
+    row returns the mean of ALL the stream's V (keys [0, keys)), the window's
+    own rows included. A block row missing the last key fails this."""
+    rng = np.random.default_rng(41)
+    rows, keys = 5, 23
+    _, K, V = _attn_inputs(rng, rows, keys, cap=keys + 9)
+    q = np.zeros((rows, NQ, D), dtype=np.uint16)
+    out = impl.attention_stream(q, K, V, keys, rows, full=True)
+    Vf = bits_f64(V)
+    for i in range(rows):
+        for h in range(NQ):
+            assert np.allclose(out[i, h], Vf[h // 4, :keys].mean(axis=0), rtol=0, atol=1e-13), (i, h)
+
+
+def pin_attn_full_brute(impl):
+    """FULL block attention on a tiny case against scipy's softmax over every
+    key (a library routine), row by row, with the 1/8 score scale."""
+    from scipy.special import softmax
+    rng = np.random.default_rng(42)
+    rows, keys = 3, 6
+    q, K, V = _attn_inputs(rng, rows, keys)
+    out = impl.attention_stream(q, K, V, keys, rows, full=True)
+    qf, Kf, Vf = bits_f64(q), bits_f64(K), bits_f64(V)
+    for i in range(rows):
+        for h in range(NQ):
+            g = h // 4
+            wts = softmax(np.array([float(np.dot(qf[i, h], Kf[g, j])) / 8.0 for j in range(keys)]))
+            want = (wts[:, None] * Vf[g, :keys]).sum(axis=0)
+            assert np.allclose(out[i, h], want, rtol=0, atol=1e-12), (i, h)
+
+
+def pin_attn_full_split_merge(impl):
+    """FULL partials merged by log-sum-exp equal the unsplit FULL softmax, and
+    no chunk of a FULL row is empty."""
+    rng = np.random.default_rng(43)
+    rows, keys = 4, 50
+    q, K, V = _attn_inputs(rng, rows, keys)
+    whole = impl.attention_stream(q, K, V, keys, rows, full=True)
+    for chunk in (1, 9, 16, 49, 50, 64):
+        m, l, o = impl.attention_partials_stream(q, K, V, keys, rows, chunk, full=True)
+        assert np.all(l > 0), chunk
+        assert np.allclose(impl.merge_partials(m, l, o), whole, rtol=0, atol=1e-12), chunk
+
+
+def pin_attn_full_layer(impl):
+    """A FULL layer over several streams: each stream's rows see exactly that
+    stream's keys -- the last stream's planted last key moves all of its rows
+    and nothing of the others."""
+    rng = np.random.default_rng(44)
+    shapes = [(2, 7), (3, 11), (4, 4)]
+    streams, off = [], 0
+    for r, k in shapes:
+        streams.append((r, off, k))
+        off += r
+    q = rand_bf16(rng, (off, NQ, D))
+    Ks = [rand_bf16(rng, (NKV, k, D)) for _, k in shapes]
+    Vs = [rand_bf16(rng, (NKV, k, D)) for _, k in shapes]
+    a = impl.attention_layer(streams, q, Ks, Vs, full=True)
+    Vs2 = [v.copy() for v in Vs]
+    Vs2[2][:, 3] = rand_bf16(rng, (NKV, D), std=4.0)
+    b = impl.attention_layer(streams, q, Ks, Vs2, full=True)
+    assert np.array_equal(a[:5], b[:5])
+    for i in range(5, 9):
+        assert not np.allclose(a[i], b[i]), i
+
+
 # ------------------------------------------------------------------ argmax
 
 def pin_argmax_golden(impl):
@@ -412,6 +481,7 @@ ALL_PINS = [
     pin_conv_causal, pin_rewind,
     pin_attn_one_key, pin_attn_q_zero, pin_attn_two_keys_scale, pin_attn_gqa,
     pin_attn_causal_edge, pin_attn_split_merge, pin_attn_permutation, pin_attn_brute,
+    pin_attn_full_q_zero, pin_attn_full_brute, pin_attn_full_split_merge, pin_attn_full_layer,
     pin_argmax_golden, pin_argmax_brute,
     pin_accept_cases, pin_accept_recipe,
     pin_segmented_equals_alone,

@@ -4,6 +4,11 @@ shared-round decode", commit "kernel contract: LFM2's shared-round launches
 carry recorded M1/M2 limits and four planted controls": a tie to the highest
 id, a nonfinite logit not flagged, every stream reading or writing the first
 stream's conv state or KV cache); the rest guard the readings the pins fix.
+The draft side's controls follow the pages' drafter contract (PR #1391 "lfm2:
+draft with LiquidAI's DSpark drafter", the commit that gives the Markov scan and
+pick, the draft ids and the block attention their planted controls: a NaN score
+not flagged, every stream reading the first stream's previous token, a pick
+past the vocabulary keeping its token, a block row missing the last key).
 The mistakes are planted in the oracle's source, on the CPU.
 """
 
@@ -12,12 +17,15 @@ import types
 
 import pytest
 
+import oracle.draft as oracle_draft
 import oracle.step as oracle_step
 import oracle_pins as P
+import oracle_pins_draft as PD
 
 
-def mutant(*edits):
-    src = inspect.getsource(oracle_step)
+def mutant(*edits, module=oracle_step):
+    src = inspect.getsource(module)
+    src = src.replace("from .step import", "from oracle.step import")
     for old, new in edits:
         assert src.count(old) == 1, old
         src = src.replace(old, new)
@@ -42,8 +50,8 @@ CONTROLS = {
         [("        new_states.append(st)\n", "        new_states[0:1] = [st]\n")],
         [P.pin_segmented_equals_alone]),
     "streams_read_first_kv_cache": (
-        [("attention_stream(q[off:off + rows], Ks[s], Vs[s], keys, rows)",
-          "attention_stream(q[off:off + rows], Ks[0], Vs[0], keys, rows)")],
+        [("attention_stream(q[off:off + rows], Ks[s], Vs[s], keys, rows, full)",
+          "attention_stream(q[off:off + rows], Ks[0], Vs[0], keys, rows, full)")],
         [P.pin_segmented_equals_alone]),
     "conv_taps_reversed": (
         [("conv = (wf[:, 0] * bf16_to_f64(seq[i])", "conv = (wf[:, 2] * bf16_to_f64(seq[i])"),
@@ -74,6 +82,47 @@ CONTROLS = {
     "rewind_one_row_early": (
         [("return np.stack([history[a + 1], history[a + 2]])", "return np.stack([history[a], history[a + 1]])")],
         [P.pin_rewind]),
+    "block_row_missing_last_key": (
+        [("    if full:\n        return keys\n", "    if full:\n        return keys - 1\n")],
+        [P.pin_attn_full_q_zero, P.pin_attn_full_brute]),
+    "block_rows_causal": (
+        [("    if full:\n        return keys\n", "    if False:\n        return keys\n")],
+        [P.pin_attn_full_q_zero, P.pin_attn_full_split_merge]),
+}
+
+DRAFT_CONTROLS = {
+    "markov_nan_score_not_flagged": (
+        [("    if not np.all(np.isfinite(score)):\n", "    if False:\n")],
+        [PD.pin_markov_worked]),
+    "markov_tie_to_highest_token": (
+        [("int(np.argmax(score))", "int(len(score) - 1 - np.argmax(score[::-1]))")],
+        [PD.pin_markov_worked]),
+    "markov_chain_stuck_on_pending_token": (
+        [("        prev = p\n", "")],
+        [PD.pin_markov_worked, PD.pin_markov_permutation_chain]),
+    "markov_dot_not_rounded": (
+        [("dot16 = bf16_to_f64(f64_to_bf16_rne_any(dot))", "dot16 = dot")],
+        [PD.pin_markov_worked, PD.pin_markov_brute]),
+    "markov_w2_column_for_row": (
+        [("dot = bf16_to_f64(W2) @ e", "dot = bf16_to_f64(W2).T[:, :len(e)] @ e if W2.shape[0] == W2.shape[1] else bf16_to_f64(W2) @ e")],
+        [PD.pin_markov_permutation_chain]),
+    "markov_streams_read_first_pending_token": (
+        [("markov_chain(base[b:b + rows - 1], W1, W2, prev[s])", "markov_chain(base[b:b + rows - 1], W1, W2, prev[0])")],
+        [PD.pin_markov_streams]),
+    "rounding_through_binary32": (
+        [("r = np.rint(v / quantum) * quantum", "r = np.rint(float(np.float32(v)) / quantum) * quantum")],
+        [PD.pin_bf16_any_golden, PD.pin_bf16_any_brute]),
+    "draft_ids_streams_read_first_pending_token": (
+        [("p = int(prev[s])", "p = int(prev[0])")],
+        [PD.pin_draft_ids_golden]),
+    "draft_ids_pick_past_vocab_keeps_token": (
+        [("bad = (draft_flag is not None and draft_flag[k]) or not (0 <= d < vocab)",
+          "bad = draft_flag is not None and draft_flag[k]")],
+        [PD.pin_draft_ids_golden]),
+    "draft_ids_flagged_pick_copied": (
+        [("bad = (draft_flag is not None and draft_flag[k]) or not (0 <= d < vocab)",
+          "bad = not (0 <= d < vocab)")],
+        [PD.pin_draft_ids_golden]),
 }
 
 
@@ -81,6 +130,15 @@ CONTROLS = {
 def test_planted_control_goes_red(name):
     edits, pins = CONTROLS[name]
     mod = mutant(*edits)
+    for pin in pins:
+        with pytest.raises(Exception):
+            pin(mod)
+
+
+@pytest.mark.parametrize("name", sorted(DRAFT_CONTROLS))
+def test_planted_draft_control_goes_red(name):
+    edits, pins = DRAFT_CONTROLS[name]
+    mod = mutant(*edits, module=oracle_draft)
     for pin in pins:
         with pytest.raises(Exception):
             pin(mod)
