@@ -18,7 +18,13 @@
  *             per-stream partials; a table reaching memory it did not declare).
  *   [DSP]   PR #1391 "lfm2: draft with LiquidAI's DSpark drafter (--drafter)":
  *           the lane core verifies every draft; the target's attention keeps
- *           its causal count.
+ *           its causal count; the drafter's block attention ("a FULL template
+ *           flag, every block row seeing the keys [0, len + 1)"), its Markov
+ *           head ("adds W2 W1[previous token] to each row's logits and takes
+ *           the argmax, one row after the other"; the step as the argmax of
+ *           bf16(base + bf16(W2 . W1[prev])), ties to the lowest token, a NaN
+ *           score flagged) and the held path's copy of the drafter's picks
+ *           into the verify's ids (a bad pick "sets a flag the verify reads").
  *
  * Conventions for every call:
  *   - All tensors are dense, row-major, in DEVICE memory owned by the caller,
@@ -51,6 +57,7 @@ extern "C" {
 #define TF_MAX_ROWS 16          /* window rows per stream (1 + drafts) */
 #define TF_MAX_KEYS (1 << 22)   /* cache rows per stream */
 #define TF_MAX_STREAMS 65536
+#define TF_MK       256         /* width of the drafter's Markov head rows (W1, W2) */
 
 typedef enum {
     TF_OK = 0,
@@ -194,6 +201,18 @@ int tf_attn_partials(const tf_segments* seg, int attn_layer, const void* q,
 int tf_attn(const tf_segments* seg, int attn_layer, const void* q, void* partials, float* out,
             tf_cuda_stream stream);
 
+/* The drafter's non-causal block attention ([DSP] lfm2_attn_block: the
+ * target's attention "with a FULL template flag, every block row seeing the
+ * keys [0, len + 1)"). Reading: len + 1 is the stream's key count including
+ * the block's own rows, so every window row sees all `keys` keys of its
+ * stream (what the last row sees under the causal count). Same arguments,
+ * records, kernels, chunking and errors as tf_attn_partials / tf_attn; the
+ * merge (tf_attn_merge) is shared. */
+int tf_attn_block_partials(const tf_segments* seg, int attn_layer, const void* q,
+                           void* partials, tf_cuda_stream stream);
+int tf_attn_block(const tf_segments* seg, int attn_layer, const void* q, void* partials,
+                  float* out, tf_cuda_stream stream);
+
 /* a3. Log-sum-exp merge of the partials into the attention output
  * ([SRD] lfm2_merge_row): out = sum_c 2^(m_c - M) o_c / sum_c 2^(m_c - M) l_c,
  * M = max_c m_c, empty chunks skipped.
@@ -253,6 +272,51 @@ int tf_accept(const tf_segments* seg, const int32_t* ids, const int32_t* pick,
               const uint8_t* flag, int vocab, int32_t* accept_len,
               int32_t* next_token, int32_t* new_keys, uint8_t* sflag,
               int rewind_conv, tf_cuda_stream stream);
+
+/* The drafter's Markov head over the draft rows of a verify table ([DSP]
+ * lfm2_markov_scan / lfm2_markov_pick). Stream s drafts rows_s - 1 tokens;
+ * its block rows are packed stream after stream at draft row o_s - s (o_s its
+ * window's row offset), R - S rows in all. Block row j of stream s scores
+ *   score[v] = bf16(base[v] + bf16(W2[v] . W1[tok]))     (v < vocab)
+ * with tok = prev[s] for j = 0 and the pick of row j-1 after that ("one row
+ * after the other"); the dot accumulates in fp32 on the tensor cores and is
+ * rounded to nearest even, as is the sum. The pick is the lowest token with
+ * the largest score.
+ *   W1, W2      bf16 [vocab][TF_MK]
+ *   base        bf16 logits, draft row k at base + k*base_stride (elements)
+ *   prev        int32 [S]: each stream's pending token
+ *   pick        int32 [R - S]: the row's pick, -1 when flagged
+ *   flag        uint8 [R - S]: bit 0 a nonfinite score in the row, or no
+ *               valid previous token (outside [0, vocab), e.g. a flagged row
+ *               before it); bit 1 the kernel gave up waiting for its own
+ *               copies or MMAs (more than 2 s; the row is not computed)
+ * One launch per step (rows_max - 1 launches), each reading W2 once for up to
+ * 128 streams. The table holds the cross-CTA scratch: calls on one table must
+ * not overlap on the GPU. Errors: TF_EINVAL (null, misaligned W2 or base,
+ * base_stride < vocab or not a multiple of 8, vocab < 1), TF_ERANGE
+ * (vocab > 2^24). */
+int tf_markov_chain(const tf_segments* seg, const void* W1, const void* W2, int vocab,
+                    const void* base, int64_t base_stride, const int32_t* prev,
+                    int32_t* pick, uint8_t* flag, tf_cuda_stream stream);
+
+/* The next verify's ids from each stream's pending token and the drafter's
+ * picks ([DSP] lfm2_draft_ids, on the GPU so that the host reads no pick
+ * between the drafter and the verify). Window row 0 of stream s is prev[s];
+ * window row j >= 1 is the draft at packed draft row o_s - s + j - 1 (the
+ * layout tf_markov_chain writes). A token outside [0, vocab), or a draft whose
+ * draft_flag is nonzero, is written as -1 (the verify never accepts it).
+ *   prev        int32 [S] (e.g. tf_accept's next_token)
+ *   drafts      int32 [R - S]; may be NULL when every window has one row
+ *   draft_flag  uint8 [R - S] or NULL
+ *   ids         int32 [R]: the verify's ids
+ *   dflag       uint8 [S]: bit 0 (TF_DFLAG_BAD_PENDING) the pending token was
+ *               bad, bit 1 (TF_DFLAG_BAD_DRAFT) a draft was bad
+ * Errors: TF_EINVAL (null, vocab < 1). */
+#define TF_DFLAG_BAD_PENDING 1
+#define TF_DFLAG_BAD_DRAFT   2
+int tf_draft_ids(const tf_segments* seg, const int32_t* prev, const int32_t* drafts,
+                 const uint8_t* draft_flag, int vocab, int32_t* ids, uint8_t* dflag,
+                 tf_cuda_stream stream);
 
 /* Name of a status code. */
 const char* tf_strerror(int status);

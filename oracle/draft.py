@@ -41,18 +41,13 @@ def f64_to_bf16_rne_any(x):
     the sign of zero is kept.
     """
     x = np.asarray(x, dtype=np.float64)
-    out = np.empty(x.shape, dtype=np.float64)
-    flat, res = x.ravel(), out.ravel()
-    for k, v in enumerate(flat):
-        if not np.isfinite(v) or v == 0.0:
-            res[k] = v
-            continue
-        _m, e = np.frexp(v)              # |v| = |m| * 2^e, 0.5 <= |m| < 1
-        quantum = np.ldexp(1.0, max(int(e) - 8, -133))
-        r = np.rint(v / quantum) * quantum
-        if abs(r) >= _BF16_OVERFLOW:
-            r = np.copysign(np.inf, v)
-        res[k] = r
+    out = x.copy()
+    fin = np.isfinite(x) & (x != 0.0)
+    v = x[fin]
+    _m, e = np.frexp(v)                  # |v| = |m| * 2^e, 0.5 <= |m| < 1
+    quantum = np.ldexp(1.0, np.maximum(e - 8, -133))
+    r = np.rint(v / quantum) * quantum
+    out[fin] = np.where(np.abs(r) >= _BF16_OVERFLOW, np.copysign(np.inf, v), r)
     f32 = out.astype(np.float32)         # exact: every bf16 value is a binary32 value
     bits = (f32.view(np.uint32) >> np.uint32(16)).astype(np.uint16)
     nan = np.isnan(out)

@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libtf.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["segments.cu", "conv.cu", "attn.cu", "attn_tc.cu", "attn_static.cu", "argmax.cu", "accept.cu"]
+SOURCES = ["segments.cu", "conv.cu", "attn.cu", "attn_tc.cu", "attn_static.cu", "argmax.cu", "accept.cu",
+           "draft.cu", "markov.cu"]
 
 
 def nvcc_path():

@@ -22,6 +22,12 @@
 //
 // HBM bound: 256 bytes of K+V per key per KV head; the window's queries ride
 // along. Arithmetic intensity 4*rows flops per byte for each of q.k and P.V.
+//
+// The same kernels serve the drafter's block attention (PR #1391: the target's
+// attention and merge "with a FULL template flag", every block row seeing the
+// keys [0, len + 1)): with `full` set every window row sees all of the
+// stream's keys instead of its causal count; nothing else changes, and the
+// merge is shared (it reads only the records).
 #include "tf_internal.cuh"
 
 namespace tf {
@@ -89,7 +95,8 @@ __device__ __forceinline__ uint32_t swz(int r, int ch) { return uint32_t(r * kRo
 template <int MT>
 __global__ void __launch_bounds__(kThreads)
 attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
-                     float* __restrict__ part_o, float2* __restrict__ part_ml, float* __restrict__ out) {
+                     float* __restrict__ part_o, float2* __restrict__ part_ml, float* __restrict__ out,
+                     int full) {
     extern __shared__ __align__(128) unsigned char smem[];
     constexpr bool kQReg = MT <= 2;
     const int item_idx = blockIdx.x / TF_NKV;
@@ -139,7 +146,9 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
     float o[MT][8][4];
     float m[MT][2], l[MT][2], mtrue[MT][2];   // m: reference max; mtrue: running max
     int lim[MT][2];
-    const int lim_all = st.keys - st.rows + 1 - c0;   // keys every real row sees (chunk-local)
+    // keys every real row sees (chunk-local): row 0's causal count, or every
+    // key for a FULL block
+    const int lim_all = (full ? st.keys : st.keys - st.rows + 1) - c0;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
@@ -152,8 +161,9 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
             mtrue[mt][r] = -INFINITY;
             l[mt][r] = 0.f;
             const int qi = mt * 16 + g8 + 8 * r;
-            // chunk-local bound of the keys row qi/4 sees (causal), 0 for padding rows
-            const int vis = st.keys - st.rows + (qi >> 2) + 1 - c0;
+            // chunk-local bound of the keys row qi/4 sees (causal, or all keys
+            // for a FULL block), 0 for padding rows
+            const int vis = (full ? st.keys : st.keys - st.rows + (qi >> 2) + 1) - c0;
             lim[mt][r] = qi < nq ? max(0, min(vis, nkeys)) : 0;
         }
     }
@@ -461,19 +471,19 @@ int attn_prepare() {
 // Launchers for other translation units: the partials and the merge of one
 // attention layer with the partial records at `po` (o) and `pml` (m, l).
 int launch_attn_partials(const SegTable& t, int layer, const uint16_t* q, float* po, float2* pml,
-                         cudaStream_t stream, float* out) {
+                         cudaStream_t stream, float* out, int full) {
     if (t.n_items_mma > 0) {
         const dim3 grid(t.n_items_mma * TF_NKV);
         int rc;
         switch (t.mma_mt) {
-            case 1: rc = launch_pdl(attn_partials_kernel<1>, grid, dim3(kThreads), smem_bytes(1), stream, t, layer, q, po, pml, out); break;
-            case 2: rc = launch_pdl(attn_partials_kernel<2>, grid, dim3(kThreads), smem_bytes(2), stream, t, layer, q, po, pml, out); break;
-            case 3: rc = launch_pdl(attn_partials_kernel<3>, grid, dim3(kThreads), smem_bytes(3), stream, t, layer, q, po, pml, out); break;
-            default: rc = launch_pdl(attn_partials_kernel<4>, grid, dim3(kThreads), smem_bytes(4), stream, t, layer, q, po, pml, out); break;
+            case 1: rc = launch_pdl(attn_partials_kernel<1>, grid, dim3(kThreads), smem_bytes(1), stream, t, layer, q, po, pml, out, full); break;
+            case 2: rc = launch_pdl(attn_partials_kernel<2>, grid, dim3(kThreads), smem_bytes(2), stream, t, layer, q, po, pml, out, full); break;
+            case 3: rc = launch_pdl(attn_partials_kernel<3>, grid, dim3(kThreads), smem_bytes(3), stream, t, layer, q, po, pml, out, full); break;
+            default: rc = launch_pdl(attn_partials_kernel<4>, grid, dim3(kThreads), smem_bytes(4), stream, t, layer, q, po, pml, out, full); break;
         }
         if (rc != TF_OK) return rc;
     }
-    if (t.n_items_mma < t.n_items) return launch_attn_partials_tc(t, layer, q, po, pml, stream, out);
+    if (t.n_items_mma < t.n_items) return launch_attn_partials_tc(t, layer, q, po, pml, stream, out, full);
     return TF_OK;
 }
 
@@ -509,6 +519,34 @@ extern "C" int tf_attn(const tf_segments* seg, int attn_layer, const void* q, vo
     float* po = static_cast<float*>(partials);
     float2* pml = reinterpret_cast<float2*>(po + t.n_partials * TF_D);
     int rc = launch_attn_partials(t, attn_layer, static_cast<const uint16_t*>(q), po, pml, stream, out);
+    if (rc != TF_OK || t.n_merge_rows == 0) return rc;
+    return launch_attn_merge(t, po, pml, out, stream, true);
+}
+
+extern "C" int tf_attn_block_partials(const tf_segments* seg, int attn_layer, const void* q, void* partials,
+                                      tf_cuda_stream stream) {
+    using namespace tf;
+    if (!seg) return TF_EINVAL;
+    const SegTable& t = seg->dev;
+    if (attn_layer < 0 || attn_layer >= t.n_attn) return TF_EINVAL;
+    if (t.R == 0) return TF_OK;
+    if (!q || !partials || !aligned16(q) || !aligned16(partials)) return TF_EINVAL;
+    float* po = static_cast<float*>(partials);
+    float2* pml = reinterpret_cast<float2*>(po + t.n_partials * TF_D);
+    return launch_attn_partials(t, attn_layer, static_cast<const uint16_t*>(q), po, pml, stream, nullptr, 1);
+}
+
+extern "C" int tf_attn_block(const tf_segments* seg, int attn_layer, const void* q, void* partials, float* out,
+                             tf_cuda_stream stream) {
+    using namespace tf;
+    if (!seg) return TF_EINVAL;
+    const SegTable& t = seg->dev;
+    if (attn_layer < 0 || attn_layer >= t.n_attn) return TF_EINVAL;
+    if (t.R == 0) return TF_OK;
+    if (!q || !partials || !out || !aligned16(q) || !aligned16(partials) || !aligned16(out)) return TF_EINVAL;
+    float* po = static_cast<float*>(partials);
+    float2* pml = reinterpret_cast<float2*>(po + t.n_partials * TF_D);
+    int rc = launch_attn_partials(t, attn_layer, static_cast<const uint16_t*>(q), po, pml, stream, out, 1);
     if (rc != TF_OK || t.n_merge_rows == 0) return rc;
     return launch_attn_merge(t, po, pml, out, stream, true);
 }

@@ -5,7 +5,9 @@
 // attn.cu (PR #1377 "LFM2: shared-round decode": one launch a layer over every
 // row from the segment table, per-stream partials; PR #1391: causal count),
 // used when a window holds 3 rows or more, where q.K and P.V are real
-// contractions (4*rows flops per byte of K/V each).
+// contractions (4*rows flops per byte of K/V each). With `full` set it is the
+// drafter's non-causal block attention (PR #1391: every block row sees the
+// keys [0, len + 1)): only the per-row key bounds change.
 //
 // One CTA per (work item = one stream's key chunk, KV head), 7 warps:
 //   warp 6, lane 0   TMA loads of K/V tiles (64 keys = 8 KB each, 128-byte
@@ -37,7 +39,7 @@
 // CTA raises a shared abort flag, waits (bounded) for its TMA copies and MMAs
 // in flight, writes NaN records (so the merged output shows the failure),
 // frees its tensor memory and returns.
-#include "tf_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace tf {
 namespace {
@@ -56,8 +58,6 @@ constexpr uint32_t kColS = 0;               // + 64 * (tile % 3)
 constexpr uint32_t kColO = 192;             // O: 64 columns
 constexpr float kLog2e8 = 0.18033688011112042f;   // log2(e) / sqrt(64)
 constexpr float kTau = 8.f;
-constexpr unsigned long long kTimeoutNs = 2000000000ull;
-constexpr unsigned long long kDrainNs = 200000000ull;
 
 struct Bars {
     uint64_t kv_full[kStages];
@@ -79,168 +79,6 @@ constexpr uint32_t kIdescQK = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(64 
                               (uint32_t(128 >> 4) << 24);
 constexpr uint32_t kIdescPV = (1u << 4) | (1u << 16) | (uint32_t(64 >> 3) << 17) | (uint32_t(128 >> 4) << 24);
 
-// Shared-memory matrix descriptor: start address, leading / stride byte
-// offsets (16-byte units), descriptor version 1, 128-byte swizzle (layout 2).
-__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = uint64_t((addr >> 4) & 0x3FFFu);
-    d |= uint64_t((lbo >> 4) & 0x3FFFu) << 16;
-    d |= uint64_t((sbo >> 4) & 0x3FFFu) << 32;
-    d |= uint64_t(1) << 46;
-    d |= uint64_t(2) << 61;
-    return d;
-}
-
-__device__ __forceinline__ uint32_t su32(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
-__device__ __forceinline__ unsigned long long gtime() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ void mbar_init(uint32_t a, uint32_t n) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(a), "r"(n) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t a, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(a), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t a) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(a) : "memory");
-}
-__device__ __forceinline__ bool mbar_test(uint32_t a, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok) : "r"(a), "r"(parity) : "memory");
-    return ok != 0;
-}
-// Bounded wait; false on timeout (raises the abort flag) or when another
-// thread raised it.
-__device__ bool mbar_wait(uint32_t a, uint32_t parity, volatile uint32_t* abort_flag) {
-    if (mbar_test(a, parity)) return true;
-    const unsigned long long t0 = gtime();
-    for (;;) {
-        if (mbar_test(a, parity)) return true;
-        if (*abort_flag) return false;
-        if (gtime() - t0 > kTimeoutNs) {
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-// Bounded wait that ignores the abort flag (draining after an abort).
-__device__ void mbar_drain(uint32_t a, uint32_t parity) {
-    const unsigned long long t0 = gtime();
-    while (!mbar_test(a, parity) && gtime() - t0 < kDrainNs) {
-    }
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
-
-__device__ __forceinline__ void tc_mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
-                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "r"(acc) : "memory");
-}
-__device__ __forceinline__ void tc_mma_ts(uint32_t d, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
-    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
-                 ::"r"(d), "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc) : "memory");
-}
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-        : "r"(taddr));
-}
-// 64 consecutive columns of this thread's lane (one wait by the caller)
-__device__ __forceinline__ void tc_ld64(uint32_t taddr, uint32_t (&r)[64]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,"
-        "%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-        "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]),
-          "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]),
-          "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]),
-          "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]),
-          "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
-        : "r"(taddr));
-}
-// N (2..64) consecutive 32-bit columns of this thread's lane; the caller waits
-template <int N>
-__device__ __forceinline__ void tc_ld_n(uint32_t taddr, uint32_t (&r)[N]) {
-    if constexpr (N == 2) {
-        asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0,%1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(taddr));
-    } else if constexpr (N == 4) {
-        asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(taddr));
-    } else if constexpr (N == 8) {
-        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                       "=r"(r[7]) : "r"(taddr));
-    } else if constexpr (N == 16) {
-        tc_ld16(taddr, r);
-    } else if constexpr (N == 64) {
-        tc_ld64(taddr, r);
-    } else {
-        static_assert(N == 32, "2, 4, 8, 16, 32 or 64 columns");
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-            "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-              "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-              "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-            : "r"(taddr));
-    }
-}
-
-__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
-        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-          "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
-          "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
-          "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
-        : "memory");
-}
-__device__ __forceinline__ void tc_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
-                 ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-                 : "memory");
-}
-template <int N>
-__device__ __forceinline__ void tc_st_n(uint32_t taddr, const uint32_t (&r)[N]) {
-    if constexpr (N == 8) {
-        tc_st8(taddr, r);
-    } else if constexpr (N == 32) {
-        tc_st32(taddr, r);
-    } else {
-        static_assert(N == 16, "8, 16 or 32 columns");
-        asm volatile(
-            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
-            ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-              "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-            : "memory");
-    }
-}
-__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
 __device__ __forceinline__ float ex2(float x) { return ex2_approx(x); }
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
     __half2 h = __floats2half2_rn(a, b);
@@ -248,14 +86,6 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
 }
 __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) {
     return pack_h2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-}
-__device__ __forceinline__ uint4 lds128(uint32_t a) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-    return v;
-}
-__device__ __forceinline__ void sts128(uint32_t a, const uint4& v) {
-    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
 // State of one softmax thread: query row qi = per*(lane quadrant) + lane sits
@@ -356,7 +186,7 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
 
 __global__ void __launch_bounds__(kThreads, 2)
 attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, float* __restrict__ part_o,
-                        float2* __restrict__ part_ml, float* __restrict__ out) {
+                        float2* __restrict__ part_ml, float* __restrict__ out, int full) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = su32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;            // 128-byte swizzle atoms need 1 KB alignment
@@ -432,8 +262,10 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
     ss.abortp = abortp;
     ss.trow = trow;
     ss.T = T;
-    ss.lim = qvalid ? st.keys - st.rows + (qi >> 2) + 1 - c0 : 0;
-    ss.lim_all = st.keys - st.rows + 1 - c0;
+    // chunk-local key bounds: causal count of the row (of row 0 for lim_all),
+    // or every key for a FULL block
+    ss.lim = qvalid ? (full ? st.keys : st.keys - st.rows + (qi >> 2) + 1) - c0 : 0;
+    ss.lim_all = (full ? st.keys : st.keys - st.rows + 1) - c0;
     ss.wact = wact;
     ss.mref = -INFINITY;
     ss.mtrue = -INFINITY;
@@ -586,10 +418,10 @@ int attn_tc_prepare() {
 }
 
 int launch_attn_partials_tc(const SegTable& t, int layer, const uint16_t* q, float* po, float2* pml,
-                            cudaStream_t stream, float* out) {
+                            cudaStream_t stream, float* out, int full) {
     if (!t.k_maps || !t.v_maps) return TF_EINVAL;
     return launch_pdl(attn_partials_tc_kernel, dim3((t.n_items - t.n_items_mma) * TF_NKV), dim3(kThreads),
-                      kSmemBytes, stream, t, layer, q, po, pml, out);
+                      kSmemBytes, stream, t, layer, q, po, pml, out, full);
 }
 
 }  // namespace tf

@@ -1,0 +1,352 @@
+// The drafter's Markov head on the 5th-generation tensor cores: per block row,
+// score[v] = bf16(base[v] + bf16(W2[v] . W1[tok])) over the vocabulary and the
+// lowest token of the largest score, one step (one block row of every stream)
+// per launch.
+//
+// PR #1391 "lfm2: draft with LiquidAI's DSpark drafter (--drafter)": the head
+// "adds W2 W1[previous token] to each row's logits and takes the argmax, one
+// row after the other"; its kernels do the W1 gather, the W2 dot, the add and
+// an argmax with ties to the lowest token and a NaN score flagged; the family
+// test states the step as the argmax of bf16(base + bf16(W2 . W1[prev])); W2
+// stays bf16 ("a bf16 scan").
+//
+// One step is a skinny GEMM followed by an argmax: D[s][v] = E[s] . W2[v] with
+// E[s] = W1[tok_s], for up to 128 streams (MMA M = 128 TMEM lanes, one lane per
+// stream; lanes without a stream hold zero rows) against 128-row tiles of W2
+// (MMA N = 128), K = 256. W2 is 128000 x 512 bytes and is read once per step
+// for all the streams, so the step is HBM bound on W2 plus each stream's base
+// row; the tensor cores keep the 2*128*256 flops per W2 row off the ALUs.
+//
+// CTA (one per SM; a contiguous range of W2 tiles), 6 warps:
+//   warp 5, lane 0   TMA loads of W2 k-blocks (128 rows x 64 columns = 16 KB,
+//                    128-byte swizzle) into an 8-stage ring;
+//   warp 4, lane 0   the MMAs: 4 per k-block, into one of two 128-column
+//                    accumulators in tensor memory (tile t uses t % 2);
+//   warps 0-3        epilogue: thread = stream lane; per tile it reads its 128
+//                    dot products, rounds them to bf16, adds its stream's base
+//                    logits (16-byte loads), rounds again and keeps the first
+//                    largest score and a nonfinite bit -- the argmax is
+//                    within the thread, no shuffles.
+// The CTAs of a launch meet through 64-bit atomicMax on (ordered score, ~token)
+// per stream and an atomicOr of the flags; the last CTA to finish writes the
+// picks and resets the scratch. The next step's launch reads those picks as
+// its previous tokens.
+//
+// Every mbarrier wait is bounded (2 s of %globaltimer); on a timeout the CTA
+// raises its abort flag, drains its copies and MMAs (bounded), marks its
+// streams' rows with flag bit 1, frees its tensor memory and returns.
+#include "tc_ptx.cuh"
+
+namespace tf {
+namespace {
+
+constexpr int kLanes = 128;             // streams per group: MMA M, TMEM lanes
+constexpr int kTileV = 128;             // W2 rows per tile: MMA N
+constexpr int kKB = TF_MK / 64;         // k-blocks of 64 columns (128 bytes) per row
+constexpr int kSlabB = 128 * 128;       // one k-block of 128 rows: 16 KB
+constexpr int kStages = 8;
+constexpr int kAB = kKB * kSlabB;       // E: 128 rows x 256 columns, 64 KB
+constexpr int kWarps = 6;
+constexpr int kThreads = kWarps * 32;
+constexpr uint32_t kCols = 256;         // two accumulators of 128 columns
+
+struct Bars {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    uint32_t abort_flag;
+    int32_t last;
+    int32_t tok[kLanes];    // previous token of the lane's stream, -1 if none or invalid
+    int32_t row[kLanes];    // draft row of the lane's stream in this step, -1 if it has none
+};
+constexpr int kSmemBytes = 1024 + kAB + kStages * kSlabB + int(sizeof(Bars));
+
+// kind::f16, fp32 accumulate, A and B bf16 K-major, N = 128, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kTileV >> 3) << 17) |
+                            (uint32_t(128 >> 4) << 24);
+
+// Orders scores as unsigned integers (larger score -> larger key); -0 is +0.
+__device__ __forceinline__ uint32_t ord_bf16(float best) {
+    uint32_t b = best == 0.f ? 0u : (__float_as_uint(best) >> 16);
+    return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// One column: the dot's bf16, plus the base logit, rounded; the running first
+// largest (ids increase along the scan, so strict > keeps the lowest).
+__device__ __forceinline__ void score_one(uint32_t acc_bits, float base_v, int id, float& best, int& bid,
+                                          uint32_t& nf) {
+    const float d16 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(acc_bits)));
+    // both terms are bf16 values: their fp32 sum rounds to the same bf16 as the exact sum
+    const __nv_bfloat16 sc = __float2bfloat16_rn(d16 + base_v);
+    const uint32_t bits = __bfloat16_as_ushort(sc);
+    nf |= uint32_t((bits & 0x7F80u) == 0x7F80u);
+    const float f = __bfloat162float(sc);
+    if (f > best) {
+        best = f;
+        bid = id;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+markov_step_kernel(SegTable t, int step, const uint16_t* __restrict__ W1, int vocab,
+                   const uint16_t* __restrict__ base, int64_t base_stride, const int32_t* __restrict__ prev,
+                   int32_t* __restrict__ pick, uint8_t* __restrict__ flag,
+                   const __grid_constant__ CUtensorMap w2map) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = su32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;          // 128-byte swizzle atoms need 1 KB alignment
+    unsigned char* gbase = smem_raw + (sbase - raw);
+    const uint32_t sA = sbase;
+    const uint32_t sB = sbase + kAB;
+    Bars* bars = reinterpret_cast<Bars*>(gbase + kAB + kStages * kSlabB);
+    volatile uint32_t* abortp = &bars->abort_flag;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int group = blockIdx.y;
+    const int s0 = group * kLanes;
+    const int nt = (vocab + kTileV - 1) / kTileV;
+    const int t_begin = int((int64_t(blockIdx.x) * nt) / gridDim.x);
+    const int t_end = int((int64_t(blockIdx.x + 1) * nt) / gridDim.x);
+    const int ntl = t_end - t_begin;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(su32(&bars->full[s]), 1);
+            mbar_init(su32(&bars->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(su32(&bars->acc_full[b]), 1);
+            mbar_init(su32(&bars->acc_empty[b]), 4);   // the 4 epilogue warps
+        }
+        mbar_init(su32(&bars->drain), 1);
+        bars->abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    pdl_wait();   // previous tokens may be the picks of the step just before
+    if (tid < kLanes) {
+        const int s = s0 + tid;
+        int tok = -1, row = -1;
+        if (s < t.S) {
+            const SegStream st = t.streams[s];
+            if (st.rows - 1 > step) {
+                row = st.row_offset - s + step;
+                tok = step == 0 ? prev[s] : pick[row - 1];
+                if (tok < 0 || tok >= vocab) tok = -1;
+            }
+        }
+        bars->tok[tid] = tok;
+        bars->row[tid] = row;
+    }
+    if (warp == 4) tc_alloc(su32(&bars->tmem_base), kCols);
+    __syncthreads();
+    // E = the lanes' W1 rows (zero rows for lanes without a token), K-major,
+    // 128-byte swizzled: 16-byte chunk c of row L in k-block c / 8
+    for (int idx = tid; idx < kLanes * (TF_MK / 8); idx += kThreads) {
+        const int L = idx >> 5, c = idx & 31;
+        const int tok = bars->tok[L];
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (tok >= 0) v = __ldg(reinterpret_cast<const uint4*>(W1 + size_t(tok) * TF_MK) + c);
+        sts128(sA + (c >> 3) * kSlabB + L * 128 + (((c & 7) ^ (L & 7)) << 4), v);
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    float best = -INFINITY;
+    int bid = 0x7FFFFFFF;
+    uint32_t nf = 0;
+    const int L = warp * 32 + lane;
+    const int my_tok = warp < 4 ? bars->tok[L] : -1;
+    const int my_row = warp < 4 ? bars->row[L] : -1;
+
+    if (warp == 5) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < ntl * kKB; ++i) {
+                const int s = i % kStages;
+                if (i >= kStages && !mbar_wait(su32(&bars->empty[s]), ((i / kStages) - 1) & 1, abortp)) break;
+                const uint32_t bar = su32(&bars->full[s]);
+                mbar_expect_tx(bar, kSlabB);
+                tma_load_2d(sB + s * kSlabB, &w2map, (i % kKB) * 64, (t_begin + i / kKB) * kTileV, bar);
+                ++issued;
+            }
+            if (*abortp)   // let the copies in flight land before the CTA exits
+                for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+                    mbar_drain(su32(&bars->full[i % kStages]), (i / kStages) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            bool ok = true;
+            for (int tt = 0; tt < ntl && ok; ++tt) {
+                const int b = tt & 1;
+                if (tt >= 2) {   // the epilogue has read this accumulator's previous tile
+                    ok = mbar_wait(su32(&bars->acc_empty[b]), ((tt >> 1) - 1) & 1, abortp);
+                    if (!ok) break;
+                }
+                tc_fence_after();
+                for (int kb = 0; kb < kKB && ok; ++kb) {
+                    const int i = tt * kKB + kb, s = i % kStages;
+                    ok = mbar_wait(su32(&bars->full[s]), (i / kStages) & 1, abortp);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t da = sdesc(sA + kb * kSlabB, 16, 1024);
+                    const uint64_t db = sdesc(sB + s * kSlabB, 16, 1024);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)   // 64 columns: 4 steps of 16 (32 bytes)
+                        tc_mma_ss(tmem + uint32_t(b * kTileV), da + 2 * k, db + 2 * k, kIdesc, (kb | k) ? 1u : 0u);
+                    tc_commit(su32(&bars->empty[s]));   // the stage is free once these MMAs complete
+                }
+                if (ok) tc_commit(su32(&bars->acc_full[b]));
+            }
+            tc_commit(su32(&bars->drain));   // every MMA issued so far
+            mbar_drain(su32(&bars->drain), 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const bool valid = my_tok >= 0;
+        const bool wact = __any_sync(0xFFFFFFFFu, valid);
+        const uint16_t* brow = base + (valid ? my_row : 0) * base_stride;
+        const uint32_t tlane = tmem + (uint32_t(warp * 32) << 16);
+        for (int tt = 0; tt < ntl; ++tt) {
+            const int b = tt & 1;
+            if (!mbar_wait(su32(&bars->acc_full[b]), (tt >> 1) & 1, abortp)) break;
+            tc_fence_after();
+            if (wact) {
+                const int v0 = (t_begin + tt) * kTileV;
+#pragma unroll 1
+                for (int p = 0; p < kTileV / 32; ++p) {
+                    const int v = v0 + 32 * p;
+                    uint32_t bw[16];
+                    if (valid && v + 32 <= vocab) {
+                        const uint4* bp = reinterpret_cast<const uint4*>(brow + v);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const uint4 x = __ldg(bp + k);
+                            bw[4 * k] = x.x;
+                            bw[4 * k + 1] = x.y;
+                            bw[4 * k + 2] = x.z;
+                            bw[4 * k + 3] = x.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            const int i0 = v + 2 * k;
+                            const uint32_t lo = (valid && i0 < vocab) ? brow[i0] : 0u;
+                            const uint32_t hi = (valid && i0 + 1 < vocab) ? brow[i0 + 1] : 0u;
+                            bw[k] = lo | (hi << 16);
+                        }
+                    }
+                    uint32_t r[32];
+                    tc_ld_n<32>(tlane + uint32_t(b * kTileV + 32 * p), r);
+                    tc_wait_ld();
+                    if (valid) {
+                        const bool whole = v + 32 <= vocab;   // else the vocabulary ends in this piece
+#pragma unroll
+                        for (int k = 0; k < 16; ++k) {
+                            if (whole || v + 2 * k < vocab)
+                                score_one(r[2 * k], bf_lo(bw[k]), v + 2 * k, best, bid, nf);
+                            if (whole || v + 2 * k + 1 < vocab)
+                                score_one(r[2 * k + 1], bf_hi(bw[k]), v + 2 * k + 1, best, bid, nf);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(su32(&bars->acc_empty[b]));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();   // every copy and MMA of the CTA is done
+    tc_fence_after();
+    pdl_trigger();
+
+    // this CTA's best of each stream, met across CTAs in the table's scratch
+    if (warp < 4 && my_tok >= 0) {
+        const int s = s0 + L;
+        if (*abortp) {
+            atomicOr(&t.mk_flags[s], 2u);
+        } else {
+            if (bid != 0x7FFFFFFF)
+                atomicMax(&t.mk_keys[s], (static_cast<unsigned long long>(ord_bf16(best)) << 32) |
+                                             static_cast<unsigned long long>(0xFFFFFFFFu - uint32_t(bid)));
+            if (nf) atomicOr(&t.mk_flags[s], 1u);
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        bars->last = atomicAdd(&t.mk_ctr[group], 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (bars->last) {
+        // the last CTA of the group: picks and flags, then the scratch back to zero
+        __threadfence();
+        if (tid < kLanes && bars->row[tid] >= 0) {
+            const int s = s0 + tid;
+            const unsigned long long key = atomicExch(&t.mk_keys[s], 0ull);
+            const uint32_t fl = atomicExch(&t.mk_flags[s], 0u);
+            int p = -1;
+            uint8_t f = 1;
+            if (bars->tok[tid] >= 0) {
+                if (fl) {
+                    f = uint8_t(fl);
+                } else {
+                    p = int(0xFFFFFFFFu - uint32_t(key & 0xFFFFFFFFull));
+                    f = 0;
+                }
+            }
+            pick[bars->row[tid]] = p;
+            flag[bars->row[tid]] = f;
+        }
+        if (tid == 0) atomicExch(&t.mk_ctr[group], 0u);
+    }
+    __syncthreads();
+    if (warp == 4) {
+        tc_fence_after();
+        tc_dealloc(tmem, kCols);
+    }
+}
+
+}  // namespace
+}  // namespace tf
+
+extern "C" int tf_markov_chain(const tf_segments* seg, const void* W1, const void* W2, int vocab, const void* base,
+                               int64_t base_stride, const int32_t* prev, int32_t* pick, uint8_t* flag,
+                               tf_cuda_stream stream) {
+    using namespace tf;
+    if (!W1 || !W2 || !base || !prev || !pick || !flag || vocab < 1) return TF_EINVAL;
+    if (vocab > (1 << 24)) return TF_ERANGE;
+    if (!aligned16(W1) || !aligned16(W2) || !aligned16(base) || base_stride < vocab || base_stride % 8 != 0)
+        return TF_EINVAL;
+    if (!seg) return TF_EINVAL;
+    const SegTable& t = seg->dev;
+    if (t.S == 0 || t.R == t.S) return TF_OK;   // no window holds a draft
+    cudaError_t e = cudaFuncSetAttribute(markov_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return cuda_fail(e);
+    CUtensorMap map;
+    if (!encode_w2_map(&map, W2, vocab)) return cuda_fail(cudaErrorInvalidValue);
+    const int nt = (vocab + kTileV - 1) / kTileV;
+    const int gx = nt < sm_count() ? nt : sm_count();
+    const dim3 grid(gx, (t.S + kLanes - 1) / kLanes);
+    const uint16_t* w1 = static_cast<const uint16_t*>(W1);
+    const uint16_t* b = static_cast<const uint16_t*>(base);
+    for (int j = 0; j + 1 < t.max_rows; ++j) {
+        const int rc = launch_pdl(markov_step_kernel, grid, dim3(kThreads), kSmemBytes, stream, t, j, w1, vocab, b,
+                                  base_stride, prev, pick, flag, map);
+        if (rc != TF_OK) return rc;
+    }
+    return TF_OK;
+}

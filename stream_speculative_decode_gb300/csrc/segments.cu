@@ -76,6 +76,19 @@ bool encode_kv_map(CUtensorMap* out, const void* base, int keys, int cap) {
 
 }  // namespace
 
+bool encode_w2_map(CUtensorMap* out, const void* w2, int rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {cuuint64_t(TF_MK), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(TF_MK) * 2};
+    const cuuint32_t box[2] = {64u, 128u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(w2), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Attention kernel of a stream: tensor cores once its window holds 3 rows (12
 // query rows per KV head); TF_ATTN_PATH=mma|tc forces one (tests compare both).
 int attn_path_of(int rows) {
@@ -258,6 +271,10 @@ int tf_segments_build(const tf_stream* streams, int n_streams,
     const size_t o_km = off;       off = align_up(off + sizeof(CUtensorMap) * n_maps, 256);
     const size_t o_vm = off;       off = align_up(off + sizeof(CUtensorMap) * n_maps, 256);
     const size_t o_ctr = off;      off = align_up(off + sizeof(int32_t) * n_ap * TF_NKV, 256);
+    const size_t n_groups = (size_t(S) + 127) / 128;   // Markov step: 128 streams per group
+    const size_t o_mkk = off;      off = align_up(off + sizeof(unsigned long long) * S, 256);
+    const size_t o_mkf = off;      off = align_up(off + sizeof(uint32_t) * S, 256);
+    const size_t o_mkc = off;      off = align_up(off + sizeof(uint32_t) * n_groups, 256);
     const size_t total = off;
 
     seg->host.assign(total, 0);
@@ -327,6 +344,9 @@ int tf_segments_build(const tf_stream* streams, int n_streams,
         t.k_maps = n_maps ? reinterpret_cast<const CUtensorMap*>(b + o_km) : nullptr;
         t.v_maps = n_maps ? reinterpret_cast<const CUtensorMap*>(b + o_vm) : nullptr;
         t.counters = reinterpret_cast<int32_t*>(b + o_ctr);   // zero in the image
+        t.mk_keys = reinterpret_cast<unsigned long long*>(b + o_mkk);   // zero in the image
+        t.mk_flags = reinterpret_cast<uint32_t*>(b + o_mkf);
+        t.mk_ctr = reinterpret_cast<uint32_t*>(b + o_mkc);
         rc = attn_prepare();
         if (rc == TF_OK) rc = attn_tc_prepare();
         if (rc != TF_OK) {

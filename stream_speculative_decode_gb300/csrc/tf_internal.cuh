@@ -60,6 +60,9 @@ struct SegTable {
     int32_t* counters;                // [n_attn][S][8] arrivals per (stream, KV head), self-resetting
     int32_t n_merge_rows;             // rows of kMergeKernel streams
     int32_t pad2_;
+    unsigned long long* mk_keys;      // [S] Markov step: best (score, token) key per stream, self-resetting
+    uint32_t* mk_flags;               // [S] Markov step: nonfinite / gave-up bits per stream, self-resetting
+    uint32_t* mk_ctr;                 // [ceil(S/128)] Markov step: CTA arrivals per stream group
 };
 
 constexpr int kAttnMma = 0;   // mma.sync flash-decode kernel (narrow windows)
@@ -68,6 +71,11 @@ constexpr int kTcMinRows = 3;
 
 // Kernel of a stream: by its window rows, unless TF_ATTN_PATH forces one.
 int attn_path_of(int rows);
+
+// segments.cu: TMA map of a bf16 [rows][256] matrix (the Markov head's W2),
+// boxes of 128 rows x 64 columns with 128-byte swizzle; rows past `rows` read
+// as zeros. False when the driver refuses it.
+bool encode_w2_map(CUtensorMap* out, const void* w2, int rows);
 
 }  // namespace tf
 
@@ -126,15 +134,16 @@ int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cud
 
 // attn.cu: one attention layer's partials and merge with the records at po/pml.
 // With out != nullptr the partials kernels also finish the streams whose
-// merge_mode is kMergeDirect or kMergeLastCta (the one-call form).
+// merge_mode is kMergeDirect or kMergeLastCta (the one-call form). full != 0:
+// the drafter's non-causal block form, every window row seeing all keys.
 int launch_attn_partials(const SegTable& t, int layer, const uint16_t* q, float* po, float2* pml,
-                         cudaStream_t stream, float* out = nullptr);
+                         cudaStream_t stream, float* out = nullptr, int full = 0);
 int launch_attn_merge(const SegTable& t, const float* po, const float2* pml, float* out, cudaStream_t stream,
                       bool kernel_mode_only = false);
 
 // attn_tc.cu: the tensor-core partials kernel (same records as the mma.sync kernel).
 int launch_attn_partials_tc(const SegTable& t, int layer, const uint16_t* q, float* po, float2* pml,
-                            cudaStream_t stream, float* out);   // items [n_items_mma, n_items)
+                            cudaStream_t stream, float* out, int full);   // items [n_items_mma, n_items)
 int attn_tc_prepare();
 
 }  // namespace tf

@@ -279,6 +279,77 @@ def make_inputs(work, backend="numpy", device="cuda"):
     return inp
 
 
+MK = 256   # width of the drafter's Markov head rows
+
+
+@dataclass
+class DraftInputs:
+    """Inputs of the draft side of a round for a table of windows: the Markov
+    head (W1, W2: [vocab][MK]), the drafter's base logits of every draft row
+    ([R - S][vocab], stream s's rows_s - 1 rows packed at o_s - s) and each
+    stream's pending token."""
+    work: Workload
+    streams: list
+    W1: object = None
+    W2: object = None
+    base: object = None
+    prev: object = None                           # int32 [S]
+    planted: dict = field(default_factory=dict)
+
+
+def make_draft_inputs(work, backend="numpy", device="cuda", w2_std=0.25, nan_rows=0, inf_rows=0):
+    """Draw the draft side's inputs for ``work``'s windows.
+
+    Recipe (PCG64(work.seed * 7919 + 29), drawn in this order): pending tokens
+    U{0..vocab-1}; W1 ~ N(0, 1); W2 ~ N(0, w2_std) (so a Markov term W2[v].W1[t]
+    has standard deviation 16 * w2_std, comparable to the N(0, 3) logits); base
+    logits N(0, 3) clamped to +-19; then ``nan_rows`` base rows get one NaN and
+    ``inf_rows`` one +Inf at a random token. The torch backend draws the same
+    distributions on the GPU from a seeded torch generator.
+    """
+    rng = np.random.Generator(np.random.PCG64(work.seed * 7919 + 29))
+    S = len(work.rows)
+    offs = row_offsets(work.rows)
+    streams = [(r, o, k) for r, o, k in zip(work.rows, offs, work.keys)]
+    n = sum(r - 1 for r in work.rows)
+    V = work.vocab
+    inp = DraftInputs(work, streams)
+    inp.prev = rng.integers(0, V, size=S).astype(np.int32)
+    if backend == "numpy":
+        def normal(shape, std=1.0):
+            return _bf16_bits_np(rng.standard_normal(size=shape, dtype=np.float32) * np.float32(std))
+        inp.W1 = normal((V, MK))
+        inp.W2 = normal((V, MK), std=w2_std)
+        z = rng.standard_normal(size=(n, V), dtype=np.float32) * np.float32(3.0)
+        np.clip(z, -LOGIT_CLAMP, LOGIT_CLAMP, out=z)
+    elif backend == "torch":
+        gen = torch.Generator(device=device)
+        gen.manual_seed(work.seed * 104729 + 11)
+
+        def normal(shape, std=1.0):
+            t = torch.randn(shape, generator=gen, device=device, dtype=torch.float32)
+            if std != 1.0:
+                t.mul_(std)
+            return t.to(torch.bfloat16)
+        inp.W1 = normal((V, MK))
+        inp.W2 = normal((V, MK), std=w2_std)
+        z = torch.randn((max(n, 1), V), generator=gen, device=device, dtype=torch.float32)[:n]
+        z.mul_(3.0).clamp_(-LOGIT_CLAMP, LOGIT_CLAMP)
+    else:
+        raise ValueError(backend)
+    special = []
+    cand = list(range(n))
+    for kind, k in (("nan", nan_rows), ("inf", inf_rows)):
+        for _ in range(min(k, len(cand))):
+            r = cand.pop(int(rng.integers(len(cand))))
+            i = int(rng.integers(V))
+            z[r, i] = float("nan") if kind == "nan" else float("inf")
+            special.append((kind, r, i))
+    inp.base = _bf16_bits_np(z) if backend == "numpy" else z.to(torch.bfloat16)
+    inp.planted = dict(nonfinite=special)
+    return inp
+
+
 def to_numpy_bits(t):
     """A torch.bfloat16 tensor (any device) as a numpy uint16 bit-pattern array."""
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)

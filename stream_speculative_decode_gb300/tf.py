@@ -17,12 +17,15 @@ LIB_PATH = os.path.join(_HERE, "libtf.so")
 
 TF_H, TF_CIN, TF_KW, TF_NQ, TF_NKV, TF_D = 2048, 6144, 3, 32, 8, 64
 TF_MAX_ROWS = 16
+TF_MK = 256
+TF_DFLAG_BAD_PENDING, TF_DFLAG_BAD_DRAFT = 1, 2
 TF_OK, TF_EINVAL, TF_ERANGE, TF_ENOMEM, TF_ECUDA = 0, 1, 2, 3, 4
 
 # every symbol include/tf.h declares
 EXPORTS = ("tf_chunk_keys", "tf_segments_plan", "tf_segments_build", "tf_segments_free",
            "tf_segments_query", "tf_partials_bytes", "tf_conv_rows", "tf_attn_partials",
-           "tf_attn_merge", "tf_attn", "tf_attn_static", "tf_argmax_rows", "tf_accept", "tf_strerror",
+           "tf_attn_merge", "tf_attn", "tf_attn_static", "tf_attn_block_partials", "tf_attn_block",
+           "tf_argmax_rows", "tf_accept", "tf_markov_chain", "tf_draft_ids", "tf_strerror",
            "tf_last_cuda_error")
 TF_STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -70,6 +73,10 @@ def _load():
         "tf_attn_merge": (i32, [vp, vp, vp, vp]),
         "tf_attn_static": (i32, [vp, i32, vp, vp, vp]),
         "tf_attn": (i32, [vp, i32, vp, vp, vp, vp]),
+        "tf_attn_block_partials": (i32, [vp, i32, vp, vp, vp]),
+        "tf_attn_block": (i32, [vp, i32, vp, vp, vp, vp]),
+        "tf_markov_chain": (i32, [vp, vp, vp, i32, vp, i64, vp, vp, vp, vp]),
+        "tf_draft_ids": (i32, [vp, vp, vp, vp, i32, vp, vp, vp]),
         "tf_argmax_rows": (i32, [vp, i32, i32, i64, vp, vp, vp]),
         "tf_accept": (i32, [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, vp]),
         "tf_strerror": (ctypes.c_char_p, [i32]),
@@ -217,6 +224,30 @@ def tf_attn_static(seg, attn_layer, q, out, stream=None):
     """One attention layer with the library's fixed partial scratch (allocates
     nothing; see include/tf.h)."""
     _check("tf_attn_static", _lib.tf_attn_static(_h(seg), attn_layer, _ptr(q), _ptr(out), _stream(stream)))
+
+
+def tf_attn_block_partials(seg, attn_layer, q, partials, stream=None):
+    """The drafter's non-causal block attention partials (every row sees all keys)."""
+    _check("tf_attn_block_partials", _lib.tf_attn_block_partials(_h(seg), attn_layer, _ptr(q), _ptr(partials),
+                                                                 _stream(stream)))
+
+
+def tf_attn_block(seg, attn_layer, q, partials, out, stream=None):
+    """One layer of the drafter's non-causal block attention in one call."""
+    _check("tf_attn_block", _lib.tf_attn_block(_h(seg), attn_layer, _ptr(q), _ptr(partials), _ptr(out),
+                                               _stream(stream)))
+
+
+def tf_markov_chain(seg, W1, W2, vocab, base, base_stride, prev, pick, flag, stream=None):
+    """The drafter's Markov head over the table's draft rows (one launch per step)."""
+    _check("tf_markov_chain", _lib.tf_markov_chain(_h(seg), _ptr(W1), _ptr(W2), vocab, _ptr(base), base_stride,
+                                                   _ptr(prev), _ptr(pick), _ptr(flag), _stream(stream)))
+
+
+def tf_draft_ids(seg, prev, drafts, draft_flag, vocab, ids, dflag, stream=None):
+    """The next verify's ids from the pending tokens and the drafter's picks."""
+    _check("tf_draft_ids", _lib.tf_draft_ids(_h(seg), _ptr(prev), _ptr(drafts), _ptr(draft_flag), vocab, _ptr(ids),
+                                             _ptr(dflag), _stream(stream)))
 
 
 def tf_argmax_rows(logits, R, V, row_stride, pick, flag, stream=None):

@@ -9,10 +9,22 @@ Tolerances (stated once, used by every parity test):
     relative L2 <= 1e-3.
   * picks, flags, accepted lengths, next tokens, key counts, stream flags,
     conv states and histories: bit-exact.
+  * Markov picks (the drafter's head): the tensor cores sum the 256 products
+    of W2[v] . W1[tok] in fp32, the oracle exactly, so bf16(dot) may differ by
+    one rounding step where the exact dot sits near a bf16 rounding boundary.
+    Rule (the pages check "the pick's score is below the row's best by more
+    than its bound"): with e = 2 * gamma_256 * sum_k |W2[v][k] W1[tok][k]|
+    (gamma_n = n u / (1 - n u), u = 2^-24, doubled for the tensor cores'
+    accumulation), each token's score lies in [lo_v, hi_v] = the scores of the
+    roundings of dot -+ e; the GPU's pick p must be a possible first argmax:
+    hi_p > lo_v for every v < p and hi_p >= lo_v for every v > p. Flags are
+    bit-exact, and the pick must equal the oracle's wherever only one token
+    passes that rule.
 """
 
 import numpy as np
 
+from oracle import draft as OD
 from oracle import step as O
 
 
@@ -73,3 +85,46 @@ def check_step(res, ref, inp, rewind=True):
     check_exact(res["flag"], ref["flag"], "flag")
     for k, name in enumerate(("accept_len", "next_token", "new_keys", "sflag")):
         check_exact(res["accept"][k], ref["accept"][k], name)
+
+
+GAMMA_256 = 256 * 2.0 ** -24 / (1 - 256 * 2.0 ** -24)
+
+
+def markov_bounds(base_row, W1, W2, tok):
+    """Per token, the lowest and highest score a correct fp32 accumulation of
+    the dot can give (see the module docstring). Returns (lo, hi) float64 [V]."""
+    e = O.bf16_to_f64(W1[int(tok)])
+    W2f = O.bf16_to_f64(W2)
+    dot = W2f @ e
+    err = 2.0 * GAMMA_256 * (np.abs(W2f) @ np.abs(e))
+    b = O.bf16_to_f64(base_row)
+    lo = O.bf16_to_f64(OD.f64_to_bf16_rne_any(b + O.bf16_to_f64(OD.f64_to_bf16_rne_any(dot - err))))
+    hi = O.bf16_to_f64(OD.f64_to_bf16_rne_any(b + O.bf16_to_f64(OD.f64_to_bf16_rne_any(dot + err))))
+    return lo, hi
+
+
+def markov_possible_picks(lo, hi):
+    """Tokens that can be the first largest score for some scores within [lo, hi]."""
+    V = len(lo)
+    # max of lo over tokens before v and after v
+    pre = np.concatenate([[-np.inf], np.maximum.accumulate(lo)[:-1]])
+    suf = np.concatenate([np.maximum.accumulate(lo[::-1])[::-1][1:], [-np.inf]])
+    ok = (hi > pre) & (hi >= suf)
+    return np.nonzero(ok)[0]
+
+
+def check_markov_row(pick, flag, base_row, W1, W2, tok, what):
+    """One GPU Markov row against the oracle, given the GPU's previous token:
+    returns True when the pick equals the oracle's own pick."""
+    sc, want_pick, want_flag = OD.markov_step(base_row, W1, W2, tok)
+    assert int(flag) == want_flag, f"{what}: flag {int(flag)}, oracle {want_flag}"
+    if want_flag:
+        assert int(pick) == -1, f"{what}: flagged row with pick {int(pick)}"
+        return True
+    lo, hi = markov_bounds(base_row, W1, W2, tok)
+    possible = markov_possible_picks(lo, hi)
+    assert int(pick) in set(possible.tolist()), \
+        f"{what}: pick {int(pick)} cannot be the first argmax (oracle {want_pick}, possible {possible[:8]})"
+    if len(possible) == 1:
+        assert int(pick) == want_pick, f"{what}: pick {int(pick)}, oracle {want_pick}"
+    return int(pick) == want_pick

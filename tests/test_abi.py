@@ -160,6 +160,22 @@ def test_calls_refuse_null_table(T):
     assert lib.tf_segments_free(None) == T.TF_OK
 
 
+def test_draft_side_refusals(T):
+    lib = T.lib()
+    a = 0x1000
+    assert lib.tf_attn_block_partials(None, 0, a, a, None) == T.TF_EINVAL
+    assert lib.tf_attn_block(None, 0, a, a, a, None) == T.TF_EINVAL
+    assert lib.tf_draft_ids(None, a, a, None, 10, a, a, None) == T.TF_EINVAL
+    # tf_markov_chain checks its arguments before the table
+    assert lib.tf_markov_chain(None, a, a, 1000, a, 1000, a, a, a, None) == T.TF_EINVAL      # no table
+    assert lib.tf_markov_chain(None, a, a, (1 << 24) + 8, a, (1 << 24) + 8, a, a, a, None) == T.TF_ERANGE
+    assert lib.tf_markov_chain(None, a, a + 8, 1000, a, 1000, a, a, a, None) == T.TF_EINVAL  # W2 misaligned
+    assert lib.tf_markov_chain(None, a, a, 1000, a, 1004, a, a, a, None) == T.TF_EINVAL      # stride % 8
+    assert lib.tf_markov_chain(None, a, a, 1000, a, 992, a, a, a, None) == T.TF_EINVAL       # stride < vocab
+    assert lib.tf_markov_chain(None, a, a, 0, a, 8, a, a, a, None) == T.TF_EINVAL
+    assert lib.tf_markov_chain(None, None, a, 1000, a, 1000, a, a, a, None) == T.TF_EINVAL
+
+
 def test_argmax_refusals(T):
     lib = T.lib()
     assert lib.tf_argmax_rows(None, 0, 10, 10, None, None, None) == T.TF_OK       # empty
