@@ -7,11 +7,18 @@ CUDA graph. Metric: verified rows per second (rows of every stream's window,
 all ranks) and the achieved HBM bandwidth.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5] [--impl tf|reference]
+    python bench.py --row markov|block [--workload 3|5] [--steps K] [--warmup W]
 
 Default workload: 16 streams of one row, 30 conv + 10 attention layers, key
 counts uniform in [256, 4096] (the plain shared round). The other workloads
 (1, 3, 4, 5) are selectable. ``--impl reference`` times the float64 CPU oracle
 on the host cores on a bounded sample of the same workload.
+
+``--row`` measures one of the draft side's operations on a workload's table of
+windows instead of the verify step (default workload 5, the 64 x 16-row
+table): ``markov`` the Markov head's chain over every draft row
+(tf_markov_chain, one launch per step), ``block`` one layer of the
+non-causal block attention (tf_attn_block). Each prints its own JSON line.
 """
 
 import argparse
@@ -38,13 +45,18 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--workload", type=int, default=None, choices=[1, 2, 3, 4, 5],
+                    help="default 2 for the verify step, 5 for --row")
+    ap.add_argument("--row", default="verify", choices=["verify", "markov", "block"])
     ap.add_argument("--impl", default="tf", choices=["tf", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--conv-layers", type=int, default=None, help="override (small profiling runs)")
     ap.add_argument("--attn-layers", type=int, default=None, help="override (small profiling runs)")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.workload is None:
+        args.workload = 2 if args.row == "verify" else 5
+    return args
 
 
 # ------------------------------------------------------------ distributed
@@ -452,11 +464,123 @@ def run_e2e(d, args, stream, flush):
             "ms_per_step": ms, "steps": steps}
 
 
+def run_row(args, rank, world):
+    """One draft-side operation on the workload's windows (see the module
+    docstring). Per step: one tf_markov_chain (every Markov step of every
+    stream) or one tf_attn_block layer, in a CUDA graph, L2 flushed between
+    steps."""
+    import numpy as np
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from stream_speculative_decode_gb300 import inputs as I
+    from stream_speculative_decode_gb300 import tf
+    from stream_speculative_decode_gb300.step import DeviceStep
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+    torch.cuda.set_device(dev)
+    dist_init(world, "nccl")
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = measured_peaks()
+    if args.row == "markov":
+        w = I.workload(args.workload, n_conv=0, n_attn=0)
+        n = sum(r - 1 for r in w.rows)
+        if n == 0:
+            raise SystemExit("--row markov needs a workload with drafts (3, 4 or 5)")
+        dr = I.make_draft_inputs(w, backend="torch", device=dev)
+        off, streams = 0, []
+        for r in w.rows:
+            streams.append((r, off, r, 64))
+            off += r
+        seg = tf.tf_segments_build(streams, [], None, [], [], 0, 0)
+        prev = torch.from_numpy(dr.prev).to(dev)
+        pick = torch.empty(n, dtype=torch.int32, device=dev)
+        flag = torch.empty(n, dtype=torch.uint8, device=dev)
+        steps_per_call = max(w.rows) - 1
+
+        def call(st):
+            tf.tf_markov_chain(seg, dr.W1, dr.W2, w.vocab, dr.base, w.vocab, prev, pick, flag, st)
+
+        units, metric, unit = n, "Markov draft rows/s (drafter head chain)", "rows/s"
+        # compulsory bytes: W2 once (steps after the first may find it in L2), every base row,
+        # the gathered W1 rows, picks and flags
+        alg = w.vocab * I.MK * 2 + n * w.vocab * 2 + n * I.MK * 2 + n * 5
+        kname = "markov_step_kernel (tcgen05 W2 . W1[tok] + argmax), whole chain"
+        launches = steps_per_call
+        extra = {"markov_steps": steps_per_call, "w2_bytes": w.vocab * I.MK * 2,
+                 "w2_reads_if_no_l2_reuse": steps_per_call * w.vocab * I.MK * 2}
+    else:
+        w = I.workload(args.workload, n_conv=0, n_attn=1)
+        inp = I.make_inputs(w, backend="torch", device=dev)
+        d = DeviceStep(inp, device=dev)
+        out = torch.empty_like(d.out[0])
+
+        def call(st):
+            tf.tf_attn_block(d.seg, 0, d.q[0], d.partials, out, st)
+
+        units, metric, unit = inp.R, "block-attention rows/s per layer (FULL, non-causal)", "rows/s"
+        alg = sum(k for _, _, k in inp.streams) * 8 * 64 * 2 * 2 + inp.R * 32 * 64 * (2 + 4)
+        kname = "tf_attn_block (partials with the merge folded in)"
+        launches = d.seg.plan["attn_kernels"] + d.seg.plan["attn_merge_launch"]
+        extra = {}
+    call(stream)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    with torch.cuda.graph(g, stream=cap):
+        call(cap)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    for _ in range(args.warmup):
+        flush.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    dist_barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for k in range(args.steps):
+        flush.zero_()
+        ev[k][0].record(stream)
+        g.replay()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    dist_barrier(world)
+    clocks.stop()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    value, ms_max = aggregate(units, ms, world, device=dev)
+    achieved = alg / (ms * 1e-3) / 1e9
+    line = {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(workload_config(w), row=args.row,
+                       l2="flushed: 256 MB written between timed steps, outside the events",
+                       graph="one CUDA graph per step", parallelism=f"replicas x{world}", **extra),
+        "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "algorithmic_bytes_per_call": alg,
+                     "avg_call_ms": ms, "peak_kind": peak_kind,
+                     "timing": "CUDA events around each graph replay (one call)"},
+        "gpu_launches": launches * args.steps,
+        "clocks": clocks.summary(t0, t1),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
     rank, world, _ = dist_env()
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.row != "verify":
+        return run_row(args, rank, world)
     return run_tf(args, rank, world)
 
 

@@ -23,9 +23,13 @@
 //   warp 4, lane 0   the MMAs: 4 per k-block, into one of two 128-column
 //                    accumulators in tensor memory (tile t uses t % 2);
 //   warps 0-3        epilogue: thread = stream lane; per tile it reads its 128
-//                    dot products, rounds them to bf16, adds its stream's base
-//                    logits (16-byte loads), rounds again and keeps the first
-//                    largest score and a nonfinite bit -- the argmax is
+//                    dot products, rounds them to bf16 two at a time
+//                    (cvt.rn.bf16x2.f32), adds its stream's base logits
+//                    (add.rn.bf16x2: one rounding of the exact sum; the base is
+//                    loaded a tile ahead), tests the exponents for nonfinite
+//                    scores and takes the packed maximum of each 32 columns;
+//                    only when that maximum beats the running best does it
+//                    look for the first column holding it -- the argmax is
 //                    within the thread, no shuffles.
 // The CTAs of a launch meet through 64-bit atomicMax on (ordered score, ~token)
 // per stream and an atomicOr of the flags; the last CTA to finish writes the
@@ -74,22 +78,83 @@ __device__ __forceinline__ uint32_t ord_bf16(float best) {
     return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    const int sz = valid ? 16 : 0;   // 0: fill the 16 bytes with zeros
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(sz) : "memory");
+}
+
+// The 128 base logits of one tile of the lane's row (bf16 pairs); zeros past
+// the vocabulary. The branch depends on the tile alone (uniform in the warp).
+__device__ __forceinline__ void load_base_tile(const uint16_t* brow, int v0, int vocab, uint32_t (&dst)[64]) {
+    if (v0 + kTileV <= vocab) {
+        const uint4* bp = reinterpret_cast<const uint4*>(brow + v0);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const uint4 x = __ldg(bp + k);
+            dst[4 * k] = x.x;
+            dst[4 * k + 1] = x.y;
+            dst[4 * k + 2] = x.z;
+            dst[4 * k + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < 64; ++k) {
+            const int i0 = v0 + 2 * k;
+            const uint32_t lo = i0 < vocab ? brow[i0] : 0u;
+            const uint32_t hi = i0 + 1 < vocab ? brow[i0 + 1] : 0u;
+            dst[k] = lo | (hi << 16);
+        }
+    }
+}
+
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// One column: the dot's bf16, plus the base logit, rounded; the running first
-// largest (ids increase along the scan, so strict > keeps the lowest).
-__device__ __forceinline__ void score_one(uint32_t acc_bits, float base_v, int id, float& best, int& bid,
-                                          uint32_t& nf) {
-    const float d16 = __bfloat162float(__float2bfloat16_rn(__uint_as_float(acc_bits)));
-    // both terms are bf16 values: their fp32 sum rounds to the same bf16 as the exact sum
-    const __nv_bfloat16 sc = __float2bfloat16_rn(d16 + base_v);
-    const uint32_t bits = __bfloat16_as_ushort(sc);
-    nf |= uint32_t((bits & 0x7F80u) == 0x7F80u);
-    const float f = __bfloat162float(sc);
-    if (f > best) {
-        best = f;
-        bid = id;
+// {hi, lo} fp32 -> bf16 pair, each rounded to nearest even
+__device__ __forceinline__ uint32_t cvt_bf16x2(float hi, float lo) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+// bf16 pair sum, each the exact sum rounded once to nearest even
+__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// 32 columns (ids v .. v+31, `n` of them inside the vocabulary): scores,
+// nonfinite bits and the running first largest.
+__device__ __forceinline__ void score_piece(const uint32_t (&r)[32], const uint32_t* base16, int v, int n,
+                                            float& best, int& bid, uint32_t& nf) {
+    uint32_t sc[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+        sc[k] = add_bf16x2(cvt_bf16x2(__uint_as_float(r[2 * k + 1]), __uint_as_float(r[2 * k])), base16[k]);
+        if (n < 32) {   // past the vocabulary: the most negative finite value (never first, never flagged)
+            if (2 * k >= n) sc[k] = (sc[k] & 0xFFFF0000u) | 0xFF7Fu;
+            if (2 * k + 1 >= n) sc[k] = (sc[k] & 0x0000FFFFu) | 0xFF7F0000u;
+        }
+        nf |= (sc[k] & 0x7F807F80u) + 0x00800080u;   // bit 15 / 31: exponent all ones
+    }
+    uint32_t m = sc[0];
+#pragma unroll
+    for (int k = 1; k < 16; ++k) m = max_bf16x2(m, sc[k]);
+    const float mv = fmaxf(bf_lo(m), bf_hi(m));
+    if (mv > best) {   // rare after the first tiles: find the first column holding mv
+        int c = 31;
+#pragma unroll
+        for (int k = 15; k >= 0; --k) {
+            if (bf_hi(sc[k]) == mv) c = 2 * k + 1;
+            if (bf_lo(sc[k]) == mv) c = 2 * k;
+        }
+        best = mv;
+        bid = v + c;
     }
 }
 
@@ -145,14 +210,15 @@ markov_step_kernel(SegTable t, int step, const uint16_t* __restrict__ W1, int vo
     if (warp == 4) tc_alloc(su32(&bars->tmem_base), kCols);
     __syncthreads();
     // E = the lanes' W1 rows (zero rows for lanes without a token), K-major,
-    // 128-byte swizzled: 16-byte chunk c of row L in k-block c / 8
+    // 128-byte swizzled: 16-byte chunk c of row L in k-block c / 8. Every copy
+    // is in flight at once (cp.async), then one wait.
     for (int idx = tid; idx < kLanes * (TF_MK / 8); idx += kThreads) {
         const int L = idx >> 5, c = idx & 31;
         const int tok = bars->tok[L];
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (tok >= 0) v = __ldg(reinterpret_cast<const uint4*>(W1 + size_t(tok) * TF_MK) + c);
-        sts128(sA + (c >> 3) * kSlabB + L * 128 + (((c & 7) ^ (L & 7)) << 4), v);
+        const uint16_t* src = tok >= 0 ? W1 + size_t(tok) * TF_MK + c * 8 : W1;
+        cp_async16(sA + (c >> 3) * kSlabB + L * 128 + (((c & 7) ^ (L & 7)) << 4), src, tok >= 0);
     }
+    asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -216,56 +282,38 @@ markov_step_kernel(SegTable t, int step, const uint16_t* __restrict__ W1, int vo
         // ------------------------------------------------------------ epilogue
         const bool valid = my_tok >= 0;
         const bool wact = __any_sync(0xFFFFFFFFu, valid);
+        // lanes without a row read row 0 (any row exists when the kernel runs) and discard it
         const uint16_t* brow = base + (valid ? my_row : 0) * base_stride;
         const uint32_t tlane = tmem + (uint32_t(warp * 32) << 16);
+        // base logits one tile ahead of the accumulator they are added to
+        uint32_t cur[64], nxt[64];
+        if (wact && ntl > 0) load_base_tile(brow, t_begin * kTileV, vocab, cur);
         for (int tt = 0; tt < ntl; ++tt) {
             const int b = tt & 1;
+            const int v0 = (t_begin + tt) * kTileV;
+            if (wact && tt + 1 < ntl) load_base_tile(brow, v0 + kTileV, vocab, nxt);
             if (!mbar_wait(su32(&bars->acc_full[b]), (tt >> 1) & 1, abortp)) break;
             tc_fence_after();
             if (wact) {
-                const int v0 = (t_begin + tt) * kTileV;
-#pragma unroll 1
+#pragma unroll
                 for (int p = 0; p < kTileV / 32; ++p) {
                     const int v = v0 + 32 * p;
-                    uint32_t bw[16];
-                    if (valid && v + 32 <= vocab) {
-                        const uint4* bp = reinterpret_cast<const uint4*>(brow + v);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint4 x = __ldg(bp + k);
-                            bw[4 * k] = x.x;
-                            bw[4 * k + 1] = x.y;
-                            bw[4 * k + 2] = x.z;
-                            bw[4 * k + 3] = x.w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            const int i0 = v + 2 * k;
-                            const uint32_t lo = (valid && i0 < vocab) ? brow[i0] : 0u;
-                            const uint32_t hi = (valid && i0 + 1 < vocab) ? brow[i0 + 1] : 0u;
-                            bw[k] = lo | (hi << 16);
-                        }
-                    }
-                    uint32_t r[32];
-                    tc_ld_n<32>(tlane + uint32_t(b * kTileV + 32 * p), r);
-                    tc_wait_ld();
-                    if (valid) {
-                        const bool whole = v + 32 <= vocab;   // else the vocabulary ends in this piece
-#pragma unroll
-                        for (int k = 0; k < 16; ++k) {
-                            if (whole || v + 2 * k < vocab)
-                                score_one(r[2 * k], bf_lo(bw[k]), v + 2 * k, best, bid, nf);
-                            if (whole || v + 2 * k + 1 < vocab)
-                                score_one(r[2 * k + 1], bf_hi(bw[k]), v + 2 * k + 1, best, bid, nf);
-                        }
+                    if (v < vocab) {   // uniform
+                        uint32_t r[32];
+                        tc_ld_n<32>(tlane + uint32_t(b * kTileV + 32 * p), r);
+                        tc_wait_ld();
+                        const int n = vocab - v < 32 ? vocab - v : 32;
+                        if (valid) score_piece(r, cur + 16 * p, v, n, best, bid, nf);
                     }
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(su32(&bars->acc_empty[b]));
+#pragma unroll
+            for (int k = 0; k < 64; ++k) cur[k] = nxt[k];
         }
+        nf = (nf & 0x80008000u) ? 1u : 0u;
     }
     tc_fence_before();
     __syncthreads();   // every copy and MMA of the CTA is done
