@@ -12,7 +12,9 @@
 //
 // One step is a skinny GEMM followed by an argmax: D[s][v] = E[s] . W2[v] with
 // E[s] = W1[tok_s], for up to 128 streams (MMA M = 128 TMEM lanes, one lane per
-// stream; lanes without a stream hold zero rows) against 128-row tiles of W2
+// stream; lanes without a stream hold zero rows; stream L of the group sits on
+// lane 32*(L%4) + L/4, so a few streams still spread over all four lane
+// quadrants and their epilogue warps) against 128-row tiles of W2
 // (MMA N = 128), K = 256. W2 is 128000 x 512 bytes and is read once per step
 // for all the streams, so the step is HBM bound on W2 plus each stream's base
 // row; the tensor cores keep the 2*128*256 flops per W2 row off the ALUs.
@@ -54,6 +56,9 @@ constexpr int kWarps = 6;
 constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kCols = 256;         // two accumulators of 128 columns
 
+// TMEM lane (= row of E) of the group's stream L, and back
+__host__ __device__ constexpr int lane_of(int L) { return 32 * (L & 3) + (L >> 2); }
+
 struct Bars {
     uint64_t full[kStages];
     uint64_t empty[kStages];
@@ -90,7 +95,7 @@ __device__ __forceinline__ void load_base_tile(const uint16_t* brow, int v0, int
         const uint4* bp = reinterpret_cast<const uint4*>(brow + v0);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-            const uint4 x = __ldg(bp + k);
+            const uint4 x = __ldcs(bp + k);   // read once: evict first
             dst[4 * k] = x.x;
             dst[4 * k + 1] = x.y;
             dst[4 * k + 2] = x.z;
@@ -142,9 +147,12 @@ __device__ __forceinline__ void score_piece(const uint32_t (&r)[32], const uint3
         }
         nf |= (sc[k] & 0x7F807F80u) + 0x00800080u;   // bit 15 / 31: exponent all ones
     }
-    uint32_t m = sc[0];
+    uint32_t m8[8], m4[4];
 #pragma unroll
-    for (int k = 1; k < 16; ++k) m = max_bf16x2(m, sc[k]);
+    for (int k = 0; k < 8; ++k) m8[k] = max_bf16x2(sc[2 * k], sc[2 * k + 1]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m4[k] = max_bf16x2(m8[2 * k], m8[2 * k + 1]);
+    const uint32_t m = max_bf16x2(max_bf16x2(m4[0], m4[1]), max_bf16x2(m4[2], m4[3]));
     const float mv = fmaxf(bf_lo(m), bf_hi(m));
     if (mv > best) {   // rare after the first tiles: find the first column holding mv
         int c = 31;
@@ -209,14 +217,14 @@ markov_step_kernel(SegTable t, int step, const uint16_t* __restrict__ W1, int vo
     }
     if (warp == 4) tc_alloc(su32(&bars->tmem_base), kCols);
     __syncthreads();
-    // E = the lanes' W1 rows (zero rows for lanes without a token), K-major,
-    // 128-byte swizzled: 16-byte chunk c of row L in k-block c / 8. Every copy
+    // E = the streams' W1 rows (zero rows for lanes without a token), K-major,
+    // 128-byte swizzled: 16-byte chunk c of row m in k-block c / 8. Every copy
     // is in flight at once (cp.async), then one wait.
     for (int idx = tid; idx < kLanes * (TF_MK / 8); idx += kThreads) {
-        const int L = idx >> 5, c = idx & 31;
+        const int L = idx >> 5, c = idx & 31, m = lane_of(L);
         const int tok = bars->tok[L];
         const uint16_t* src = tok >= 0 ? W1 + size_t(tok) * TF_MK + c * 8 : W1;
-        cp_async16(sA + (c >> 3) * kSlabB + L * 128 + (((c & 7) ^ (L & 7)) << 4), src, tok >= 0);
+        cp_async16(sA + (c >> 3) * kSlabB + m * 128 + (((c & 7) ^ (m & 7)) << 4), src, tok >= 0);
     }
     asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
     fence_async_smem();
@@ -228,20 +236,23 @@ markov_step_kernel(SegTable t, int step, const uint16_t* __restrict__ W1, int vo
     float best = -INFINITY;
     int bid = 0x7FFFFFFF;
     uint32_t nf = 0;
-    const int L = warp * 32 + lane;
+    const int L = 4 * lane + warp;   // the stream on TMEM lane 32*warp + lane (epilogue warps)
     const int my_tok = warp < 4 ? bars->tok[L] : -1;
     const int my_row = warp < 4 ? bars->row[L] : -1;
 
     if (warp == 5) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
+            // W2 is read again by every step of the chain: ask L2 to keep it
+            // (the base rows, read once, stream past it)
+            const uint64_t keep = l2_evict_last();
             int issued = 0;
             for (int i = 0; i < ntl * kKB; ++i) {
                 const int s = i % kStages;
                 if (i >= kStages && !mbar_wait(su32(&bars->empty[s]), ((i / kStages) - 1) & 1, abortp)) break;
                 const uint32_t bar = su32(&bars->full[s]);
                 mbar_expect_tx(bar, kSlabB);
-                tma_load_2d(sB + s * kSlabB, &w2map, (i % kKB) * 64, (t_begin + i / kKB) * kTileV, bar);
+                tma_load_2d_hint(sB + s * kSlabB, &w2map, (i % kKB) * 64, (t_begin + i / kKB) * kTileV, bar, keep);
                 ++issued;
             }
             if (*abortp)   // let the copies in flight land before the CTA exits
