@@ -169,7 +169,7 @@ int tf_conv_rows(const tf_segments* seg, int conv_layer, const void* bcx,
 /* a2. Causal GQA attention partials of one attention layer: for every stream,
  * KV head, key chunk, window row and query head, (m, l, o) over the chunk's
  * visible keys ([SRD] "qk, attention and merge (10 layers)"). Streams with
- * windows of 3 rows or more run on the tcgen05 tensor-core kernel, the others
+ * windows of 13 rows or more run on the tcgen05 tensor-core kernel, the others
  * on the mma.sync kernel; the choice depends on the stream alone (so a
  * stream's bits do not depend on its round), and a round holding both kinds
  * makes one launch of each (tf_plan.attn_kernels). The environment variable

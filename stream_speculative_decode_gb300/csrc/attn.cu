@@ -377,19 +377,24 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
     }
 }
 
-constexpr int kMergeWarps = 8;
-constexpr int kMergeThreads = kMergeWarps * 32;
-constexpr int kMergeUnroll = 8;
+constexpr int kMergeSplit = 4;                       // warps per (row, query head)
+constexpr int kMergeHeads = 2;                       // query heads per CTA
+constexpr int kMergeThreads = kMergeSplit * kMergeHeads * 32;
+constexpr int kMergeCtasPerRow = TF_NQ / kMergeHeads;
+constexpr int kMergeUnroll = 16;
 
-// One warp per (row, query head); a CTA covers 8 heads of one row. Lanes read
-// the chunks' (m, l) in parallel; the o records are then read kMergeUnroll at a
-// time with independent loads, lane j holding dimensions 2j and 2j+1.
+// kMergeSplit warps share one (row, query head): warp k takes the chunks
+// c = k, k + kMergeSplit, ...; lanes read those chunks' (m, l) in parallel,
+// then the o records kMergeUnroll at a time with independent loads (lane j
+// holding dimensions 2j and 2j+1). The warps' (M, L, o) are combined through
+// shared memory at the end.
 __global__ void __launch_bounds__(kMergeThreads)
 attn_merge_kernel(SegTable t, const float* __restrict__ part_o, const float2* __restrict__ part_ml,
                   float* __restrict__ out, int kernel_mode_only) {
-    const int row = blockIdx.x >> 2;
+    const int row = blockIdx.x / kMergeCtasPerRow;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int h = (blockIdx.x & 3) * kMergeWarps + warp;
+    const int hl = warp / kMergeSplit, split = warp % kMergeSplit;
+    const int h = (blockIdx.x % kMergeCtasPerRow) * kMergeHeads + hl;
     const int s = t.row_stream[row];
     const SegStream st = t.streams[s];
     if (kernel_mode_only && st.merge_mode != kMergeKernel) {   // finished by the partials kernel
@@ -402,11 +407,13 @@ attn_merge_kernel(SegTable t, const float* __restrict__ part_o, const float2* __
     const int64_t stride = int64_t(TF_NKV) * nq;   // records between chunks
     const int64_t base = st.pbase + int64_t(g) * nq + i * 4 + hh;
     const int C = st.n_chunks;
+    const int nc = C > split ? (C - split + kMergeSplit - 1) / kMergeSplit : 0;   // this warp's chunks
     pdl_wait();
 
+    // chunk j of this warp is c = split + j * kMergeSplit
     float M = -INFINITY;
-    for (int c = lane; c < C; c += 32) {
-        const float2 ml = part_ml[base + c * stride];
+    for (int j = lane; j < nc; j += 32) {
+        const float2 ml = part_ml[base + int64_t(split + j * kMergeSplit) * stride];
         if (ml.y > 0.f) M = fmaxf(M, ml.x);
     }
 #pragma unroll
@@ -414,16 +421,16 @@ attn_merge_kernel(SegTable t, const float* __restrict__ part_o, const float2* __
 
     float2 acc = make_float2(0.f, 0.f);
     float lsum = 0.f;
-    for (int c0 = 0; c0 < C; c0 += 32) {
+    for (int j0 = 0; j0 < nc; j0 += 32) {
         float wj = 0.f;
-        if (c0 + lane < C) {
-            const float2 ml = part_ml[base + (c0 + lane) * stride];
+        if (j0 + lane < nc) {
+            const float2 ml = part_ml[base + int64_t(split + (j0 + lane) * kMergeSplit) * stride];
             if (ml.y > 0.f) {
                 wj = ex2(ml.x - M);
                 lsum += wj * ml.y;
             }
         }
-        const int n = min(32, C - c0);
+        const int n = min(32, nc - j0);
         for (int j = 0; j < n; j += kMergeUnroll) {
             float2 v[kMergeUnroll];
             float wk[kMergeUnroll];
@@ -431,8 +438,10 @@ attn_merge_kernel(SegTable t, const float* __restrict__ part_o, const float2* __
             for (int k = 0; k < kMergeUnroll; ++k) {
                 wk[k] = __shfl_sync(0xFFFFFFFFu, wj, (j + k) & 31);
                 v[k] = make_float2(0.f, 0.f);
-                if (j + k < n)
-                    v[k] = *reinterpret_cast<const float2*>(part_o + (base + (c0 + j + k) * stride) * TF_D + 2 * lane);
+                if (j + k < n) {
+                    const int64_t rec = base + int64_t(split + (j0 + j + k) * kMergeSplit) * stride;
+                    v[k] = *reinterpret_cast<const float2*>(part_o + rec * TF_D + 2 * lane);
+                }
             }
 #pragma unroll
             for (int k = 0; k < kMergeUnroll; ++k) {
@@ -446,9 +455,34 @@ attn_merge_kernel(SegTable t, const float* __restrict__ part_o, const float2* __
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
     pdl_trigger();
-    const float inv = 1.f / lsum;
-    *reinterpret_cast<float2*>(out + (size_t(row) * TF_NQ + h) * TF_D + 2 * lane) =
-        make_float2(acc.x * inv, acc.y * inv);
+
+    // combine the kMergeSplit warps of each head
+    __shared__ float sM[kMergeHeads][kMergeSplit], sL[kMergeHeads][kMergeSplit];
+    __shared__ float2 sO[kMergeHeads][kMergeSplit][32];
+    if (lane == 0) {
+        sM[hl][split] = M;
+        sL[hl][split] = lsum;
+    }
+    sO[hl][split][lane] = acc;
+    __syncthreads();
+    if (split == 0) {
+        float Mt = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kMergeSplit; ++k) Mt = fmaxf(Mt, sM[hl][k]);
+        float L = 0.f;
+        float2 o2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < kMergeSplit; ++k) {
+            if (sM[hl][k] == -INFINITY) continue;   // no visible key in this warp's chunks
+            const float f = ex2(sM[hl][k] - Mt);
+            L += f * sL[hl][k];
+            o2.x += f * sO[hl][k][lane].x;
+            o2.y += f * sO[hl][k][lane].y;
+        }
+        const float inv = 1.f / L;
+        *reinterpret_cast<float2*>(out + (size_t(row) * TF_NQ + h) * TF_D + 2 * lane) =
+            make_float2(o2.x * inv, o2.y * inv);
+    }
 }
 
 template <int MT>
@@ -489,8 +523,8 @@ int launch_attn_partials(const SegTable& t, int layer, const uint16_t* q, float*
 
 int launch_attn_merge(const SegTable& t, const float* po, const float2* pml, float* out, cudaStream_t stream,
                       bool kernel_mode_only) {
-    return launch_pdl(attn_merge_kernel, dim3(t.R * 4), dim3(kMergeThreads), 0, stream, t, po, pml, out,
-                      kernel_mode_only ? 1 : 0);
+    return launch_pdl(attn_merge_kernel, dim3(t.R * kMergeCtasPerRow), dim3(kMergeThreads), 0, stream, t, po, pml,
+                      out, kernel_mode_only ? 1 : 0);
 }
 
 }  // namespace tf

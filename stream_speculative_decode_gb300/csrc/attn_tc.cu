@@ -4,8 +4,9 @@
 // Same work items, chunking and partial records as the mma.sync kernel in
 // attn.cu (PR #1377 "LFM2: shared-round decode": one launch a layer over every
 // row from the segment table, per-stream partials; PR #1391: causal count),
-// used when a window holds 3 rows or more, where q.K and P.V are real
-// contractions (4*rows flops per byte of K/V each). With `full` set it is the
+// used when a window holds 13 rows or more, where q.K and P.V are real
+// contractions (4*rows flops per byte of K/V each) and the mma.sync kernel
+// would need a fourth 16-row query tile. With `full` set it is the
 // drafter's non-causal block attention (PR #1391: every block row sees the
 // keys [0, len + 1)): only the per-row key bounds change.
 //

@@ -185,9 +185,10 @@ def test_argmax_refusals(T):
     assert lib.tf_argmax_rows(0x1000, 2, (1 << 30) + 1, (1 << 30) + 1, 0x1000, 0x2000, None) == T.TF_ERANGE
 
 
-@pytest.mark.parametrize("rows,kernels", [([1], 1), ([1, 2], 1), ([3], 1), ([16, 4], 1), ([1, 3], 2), ([2, 12, 1], 2)])
+@pytest.mark.parametrize("rows,kernels", [([1], 1), ([1, 2], 1), ([3], 1), ([12, 4], 1), ([13], 1), ([16, 13], 1),
+                                          ([1, 13], 2), ([2, 16, 1], 2), ([12, 16], 2)])
 def test_attention_kernel_count(T, rows, kernels, monkeypatch):
-    """Windows of 3 rows or more go to the tensor-core kernel, narrower ones to
+    """Windows of 13 rows or more go to the tensor-core kernel, narrower ones to
     the mma.sync kernel; a round holding both makes one launch of each."""
     monkeypatch.delenv("TF_ATTN_PATH", raising=False)
     streams, off = [], 0
