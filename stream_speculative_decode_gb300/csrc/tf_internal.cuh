@@ -170,9 +170,9 @@ __device__ __forceinline__ float* out_row(float* out, const SegStream& st, int g
 // output, by the threads [tid, nthreads) of one CTA, one pass over the chunks
 // eight at a time (their loads in flight together) with a running max. The
 // records were written by other CTAs: they are read through L2 (ld.global.cg).
+template <int kB>   // records in flight per thread
 __device__ __forceinline__ void merge_stream_head(const SegStream& st, int g, const float* part_o,
                                                   const float2* part_ml, float* out, int tid, int nthreads) {
-    constexpr int kB = 8;
     const int nq = st.rows * 4;
     const int64_t stride = int64_t(TF_NKV) * nq;
     const int64_t base = st.pbase + int64_t(g) * nq;
@@ -227,6 +227,7 @@ __device__ __forceinline__ void merge_stream_head(const SegStream& st, int g, co
 // CTA of (stream, KV head) counts its arrival after its records are visible;
 // the last one merges and resets the counter for the next launch. All threads
 // of the CTA call this.
+template <int kB = 8>
 __device__ __forceinline__ void finish_last_cta(const SegTable& t, int layer, int s, const SegStream& st, int g,
                                                 const float* part_o, const float2* part_ml, float* out,
                                                 int* smem_flag) {
@@ -237,7 +238,7 @@ __device__ __forceinline__ void finish_last_cta(const SegTable& t, int layer, in
     __syncthreads();
     if (*smem_flag) {
         __threadfence();
-        merge_stream_head(st, g, part_o, part_ml, out, threadIdx.x, blockDim.x);
+        merge_stream_head<kB>(st, g, part_o, part_ml, out, threadIdx.x, blockDim.x);
         if (threadIdx.x == 0) atomicExch(ctr, 0);
     }
 }
