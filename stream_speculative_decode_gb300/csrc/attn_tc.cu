@@ -60,6 +60,9 @@ constexpr uint32_t kColO = 192;             // O: 64 columns
 constexpr float kLog2e8 = 0.18033688011112042f;   // log2(e) / sqrt(64)
 constexpr float kTau = 8.f;
 
+constexpr int kUQ = 4;                      // queue of the CTA's next units
+constexpr int kUQConsumers = 6;             // MMA thread, V converter warp, 4 softmax warps
+
 struct Bars {
     uint64_t kv_full[kStages];
     uint64_t kv_empty[kStages];
@@ -67,9 +70,15 @@ struct Bars {
     uint64_t s_full[kSBuf];      // per S buffer
     uint64_t p_full[kSBuf];      // per S buffer
     uint64_t o_done[kSBuf];      // P.V of a tile using S buffer b completed
+    uint64_t q_ready;            // the unit's queries are in shared memory (one phase a unit)
+    uint64_t uq_full[kUQ];       // the CTA's next units (unit index, -1 when there are no more)
+    uint64_t uq_empty[kUQ];
+    int32_t uq[kUQ];
+    uint64_t grp;                // the four softmax warps meet here (last-CTA merges)
     uint64_t drain;
     uint32_t tmem_base;
     uint32_t abort_flag;
+    int32_t last;
 };
 constexpr int kSmemBytes = 1024 + kQB + kStages * kStageB + int(sizeof(Bars));
 
@@ -89,12 +98,37 @@ __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) {
     return pack_h2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
-// State of one softmax thread: query row qi = per*(lane quadrant) + lane sits
-// on TMEM lane quadrant*32 + lane (lanes past `per` hold zero rows).
+// One unit of work: one key chunk of one stream (an attention item) for one
+// KV head. A CTA takes the units blockIdx.x, blockIdx.x + gridDim.x, ... of the
+// tensor-core items (largest first); every role walks the same list.
+struct Unit {
+    SegStream st;
+    const CUtensorMap* kmap;
+    const CUtensorMap* vmap;
+    int stream, chunk, g, c0, T;
+};
+__device__ __forceinline__ Unit unit_of(const SegTable& t, int layer, int u) {
+    Unit U;
+    const AttnItem it = t.items[t.n_items_mma + u / TF_NKV];   // tensor-core items follow the mma.sync ones
+    U.g = u % TF_NKV;
+    U.stream = it.stream;
+    U.chunk = it.chunk;
+    U.st = t.streams[it.stream];
+    U.c0 = it.chunk * U.st.chunk_keys;
+    U.T = (min(U.st.chunk_keys, U.st.keys - U.c0) + kKT - 1) / kKT;
+    const size_t slot = size_t(layer) * t.S + it.stream;
+    U.kmap = t.k_maps + slot;
+    U.vmap = t.v_maps + slot;
+    return U;
+}
+
+// State of one softmax thread for one unit: query row qi = per*(lane quadrant)
+// + lane sits on TMEM lane quadrant*32 + lane (lanes past `per` hold zero rows).
 struct SoftState {
     Bars* bars;
     volatile uint32_t* abortp;
     uint32_t trow;       // TMEM address of the warp's lane quadrant
+    int g0;              // the CTA's running tile count at the unit's first tile
     int T, lim, lim_all;
     bool wact;           // the warp holds at least one real query row
     float mref, mtrue;   // reference (lazy) and true running max, log2 units
@@ -106,9 +140,10 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
     const int lane = threadIdx.x & 31;
     Bars* bars = st.bars;
     for (int j = 0; j < st.T; ++j) {
-        const int b = j % kSBuf;
+        const int gj = st.g0 + j;
+        const int b = gj % kSBuf;
         const uint32_t colS = kColS + 64 * b;
-        if (!mbar_wait(su32(&bars->s_full[b]), (j / kSBuf) & 1, st.abortp)) break;
+        if (!mbar_wait(su32(&bars->s_full[b]), (gj / kSBuf) & 1, st.abortp)) break;
         tc_fence_after();
         if (st.wact) {
             const int k0 = j * kKT;                  // chunk-local first key of the tile
@@ -138,8 +173,8 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
             st.mtrue = fmaxf(st.mtrue, mxs);
             const bool resc = mxs > st.mref + kTau;
             if (__any_sync(0xFFFFFFFFu, resc)) {
-                // O holds P.V of tiles < j; the last of them (j-1) must be done
-                if (j >= 1 && !mbar_wait(su32(&bars->o_done[(j - 1) % kSBuf]), ((j - 1) / kSBuf) & 1, st.abortp))
+                // O holds P.V of the unit's tiles < j; the last of them (j-1) must be done
+                if (j >= 1 && !mbar_wait(su32(&bars->o_done[(gj - 1) % kSBuf]), ((gj - 1) / kSBuf) & 1, st.abortp))
                     break;
                 tc_fence_after();
                 const float alpha = resc ? ex2(st.mref - mxs) : 1.f;
@@ -185,9 +220,59 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
     }
 }
 
+// The m-th unit the producer handed this CTA after its first (blockIdx.x), or
+// -1: no more (or the CTA gave up). Single-thread consumer (the MMA thread).
+__device__ __forceinline__ int next_unit_thread(Bars* bars, int m, volatile uint32_t* abortp) {
+    const int slot = m % kUQ;
+    if (!mbar_wait(su32(&bars->uq_full[slot]), (m / kUQ) & 1, abortp)) return -1;
+    const int u = reinterpret_cast<volatile int32_t*>(bars->uq)[slot];
+    mbar_arrive(su32(&bars->uq_empty[slot]));
+    return u;
+}
+// The same for a whole warp: every lane reads, then lane 0 releases the slot.
+__device__ __forceinline__ int next_unit_warp(Bars* bars, int m, volatile uint32_t* abortp) {
+    const int slot = m % kUQ;
+    int u = -1;
+    if (mbar_wait(su32(&bars->uq_full[slot]), (m / kUQ) & 1, abortp))
+        u = reinterpret_cast<volatile int32_t*>(bars->uq)[slot];
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(su32(&bars->uq_empty[slot]));
+    return u;
+}
+
+// The four softmax warps (128 threads) meet; bounded like every wait here.
+__device__ __forceinline__ bool group_sync(Bars* bars, int& ph, volatile uint32_t* abortp) {
+    mbar_arrive(su32(&bars->grp));
+    const bool ok = mbar_wait(su32(&bars->grp), ph & 1, abortp);
+    ++ph;
+    return ok;
+}
+
+// The unit's queries into shared memory (cp.async, zero rows past 4*rows),
+// swizzled K-major: lane L holds query qi = per*(L/32) + L%32 when L%32 < per.
+__device__ __forceinline__ void load_q_async(uint32_t sQ, const uint16_t* q, const Unit& U, int tid) {
+    const int nq = U.st.rows * 4, per = (nq + 3) / 4;
+    for (int idx = tid; idx < kQRows * 8; idx += 128) {
+        const int L = idx >> 3, ch = idx & 7;
+        const int qq = per * (L >> 5) + (L & 31);
+        const bool valid = (L & 31) < per && qq < nq;
+        const uint16_t* src = q + ((size_t(U.st.row_offset + (qq >> 2)) * TF_NQ + 4 * U.g + (qq & 3)) * TF_D + ch * 8);
+        cp_async16(sQ + L * 128 + ((ch ^ (L & 7)) << 4), valid ? src : q, valid);
+    }
+    cp_async_commit();
+}
+
+// Persistent: one launch of at most two CTAs per SM; each CTA runs its units
+// back to back. A CTA starts with unit blockIdx.x; whenever its TMA producer
+// has issued a unit's last tile it takes the next unit of the launch (an atomic
+// counter in the table, so the largest-first list is handed out greedily) and
+// passes it to the other roles through a small queue in shared memory. The
+// TMA producer and the MMA thread run into the next unit's tiles while the
+// softmax warps finish the previous unit (records, merges); the ring stages, S
+// buffers and their mbarrier phases follow one running tile count.
 __global__ void __launch_bounds__(kThreads, 2)
 attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, float* __restrict__ part_o,
-                        float2* __restrict__ part_ml, float* __restrict__ out, int full) {
+                        float2* __restrict__ part_ml, float* __restrict__ out, int full, int n_units) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = su32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;            // 128-byte swizzle atoms need 1 KB alignment
@@ -196,22 +281,6 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
     const uint32_t sStage = base + kQB;
     Bars* bars = reinterpret_cast<Bars*>(gbase + kQB + kStages * kStageB);
     volatile uint32_t* abortp = &bars->abort_flag;
-
-    const int item_idx = t.n_items_mma + blockIdx.x / TF_NKV;   // tensor-core items follow the mma.sync ones
-    const int g = blockIdx.x % TF_NKV;
-    const AttnItem item = t.items[item_idx];
-    const SegStream st = t.streams[item.stream];
-    const int nq = st.rows * 4;
-    const int mode = out ? st.merge_mode : kMergeKernel;   // records only in the two-call form
-    // query rows per TMEM lane quadrant: rows spread over the four quadrants so
-    // that all four SM sub-partitions share the softmax
-    const int per = (nq + 3) / 4;
-    const int c0 = item.chunk * st.chunk_keys;
-    const int nkeys = min(st.chunk_keys, st.keys - c0);
-    const int T = (nkeys + kKT - 1) / kKT;
-    const size_t slot = size_t(layer) * t.S + item.stream;
-    const CUtensorMap* kmap = t.k_maps + slot;
-    const CUtensorMap* vmap = t.v_maps + slot;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
@@ -225,6 +294,12 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
             mbar_init(su32(&bars->p_full[b]), 4);   // the 4 softmax warps
             mbar_init(su32(&bars->o_done[b]), 1);
         }
+        mbar_init(su32(&bars->q_ready), 128);       // every softmax thread, after its copies
+        for (int k = 0; k < kUQ; ++k) {
+            mbar_init(su32(&bars->uq_full[k]), 1);
+            mbar_init(su32(&bars->uq_empty[k]), kUQConsumers);
+        }
+        mbar_init(su32(&bars->grp), 128);
         mbar_init(su32(&bars->drain), 1);
         bars->abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -234,82 +309,60 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(su32(&bars->tmem_base)), "r"(kCols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    } else if (warp < 4) {
-        // Q rows on their lanes (zero elsewhere), swizzled K-major: lane L holds
-        // query qi = per*(L/32) + L%32 when L%32 < per and qi < 4*rows
-        for (int idx = tid; idx < kQRows * 8; idx += 128) {
-            const int L = idx >> 3, ch = idx & 7;
-            const int qq = per * (L >> 5) + (L & 31);
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if ((L & 31) < per && qq < nq)
-                v = *reinterpret_cast<const uint4*>(
-                    q + ((size_t(st.row_offset + (qq >> 2)) * TF_NQ + 4 * g + (qq & 3)) * TF_D + ch * 8));
-            sts128(sQ + L * 128 + ((ch ^ (L & 7)) << 4), v);
-        }
-        fence_async_smem();
+    } else if (warp < 4 && int(blockIdx.x) < n_units) {
+        load_q_async(sQ, q, unit_of(t, layer, blockIdx.x), tid);   // the first unit's queries
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
 
-    // softmax-thread state (warps 0-3): this thread's TMEM lane, query row and key slice
-    const int qi = per * warp + lane;
-    const bool qvalid = warp < 4 && lane < per && qi < nq;
-    const bool wact = warp < 4 && per * warp < nq;      // the warp holds at least one real row
-    const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);
-    SoftState ss;
-    ss.bars = bars;
-    ss.abortp = abortp;
-    ss.trow = trow;
-    ss.T = T;
-    // chunk-local key bounds: causal count of the row (of row 0 for lim_all),
-    // or every key for a FULL block
-    ss.lim = qvalid ? (full ? st.keys : st.keys - st.rows + (qi >> 2) + 1) - c0 : 0;
-    ss.lim_all = (full ? st.keys : st.keys - st.rows + 1) - c0;
-    ss.wact = wact;
-    ss.mref = -INFINITY;
-    ss.mtrue = -INFINITY;
-    ss.l = 0.f;
-
     if (warp == 4) {
         // ------------------------------------------------------------ control
         if (lane == 0) {
             const uint64_t dq = sdesc(sQ, 16, 1024);
             bool ok = true;
-            for (int j = 0; j <= T && ok; ++j) {
-                if (j < T) {
-                    const int s = j % kStages, b = j % kSBuf;
-                    ok = mbar_wait(su32(&bars->kv_full[s]), (j / kStages) & 1, abortp);
-                    if (!ok) break;
-                    if (j >= kSBuf) {   // P.V(j-3) has released S buffer b
-                        ok = mbar_wait(su32(&bars->o_done[b]), ((j - kSBuf) / kSBuf) & 1, abortp);
+            int gt = 0, n = 0;
+            for (int u = blockIdx.x; u >= 0 && ok; ++n) {
+                const int T = unit_of(t, layer, u).T;
+                ok = mbar_wait(su32(&bars->q_ready), n & 1, abortp);   // the unit's queries landed
+                if (!ok) break;
+                tc_fence_after();
+                for (int j = 0; j <= T && ok; ++j) {
+                    if (j < T) {
+                        const int g1 = gt + j, s = g1 % kStages, b = g1 % kSBuf;
+                        ok = mbar_wait(su32(&bars->kv_full[s]), (g1 / kStages) & 1, abortp);
                         if (!ok) break;
+                        if (g1 >= kSBuf) {   // P.V(g1-3) has released S buffer b
+                            ok = mbar_wait(su32(&bars->o_done[b]), ((g1 - kSBuf) / kSBuf) & 1, abortp);
+                            if (!ok) break;
+                        }
+                        tc_fence_after();
+                        const uint64_t dk = sdesc(sStage + s * kStageB, 16, 1024);
+#pragma unroll
+                        for (int k = 0; k < TF_D / 16; ++k)   // K = 64: 4 steps of 16 (32 bytes)
+                            tc_mma_ss(tmem + kColS + 64 * b, dq + 2 * k, dk + 2 * k, kIdescQK, k > 0 ? 1u : 0u);
+                        tc_commit(su32(&bars->s_full[b]));
                     }
-                    tc_fence_after();
-                    const uint64_t dk = sdesc(sStage + s * kStageB, 16, 1024);
+                    if (j >= 1) {
+                        const int jj = j - 1, g2 = gt + jj, s = g2 % kStages, b = g2 % kSBuf;
+                        ok = mbar_wait(su32(&bars->p_full[b]), (g2 / kSBuf) & 1, abortp);
+                        if (!ok) break;
+                        ok = mbar_wait(su32(&bars->v_ready[s]), (g2 / kStages) & 1, abortp);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint64_t dv = sdesc(sStage + s * kStageB + kTileB, kTileB, 1024);
 #pragma unroll
-                    for (int k = 0; k < TF_D / 16; ++k)   // K = 64: 4 steps of 16 (32 bytes)
-                        tc_mma_ss(tmem + kColS + 64 * b, dq + 2 * k, dk + 2 * k, kIdescQK, k > 0 ? 1u : 0u);
-                    tc_commit(su32(&bars->s_full[b]));
+                        for (int k = 0; k < kKT / 16; ++k)   // 64 keys: 4 steps of 16 (2 KB of V rows)
+                            tc_mma_ts(tmem + kColO, tmem + kColS + 64 * b + 8 * k, dv + 128 * k, kIdescPV,
+                                      (jj > 0 || k > 0) ? 1u : 0u);
+                        tc_commit(su32(&bars->o_done[b]));
+                        tc_commit(su32(&bars->kv_empty[s]));
+                    }
                 }
-                if (j >= 1) {
-                    const int jj = j - 1, s = jj % kStages, b = jj % kSBuf;
-                    ok = mbar_wait(su32(&bars->p_full[b]), (jj / kSBuf) & 1, abortp);
-                    if (!ok) break;
-                    ok = mbar_wait(su32(&bars->v_ready[s]), (jj / kStages) & 1, abortp);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint64_t dv = sdesc(sStage + s * kStageB + kTileB, kTileB, 1024);
-#pragma unroll
-                    for (int k = 0; k < kKT / 16; ++k)   // 64 keys: 4 steps of 16 (2 KB of V rows)
-                        tc_mma_ts(tmem + kColO, tmem + kColS + 64 * b + 8 * k, dv + 128 * k, kIdescPV,
-                                  (jj > 0 || k > 0) ? 1u : 0u);
-                    tc_commit(su32(&bars->o_done[b]));
-                    tc_commit(su32(&bars->kv_empty[s]));
-                }
+                gt += T;
+                if (ok) u = next_unit_thread(bars, n, abortp);
             }
-            if (ok) mbar_wait(su32(&bars->kv_empty[(T - 1) % kStages]), ((T - 1) / kStages) & 1, abortp);
             tc_commit(su32(&bars->drain));   // every MMA issued so far
             mbar_drain(su32(&bars->drain), 0);
         }
@@ -317,93 +370,178 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
     } else if (warp == 6) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int issued = 0;
-            for (int j = 0; j < T; ++j) {
-                const int s = j % kStages;
-                if (j >= kStages &&   // the stage is free once the P.V of tile j - kStages completed
-                    !mbar_wait(su32(&bars->kv_empty[s]), ((j - kStages) / kStages) & 1, abortp))
-                    break;
-                const uint32_t bar = su32(&bars->kv_full[s]);
-                mbar_expect_tx(bar, kStageB);
-                tma_load_3d(sStage + s * kStageB, kmap, 0, c0 + j * kKT, g, bar);
-                tma_load_3d(sStage + s * kStageB + kTileB, vmap, 0, c0 + j * kKT, g, bar);
-                ++issued;
+            int gt = 0;
+            bool ok = true;
+            for (int u = blockIdx.x, m = 0; u >= 0 && ok; ++m) {
+                const Unit U = unit_of(t, layer, u);
+                for (int j = 0; j < U.T; ++j, ++gt) {
+                    const int s = gt % kStages;
+                    if (gt >= kStages &&   // the stage is free once the P.V of tile gt - kStages completed
+                        !mbar_wait(su32(&bars->kv_empty[s]), ((gt - kStages) / kStages) & 1, abortp)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t bar = su32(&bars->kv_full[s]);
+                    mbar_expect_tx(bar, kStageB);
+                    tma_load_3d(sStage + s * kStageB, U.kmap, 0, U.c0 + j * kKT, U.g, bar);
+                    tma_load_3d(sStage + s * kStageB + kTileB, U.vmap, 0, U.c0 + j * kKT, U.g, bar);
+                }
+                if (!ok) break;
+                // the next unit of the launch, for this CTA's roles
+                int un = int(gridDim.x) + atomicAdd(&t.tc_work[2 * layer], 1);
+                if (un >= n_units) un = -1;
+                const int slot = m % kUQ;
+                if (m >= kUQ && !mbar_wait(su32(&bars->uq_empty[slot]), ((m / kUQ) - 1) & 1, abortp)) break;
+                bars->uq[slot] = un;
+                mbar_arrive(su32(&bars->uq_full[slot]));   // release: the index is visible to the waiters
+                u = un;
             }
             if (*abortp)   // let the copies in flight land before the CTA exits
-                for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
-                    mbar_drain(su32(&bars->kv_full[j % kStages]), (j / kStages) & 1);
+                for (int k = gt > kStages ? gt - kStages : 0; k < gt; ++k)
+                    mbar_drain(su32(&bars->kv_full[k % kStages]), (k / kStages) & 1);
         }
         __syncwarp();
-    } else if (warp < 4) {
-        // ------------------------------------------------------------ softmax
-        softmax_tiles<kKT>(ss);
-        if (!*abortp) mbar_wait(su32(&bars->o_done[(T - 1) % kSBuf]), ((T - 1) / kSBuf) & 1, abortp);
-    } else {
+    } else if (warp == 5) {
         // ------------------------------------------------------------ V tiles bf16 -> fp16
-        for (int j = 0; j < T; ++j) {
-            const int s = j % kStages;
-            if (!mbar_wait(su32(&bars->kv_full[s]), (j / kStages) & 1, abortp)) break;
-            const uint32_t vs = sStage + s * kStageB + kTileB;
+        int gt = 0;
+        bool ok = true;
+        for (int u = blockIdx.x, m = 0; u >= 0 && ok; ++m) {
+            const int T = unit_of(t, layer, u).T;
+            for (int j = 0; j < T; ++j, ++gt) {
+                const int s = gt % kStages;
+                if (!mbar_wait(su32(&bars->kv_full[s]), (gt / kStages) & 1, abortp)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t vs = sStage + s * kStageB + kTileB;
 #pragma unroll
-            for (int c = 0; c < kTileB / 16 / 32; ++c) {
-                const uint32_t a = vs + uint32_t(lane + 32 * c) * 16u;
-                uint4 v = lds128(a);
-                v.x = bf2_to_h2(v.x);
-                v.y = bf2_to_h2(v.y);
-                v.z = bf2_to_h2(v.z);
-                v.w = bf2_to_h2(v.w);
-                sts128(a, v);
+                for (int c = 0; c < kTileB / 16 / 32; ++c) {
+                    const uint32_t a = vs + uint32_t(lane + 32 * c) * 16u;
+                    uint4 v = lds128(a);
+                    v.x = bf2_to_h2(v.x);
+                    v.y = bf2_to_h2(v.y);
+                    v.z = bf2_to_h2(v.z);
+                    v.w = bf2_to_h2(v.w);
+                    sts128(a, v);
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(su32(&bars->v_ready[s]));
+                // the stage is refilled only after this tile's P.V, which waits on
+                // this arrival, so the next use of this stage cannot overtake it
             }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(su32(&bars->v_ready[s]));
-            // the stage is refilled only after this tile's P.V, which waits on
-            // this arrival, so the next use of this stage cannot overtake it
+            if (ok) u = next_unit_warp(bars, m, abortp);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax + records
+        int gt = 0, gph = 0;
+        const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);
+        // the first unit's queries (copied by this thread) become visible to the tensor cores
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        fence_async_smem();
+        mbar_arrive(su32(&bars->q_ready));
+        for (int u = blockIdx.x, m = 0; u >= 0; ++m) {
+            const Unit U = unit_of(t, layer, u);
+            const SegStream& st = U.st;
+            const int nq = st.rows * 4, per = (nq + 3) / 4;
+            const int qi = per * warp + lane;
+            const bool qvalid = lane < per && qi < nq;
+            const bool wact = per * warp < nq;      // the warp holds at least one real row
+            const int mode = out ? st.merge_mode : kMergeKernel;   // records only in the two-call form
+            SoftState ss;
+            ss.bars = bars;
+            ss.abortp = abortp;
+            ss.trow = trow;
+            ss.g0 = gt;
+            ss.T = U.T;
+            // chunk-local key bounds: causal count of the row (of row 0 for lim_all),
+            // or every key for a FULL block
+            ss.lim = qvalid ? (full ? st.keys : st.keys - st.rows + (qi >> 2) + 1) - U.c0 : 0;
+            ss.lim_all = (full ? st.keys : st.keys - st.rows + 1) - U.c0;
+            ss.wact = wact;
+            ss.mref = -INFINITY;
+            ss.mtrue = -INFINITY;
+            ss.l = 0.f;
+            softmax_tiles<kKT>(ss);
+            gt += U.T;
+            // every q.K of this unit is done (the softmax read each S): the next
+            // unit's queries may overwrite the buffer while this one finishes
+            const int un = next_unit_warp(bars, m, abortp);
+            if (un >= 0) load_q_async(sQ, q, unit_of(t, layer, un), tid);
+            if (!*abortp) mbar_wait(su32(&bars->o_done[(gt - 1) % kSBuf]), ((gt - 1) / kSBuf) & 1, abortp);
+            tc_fence_after();
+            if (wact) {
+                // (m, l, O) renormalised to the true running max -> the chunk's record
+                const bool aborted = *abortp != 0;
+                float f = 1.f;
+                if (ss.mtrue > ss.mref && ss.mref != -INFINITY) f = ex2(ss.mref - ss.mtrue);
+                uint32_t ro[64];
+                tc_ld64(trow + kColO, ro);
+                tc_wait_ld();
+                const float lsum = ss.l;
+                if (qvalid && mode == kMergeDirect) {   // the stream's only chunk: the output itself
+                    const float inv = aborted ? NAN : 1.f / lsum;   // a row always sees key 0 of its stream
+                    float4* dst = reinterpret_cast<float4*>(out_row(out, st, U.g, qi));
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        dst[c] = make_float4(__uint_as_float(ro[4 * c]) * inv, __uint_as_float(ro[4 * c + 1]) * inv,
+                                             __uint_as_float(ro[4 * c + 2]) * inv,
+                                             __uint_as_float(ro[4 * c + 3]) * inv);
+                } else if (qvalid) {
+                    const int64_t rec = st.pbase + (int64_t(U.chunk) * TF_NKV + U.g) * nq + qi;
+                    const bool empty = ss.mtrue == -INFINITY;
+                    float4* dst = reinterpret_cast<float4*>(part_o + rec * TF_D);
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        float4 v = make_float4(__uint_as_float(ro[4 * c]) * f, __uint_as_float(ro[4 * c + 1]) * f,
+                                               __uint_as_float(ro[4 * c + 2]) * f,
+                                               __uint_as_float(ro[4 * c + 3]) * f);
+                        if (aborted) v = make_float4(NAN, NAN, NAN, NAN);
+                        else if (empty) v = make_float4(0.f, 0.f, 0.f, 0.f);
+                        dst[c] = v;
+                    }
+                    part_ml[rec] = aborted ? make_float2(NAN, INFINITY)
+                                           : make_float2(ss.mtrue, empty ? 0.f : lsum * f);
+                }
+            }
+            // O is read: the next unit's first P.V (which overwrites it) waits for
+            // this thread's next p_full arrival
+            tc_fence_before();
+            if (un >= 0) {   // the next unit's queries, copied by this thread, are visible
+                asm volatile("cp.async.wait_all;" ::: "memory");
+                fence_async_smem();
+                mbar_arrive(su32(&bars->q_ready));
+            }
+            if (mode == kMergeLastCta) {
+                // every CTA of (stream, KV head) counts its arrival after its records
+                // are visible; the last one merges and resets the counter
+                __threadfence();
+                if (group_sync(bars, gph, abortp)) {
+                    int* ctr = t.counters + (size_t(layer) * t.S + U.stream) * TF_NKV + U.g;
+                    if (tid == 0) bars->last = (atomicAdd(ctr, 1) == st.n_chunks - 1);
+                    if (group_sync(bars, gph, abortp) && bars->last) {
+                        __threadfence();
+                        merge_stream_head<4>(st, U.g, part_o, part_ml, out, tid, 128);
+                        if (tid == 0) atomicExch(ctr, 0);
+                    }
+                }
+            }
+            u = un;
         }
     }
     tc_fence_before();
-    __syncthreads();   // every MMA and copy of the CTA is done
+    __syncthreads();   // every role is done
     tc_fence_after();
-    pdl_trigger();
-
-    if (wact) {
-        // (m, l, O) renormalised to the true running max -> the chunk's record
-        const bool aborted = *abortp != 0;
-        float f = 1.f;
-        if (ss.mtrue > ss.mref && ss.mref != -INFINITY) f = ex2(ss.mref - ss.mtrue);
-        uint32_t ro[64];
-        tc_ld64(trow + kColO, ro);
-        tc_wait_ld();
-        const float lsum = ss.l;
-        float o[64];
-#pragma unroll
-        for (int d = 0; d < 64; ++d) o[d] = __uint_as_float(ro[d]);
-        if (qvalid && mode == kMergeDirect) {   // the stream's only chunk: the output itself
-            const float inv = aborted ? NAN : 1.f / lsum;   // a row always sees key 0 of its stream
-            float4* dst = reinterpret_cast<float4*>(out_row(out, st, g, qi));
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-                dst[c] = make_float4(o[4 * c] * inv, o[4 * c + 1] * inv, o[4 * c + 2] * inv, o[4 * c + 3] * inv);
-        } else if (qvalid) {
-            const int64_t rec = st.pbase + (int64_t(item.chunk) * TF_NKV + g) * nq + qi;
-            const bool empty = ss.mtrue == -INFINITY;
-            float4* dst = reinterpret_cast<float4*>(part_o + rec * TF_D);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                float4 v = make_float4(o[4 * c] * f, o[4 * c + 1] * f, o[4 * c + 2] * f, o[4 * c + 3] * f);
-                if (aborted) v = make_float4(NAN, NAN, NAN, NAN);
-                else if (empty) v = make_float4(0.f, 0.f, 0.f, 0.f);
-                dst[c] = v;
-            }
-            part_ml[rec] = aborted ? make_float2(NAN, INFINITY)
-                                   : make_float2(ss.mtrue, empty ? 0.f : lsum * f);
+    if (tid == 0) {
+        // the last CTA to finish (every unit has been handed out by then) resets
+        // the work counters for the next launch
+        __threadfence();
+        if (atomicAdd(&t.tc_work[2 * layer + 1], 1) == int(gridDim.x) - 1) {
+            atomicExch(&t.tc_work[2 * layer], 0);
+            atomicExch(&t.tc_work[2 * layer + 1], 0);
         }
     }
-    if (mode == kMergeLastCta) {
-        __shared__ int last_flag;
-        finish_last_cta(t, layer, item.stream, st, g, part_o, part_ml, out, &last_flag);
-    }
-    __syncthreads();
+    pdl_trigger();
     if (warp == 4) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
@@ -421,8 +559,11 @@ int attn_tc_prepare() {
 int launch_attn_partials_tc(const SegTable& t, int layer, const uint16_t* q, float* po, float2* pml,
                             cudaStream_t stream, float* out, int full) {
     if (!t.k_maps || !t.v_maps) return TF_EINVAL;
-    return launch_pdl(attn_partials_tc_kernel, dim3((t.n_items - t.n_items_mma) * TF_NKV), dim3(kThreads),
-                      kSmemBytes, stream, t, layer, q, po, pml, out, full);
+    const int n_units = (t.n_items - t.n_items_mma) * TF_NKV;
+    const int slots = 2 * sm_count();   // two CTAs per SM, all resident
+    const int grid = n_units < slots ? n_units : slots;
+    return launch_pdl(attn_partials_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, t, layer, q, po, pml,
+                      out, full, n_units);
 }
 
 }  // namespace tf

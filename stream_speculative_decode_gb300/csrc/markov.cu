@@ -83,11 +83,6 @@ __device__ __forceinline__ uint32_t ord_bf16(float best) {
     return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-    const int sz = valid ? 16 : 0;   // 0: fill the 16 bytes with zeros
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(sz) : "memory");
-}
-
 // The 128 base logits of one tile of the lane's row (bf16 pairs); zeros past
 // the vocabulary. The branch depends on the tile alone (uniform in the warp).
 __device__ __forceinline__ void load_base_tile(const uint16_t* brow, int v0, int vocab, uint32_t (&dst)[64]) {

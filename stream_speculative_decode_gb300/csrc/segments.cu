@@ -275,6 +275,7 @@ int tf_segments_build(const tf_stream* streams, int n_streams,
     const size_t o_mkk = off;      off = align_up(off + sizeof(unsigned long long) * S, 256);
     const size_t o_mkf = off;      off = align_up(off + sizeof(uint32_t) * S, 256);
     const size_t o_mkc = off;      off = align_up(off + sizeof(uint32_t) * n_groups, 256);
+    const size_t o_tcw = off;      off = align_up(off + sizeof(int32_t) * 2 * size_t(n_attn), 256);
     const size_t total = off;
 
     seg->host.assign(total, 0);
@@ -347,6 +348,7 @@ int tf_segments_build(const tf_stream* streams, int n_streams,
         t.mk_keys = reinterpret_cast<unsigned long long*>(b + o_mkk);   // zero in the image
         t.mk_flags = reinterpret_cast<uint32_t*>(b + o_mkf);
         t.mk_ctr = reinterpret_cast<uint32_t*>(b + o_mkc);
+        t.tc_work = reinterpret_cast<int32_t*>(b + o_tcw);   // zero in the image
         rc = attn_prepare();
         if (rc == TF_OK) rc = attn_tc_prepare();
         if (rc != TF_OK) {

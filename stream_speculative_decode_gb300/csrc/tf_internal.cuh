@@ -63,6 +63,7 @@ struct SegTable {
     unsigned long long* mk_keys;      // [S] Markov step: best (score, token) key per stream, self-resetting
     uint32_t* mk_flags;               // [S] Markov step: nonfinite / gave-up bits per stream, self-resetting
     uint32_t* mk_ctr;                 // [ceil(S/128)] Markov step: CTA arrivals per stream group
+    int32_t* tc_work;                 // [n_attn][2] tensor-core attention: units handed out, CTAs done (self-resetting)
 };
 
 constexpr int kAttnMma = 0;   // mma.sync flash-decode kernel (narrow windows)
