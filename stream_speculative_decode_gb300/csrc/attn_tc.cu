@@ -370,6 +370,9 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
     } else if (warp == 6) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
+            // K/V are read once: ask L2 to evict them first (measured 4% faster
+            // than the default policy on the 64 x 16-row round)
+            const uint64_t once = l2_evict_first();
             int gt = 0;
             bool ok = true;
             for (int u = blockIdx.x, m = 0; u >= 0 && ok; ++m) {
@@ -383,8 +386,8 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                     }
                     const uint32_t bar = su32(&bars->kv_full[s]);
                     mbar_expect_tx(bar, kStageB);
-                    tma_load_3d(sStage + s * kStageB, U.kmap, 0, U.c0 + j * kKT, U.g, bar);
-                    tma_load_3d(sStage + s * kStageB + kTileB, U.vmap, 0, U.c0 + j * kKT, U.g, bar);
+                    tma_load_3d_hint(sStage + s * kStageB, U.kmap, 0, U.c0 + j * kKT, U.g, bar, once);
+                    tma_load_3d_hint(sStage + s * kStageB + kTileB, U.vmap, 0, U.c0 + j * kKT, U.g, bar, once);
                 }
                 if (!ok) break;
                 // the next unit of the launch, for this CTA's roles
