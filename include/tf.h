@@ -56,6 +56,7 @@ extern "C" {
 #define TF_D        64
 #define TF_MAX_ROWS 16          /* window rows per stream (1 + drafts) */
 #define TF_MAX_KEYS (1 << 22)   /* cache rows per stream */
+#define TF_MAX_PROMPT_ROWS 65536  /* rows of one prompt call (tf_prompt_build) */
 #define TF_MAX_STREAMS 65536
 #define TF_MK       256         /* width of the drafter's Markov head rows (W1, W2) */
 
@@ -317,6 +318,27 @@ int tf_markov_chain(const tf_segments* seg, const void* W1, const void* W2, int 
 int tf_draft_ids(const tf_segments* seg, const int32_t* prev, const int32_t* drafts,
                  const uint8_t* draft_flag, int vocab, int32_t* ids, uint8_t* dflag,
                  tf_cuda_stream stream);
+
+/* A prompt (prefill) call of one stream ([SRD]: "Prompt calls and one-stream
+ * windows keep their launches"; the per-stream kernels' "own 16-row tiles"):
+ * `rows` new rows (row 0 first) whose K/V are already in the cache, so the
+ * cache holds `keys` entries in all (keys >= rows). The returned table serves
+ * tf_conv_rows (the rows in order with the stream's conv state; no history)
+ * and the attention calls (tf_attn, tf_attn_partials + tf_attn_merge,
+ * tf_attn_static, tf_partials_bytes): the rows run as windows of 16 rows
+ * (the last may be shorter), window t seeing its causal count
+ * keys - rows + 16t + i + 1 for its row i, all reading the one cache.
+ *   conv_state  [n_conv] -> bf16 [2][TF_H], updated in place
+ *   k_cache, v_cache [n_attn] -> bf16 [TF_NKV][kv_capacity][TF_D]
+ * The conv input, queries and outputs are [rows][...] as in the verify calls.
+ * tf_accept, tf_draft_ids and tf_markov_chain refuse a prompt table.
+ * Errors: TF_EINVAL (null/misaligned/overlapping buffers, rows < 1,
+ * keys < rows, kv_capacity < keys), TF_ERANGE (rows > TF_MAX_PROMPT_ROWS,
+ * kv_capacity > TF_MAX_KEYS), TF_ENOMEM, TF_ECUDA. Free with tf_segments_free. */
+int tf_prompt_build(int32_t rows, int32_t keys, int32_t kv_capacity,
+                    const void* const* conv_state, const void* const* k_cache,
+                    const void* const* v_cache, int n_conv, int n_attn,
+                    tf_cuda_stream stream, tf_segments** out);
 
 /* Name of a status code. */
 const char* tf_strerror(int status);

@@ -71,7 +71,7 @@ extern "C" int tf_accept(const tf_segments* seg, const int32_t* ids, const int32
                          const uint8_t* flag, int vocab, int32_t* accept_len, int32_t* next_token,
                          int32_t* new_keys, uint8_t* sflag, int rewind_conv, tf_cuda_stream stream) {
     using namespace tf;
-    if (!seg) return TF_EINVAL;
+    if (!seg || seg->prompt) return TF_EINVAL;
     const SegTable& t = seg->dev;
     if (t.S == 0) return TF_OK;
     if (!ids || !pick || !flag || !accept_len || !next_token || !new_keys || !sflag || vocab < 1)

@@ -60,7 +60,7 @@ extern "C" int tf_draft_ids(const tf_segments* seg, const int32_t* prev, const i
                             const uint8_t* draft_flag, int vocab, int32_t* ids, uint8_t* dflag,
                             tf_cuda_stream stream) {
     using namespace tf;
-    if (!seg) return TF_EINVAL;
+    if (!seg || seg->prompt) return TF_EINVAL;
     const SegTable& t = seg->dev;
     if (t.S == 0) return TF_OK;
     if (!prev || !ids || !dflag || vocab < 1) return TF_EINVAL;

@@ -385,7 +385,7 @@ extern "C" int tf_markov_chain(const tf_segments* seg, const void* W1, const voi
     if (vocab > (1 << 24)) return TF_ERANGE;
     if (!aligned16(W1) || !aligned16(W2) || !aligned16(base) || base_stride < vocab || base_stride % 8 != 0)
         return TF_EINVAL;
-    if (!seg) return TF_EINVAL;
+    if (!seg || seg->prompt) return TF_EINVAL;
     const SegTable& t = seg->dev;
     if (t.S == 0 || t.R == t.S) return TF_OK;   // no window holds a draft
     cudaError_t e = cudaFuncSetAttribute(markov_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);

@@ -117,6 +117,146 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 }  // namespace
 }  // namespace tf
 
+namespace {
+
+// The rest of a build, shared by the verify and the prompt tables: sort the
+// attention items, lay out and upload the blob, encode the TMA maps. `seg`
+// (with its plan) is owned here from now on: freed on failure.
+int finish_build(tf_segments* seg, std::vector<tf::SegStream>& ss, std::vector<int32_t>& row_stream,
+                 std::vector<tf::ConvTile>& tiles, std::vector<tf::AttnItem>& items,
+                 const void* const* conv_state, const void* const* conv_hist, const void* const* k_cache,
+                 const void* const* v_cache, int n_conv, int n_attn, tf_cuda_stream stream, tf_segments** out) {
+    using namespace tf;
+    const int S = int(ss.size());
+    const int R = int(row_stream.size());
+    const tf_plan& plan = seg->plan;
+    int rc = TF_OK;
+    // mma.sync items first, then tensor-core items; within each, largest
+    // chunks first so the long work starts early in the grid
+    std::stable_sort(items.begin(), items.end(), [&](const AttnItem& a, const AttnItem& b) {
+        const int pa = attn_path_of(ss[a.stream].rows), pb = attn_path_of(ss[b.stream].rows);
+        if (pa != pb) return pa < pb;
+        auto len = [&](const AttnItem& it) {
+            const SegStream& d = ss[it.stream];
+            int lo = it.chunk * d.chunk_keys;
+            int len_keys = std::min(d.keys, lo + d.chunk_keys) - lo;
+            return int64_t(len_keys) * ((d.rows + 3) / 4 + 1);
+        };
+        return len(a) > len(b);
+    });
+    int n_items_mma = 0, mma_rows = 1;
+    for (const AttnItem& it : items)
+        if (attn_path_of(ss[it.stream].rows) == kAttnMma) {
+            ++n_items_mma;
+            mma_rows = std::max(mma_rows, ss[it.stream].rows);
+        }
+
+    size_t off = 0;
+    const size_t o_streams = off;  off = align_up(off + sizeof(SegStream) * S, 256);
+    const size_t o_rows = off;     off = align_up(off + sizeof(int32_t) * R, 256);
+    const size_t o_tiles = off;    off = align_up(off + sizeof(ConvTile) * tiles.size(), 256);
+    const size_t o_items = off;    off = align_up(off + sizeof(AttnItem) * items.size(), 256);
+    const size_t n_cp = size_t(n_conv) * S, n_ap = size_t(n_attn) * S;
+    const size_t o_cs = off;       off = align_up(off + sizeof(void*) * n_cp, 256);
+    const size_t o_ch = off;       off = align_up(off + (conv_hist ? sizeof(void*) * n_cp : 0), 256);
+    const size_t o_k = off;        off = align_up(off + sizeof(void*) * n_ap, 256);
+    const size_t o_v = off;        off = align_up(off + sizeof(void*) * n_ap, 256);
+    const size_t n_maps = size_t(n_items_mma) < items.size() ? n_ap : 0;
+    const size_t o_km = off;       off = align_up(off + sizeof(CUtensorMap) * n_maps, 256);
+    const size_t o_vm = off;       off = align_up(off + sizeof(CUtensorMap) * n_maps, 256);
+    const size_t o_ctr = off;      off = align_up(off + sizeof(int32_t) * n_ap * TF_NKV, 256);
+    const size_t n_groups = (size_t(S) + 127) / 128;   // Markov step: 128 streams per group
+    const size_t o_mkk = off;      off = align_up(off + sizeof(unsigned long long) * S, 256);
+    const size_t o_mkf = off;      off = align_up(off + sizeof(uint32_t) * S, 256);
+    const size_t o_mkc = off;      off = align_up(off + sizeof(uint32_t) * n_groups, 256);
+    const size_t o_tcw = off;      off = align_up(off + sizeof(int32_t) * 2 * size_t(n_attn), 256);
+    const size_t total = off;
+
+    seg->host.assign(total, 0);
+    unsigned char* h = seg->host.data();
+    if (S) std::memcpy(h + o_streams, ss.data(), sizeof(SegStream) * S);
+    if (R) std::memcpy(h + o_rows, row_stream.data(), sizeof(int32_t) * R);
+    if (!tiles.empty()) std::memcpy(h + o_tiles, tiles.data(), sizeof(ConvTile) * tiles.size());
+    if (!items.empty()) std::memcpy(h + o_items, items.data(), sizeof(AttnItem) * items.size());
+    if (n_cp) std::memcpy(h + o_cs, conv_state, sizeof(void*) * n_cp);
+    if (n_cp && conv_hist) std::memcpy(h + o_ch, conv_hist, sizeof(void*) * n_cp);
+    if (n_ap) {
+        std::memcpy(h + o_k, k_cache, sizeof(void*) * n_ap);
+        std::memcpy(h + o_v, v_cache, sizeof(void*) * n_ap);
+    }
+    for (size_t i = 0; i < n_maps; ++i) {
+        const SegStream& st = ss[i % S];
+        CUtensorMap km, vm;   // aligned locals, copied into the image
+        if (!encode_kv_map(&km, k_cache[i], st.keys, st.cap) ||
+            !encode_kv_map(&vm, v_cache[i], st.keys, st.cap)) {
+            delete seg;
+            return cuda_fail(cudaErrorInvalidValue);
+        }
+        std::memcpy(h + o_km + i * sizeof(CUtensorMap), &km, sizeof(CUtensorMap));
+        std::memcpy(h + o_vm + i * sizeof(CUtensorMap), &vm, sizeof(CUtensorMap));
+    }
+    seg->streams = ss;
+
+    SegTable& t = seg->dev;
+    std::memset(&t, 0, sizeof(t));
+    t.S = S;
+    t.R = R;
+    t.n_tiles = int32_t(tiles.size());
+    t.n_items = int32_t(items.size());
+    t.n_conv = n_conv;
+    t.n_attn = n_attn;
+    t.max_rows = plan.max_rows;
+    t.has_hist = conv_hist ? 1 : 0;
+    t.n_partials = plan.n_partials;
+    t.n_items_mma = n_items_mma;
+    t.mma_mt = (mma_rows + 3) / 4;
+    t.n_merge_rows = 0;
+    for (const SegStream& d : ss)
+        if (d.merge_mode == kMergeKernel) t.n_merge_rows += d.rows;
+
+    if (total > 0 && S > 0) {
+        cudaError_t e = cudaMalloc(&seg->blob, total);
+        if (e != cudaSuccess) {
+            delete seg;
+            cuda_fail(e);
+            return e == cudaErrorMemoryAllocation ? TF_ENOMEM : TF_ECUDA;
+        }
+        e = cudaMemcpyAsync(seg->blob, h, total, cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) {
+            cudaFree(seg->blob);
+            delete seg;
+            return cuda_fail(e);
+        }
+        unsigned char* b = static_cast<unsigned char*>(seg->blob);
+        t.streams = reinterpret_cast<const SegStream*>(b + o_streams);
+        t.row_stream = reinterpret_cast<const int32_t*>(b + o_rows);
+        t.tiles = reinterpret_cast<const ConvTile*>(b + o_tiles);
+        t.items = reinterpret_cast<const AttnItem*>(b + o_items);
+        t.conv_state = reinterpret_cast<void* const*>(b + o_cs);
+        t.conv_hist = conv_hist ? reinterpret_cast<void* const*>(b + o_ch) : nullptr;
+        t.k_cache = reinterpret_cast<const void* const*>(b + o_k);
+        t.v_cache = reinterpret_cast<const void* const*>(b + o_v);
+        t.k_maps = n_maps ? reinterpret_cast<const CUtensorMap*>(b + o_km) : nullptr;
+        t.v_maps = n_maps ? reinterpret_cast<const CUtensorMap*>(b + o_vm) : nullptr;
+        t.counters = reinterpret_cast<int32_t*>(b + o_ctr);   // zero in the image
+        t.mk_keys = reinterpret_cast<unsigned long long*>(b + o_mkk);   // zero in the image
+        t.mk_flags = reinterpret_cast<uint32_t*>(b + o_mkf);
+        t.mk_ctr = reinterpret_cast<uint32_t*>(b + o_mkc);
+        t.tc_work = reinterpret_cast<int32_t*>(b + o_tcw);   // zero in the image
+        rc = attn_prepare();
+        if (rc == TF_OK) rc = attn_tc_prepare();
+        if (rc != TF_OK) {
+            cudaFree(seg->blob);
+            delete seg;
+            return rc;
+        }
+    }
+    *out = seg;
+    return TF_OK;
+}
+
+}  // namespace
+
 extern "C" {
 
 int32_t tf_chunk_keys(int32_t rows) { return 256 * (rows < 4 ? 4 : rows); }
@@ -237,128 +377,94 @@ int tf_segments_build(const tf_stream* streams, int n_streams,
             tiles.push_back({s, r0, std::min(kConvTileRows, st.rows - r0), 0});
         for (int c = 0; c < d.n_chunks; ++c) items.push_back({s, c});
     }
-    // mma.sync items first, then tensor-core items; within each, largest
-    // chunks first so the long work starts early in the grid
-    std::stable_sort(items.begin(), items.end(), [&](const AttnItem& a, const AttnItem& b) {
-        const int pa = attn_path_of(ss[a.stream].rows), pb = attn_path_of(ss[b.stream].rows);
-        if (pa != pb) return pa < pb;
-        auto len = [&](const AttnItem& it) {
-            const SegStream& d = ss[it.stream];
-            int lo = it.chunk * d.chunk_keys;
-            int len_keys = std::min(d.keys, lo + d.chunk_keys) - lo;
-            return int64_t(len_keys) * ((d.rows + 3) / 4 + 1);
-        };
-        return len(a) > len(b);
-    });
-    int n_items_mma = 0, mma_rows = 1;
-    for (const AttnItem& it : items)
-        if (attn_path_of(ss[it.stream].rows) == kAttnMma) {
-            ++n_items_mma;
-            mma_rows = std::max(mma_rows, ss[it.stream].rows);
-        }
+    return finish_build(seg, ss, row_stream, tiles, items, conv_state, conv_hist, k_cache, v_cache, n_conv, n_attn,
+                        stream, out);
+}
 
-    size_t off = 0;
-    const size_t o_streams = off;  off = align_up(off + sizeof(SegStream) * S, 256);
-    const size_t o_rows = off;     off = align_up(off + sizeof(int32_t) * R, 256);
-    const size_t o_tiles = off;    off = align_up(off + sizeof(ConvTile) * tiles.size(), 256);
-    const size_t o_items = off;    off = align_up(off + sizeof(AttnItem) * items.size(), 256);
-    const size_t n_cp = size_t(n_conv) * S, n_ap = size_t(n_attn) * S;
-    const size_t o_cs = off;       off = align_up(off + sizeof(void*) * n_cp, 256);
-    const size_t o_ch = off;       off = align_up(off + (conv_hist ? sizeof(void*) * n_cp : 0), 256);
-    const size_t o_k = off;        off = align_up(off + sizeof(void*) * n_ap, 256);
-    const size_t o_v = off;        off = align_up(off + sizeof(void*) * n_ap, 256);
-    const size_t n_maps = size_t(n_items_mma) < items.size() ? n_ap : 0;
-    const size_t o_km = off;       off = align_up(off + sizeof(CUtensorMap) * n_maps, 256);
-    const size_t o_vm = off;       off = align_up(off + sizeof(CUtensorMap) * n_maps, 256);
-    const size_t o_ctr = off;      off = align_up(off + sizeof(int32_t) * n_ap * TF_NKV, 256);
-    const size_t n_groups = (size_t(S) + 127) / 128;   // Markov step: 128 streams per group
-    const size_t o_mkk = off;      off = align_up(off + sizeof(unsigned long long) * S, 256);
-    const size_t o_mkf = off;      off = align_up(off + sizeof(uint32_t) * S, 256);
-    const size_t o_mkc = off;      off = align_up(off + sizeof(uint32_t) * n_groups, 256);
-    const size_t o_tcw = off;      off = align_up(off + sizeof(int32_t) * 2 * size_t(n_attn), 256);
-    const size_t total = off;
-
-    seg->host.assign(total, 0);
-    unsigned char* h = seg->host.data();
-    if (S) std::memcpy(h + o_streams, ss.data(), sizeof(SegStream) * S);
-    if (R) std::memcpy(h + o_rows, row_stream.data(), sizeof(int32_t) * R);
-    if (!tiles.empty()) std::memcpy(h + o_tiles, tiles.data(), sizeof(ConvTile) * tiles.size());
-    if (!items.empty()) std::memcpy(h + o_items, items.data(), sizeof(AttnItem) * items.size());
-    if (n_cp) std::memcpy(h + o_cs, conv_state, sizeof(void*) * n_cp);
-    if (n_cp && conv_hist) std::memcpy(h + o_ch, conv_hist, sizeof(void*) * n_cp);
-    if (n_ap) {
-        std::memcpy(h + o_k, k_cache, sizeof(void*) * n_ap);
-        std::memcpy(h + o_v, v_cache, sizeof(void*) * n_ap);
+int tf_prompt_build(int32_t rows, int32_t keys, int32_t kv_capacity, const void* const* conv_state,
+                    const void* const* k_cache, const void* const* v_cache, int n_conv, int n_attn,
+                    tf_cuda_stream stream, tf_segments** out) {
+    using namespace tf;
+    if (!out) return TF_EINVAL;
+    *out = nullptr;
+    if (n_conv < 0 || n_attn < 0 || n_conv > 4096 || n_attn > 4096) return TF_EINVAL;
+    if (rows < 1 || keys < rows || kv_capacity < keys) return TF_EINVAL;
+    if (rows > TF_MAX_PROMPT_ROWS || kv_capacity > TF_MAX_KEYS) return TF_ERANGE;
+    if ((n_conv > 0 && !conv_state) || (n_attn > 0 && (!k_cache || !v_cache))) return TF_EINVAL;
+    std::vector<Interval> conv_iv, kv_iv;
+    for (int l = 0; l < n_conv; ++l) {
+        const void* p = conv_state[l];
+        if (!p || !aligned16(p)) return TF_EINVAL;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+        conv_iv.push_back({a, a + size_t(2) * TF_H * 2});
     }
-    for (size_t i = 0; i < n_maps; ++i) {
-        const tf_stream& st = streams[i % S];
-        CUtensorMap km, vm;   // aligned locals, copied into the image
-        if (!encode_kv_map(&km, k_cache[i], st.keys, st.kv_capacity) ||
-            !encode_kv_map(&vm, v_cache[i], st.keys, st.kv_capacity)) {
-            delete seg;
-            return cuda_fail(cudaErrorInvalidValue);
-        }
-        std::memcpy(h + o_km + i * sizeof(CUtensorMap), &km, sizeof(CUtensorMap));
-        std::memcpy(h + o_vm + i * sizeof(CUtensorMap), &vm, sizeof(CUtensorMap));
+    const size_t kv_bytes = size_t(TF_NKV) * kv_capacity * TF_D * 2;
+    for (int l = 0; l < n_attn; ++l) {
+        const void* k = k_cache[l];
+        const void* v = v_cache[l];
+        if (!k || !v || !aligned16(k) || !aligned16(v)) return TF_EINVAL;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(k), b = reinterpret_cast<uintptr_t>(v);
+        kv_iv.push_back({a, a + kv_bytes});
+        kv_iv.push_back({b, b + kv_bytes});
     }
-    seg->streams = ss;
+    if (any_overlap(conv_iv) || any_overlap(kv_iv)) return TF_EINVAL;
 
-    SegTable& t = seg->dev;
-    std::memset(&t, 0, sizeof(t));
-    t.S = S;
-    t.R = R;
-    t.n_tiles = int32_t(tiles.size());
-    t.n_items = int32_t(items.size());
-    t.n_conv = n_conv;
-    t.n_attn = n_attn;
-    t.max_rows = plan.max_rows;
-    t.has_hist = conv_hist ? 1 : 0;
-    t.n_partials = plan.n_partials;
-    t.n_items_mma = n_items_mma;
-    t.mma_mt = (mma_rows + 3) / 4;
-    t.n_merge_rows = 0;
-    for (const SegStream& d : ss)
-        if (d.merge_mode == kMergeKernel) t.n_merge_rows += d.rows;
-
-    if (total > 0 && S > 0) {
-        cudaError_t e = cudaMalloc(&seg->blob, total);
-        if (e != cudaSuccess) {
-            delete seg;
-            cuda_fail(e);
-            return e == cudaErrorMemoryAllocation ? TF_ENOMEM : TF_ECUDA;
-        }
-        e = cudaMemcpyAsync(seg->blob, h, total, cudaMemcpyHostToDevice, stream);
-        if (e != cudaSuccess) {
-            cudaFree(seg->blob);
-            delete seg;
-            return cuda_fail(e);
-        }
-        unsigned char* b = static_cast<unsigned char*>(seg->blob);
-        t.streams = reinterpret_cast<const SegStream*>(b + o_streams);
-        t.row_stream = reinterpret_cast<const int32_t*>(b + o_rows);
-        t.tiles = reinterpret_cast<const ConvTile*>(b + o_tiles);
-        t.items = reinterpret_cast<const AttnItem*>(b + o_items);
-        t.conv_state = reinterpret_cast<void* const*>(b + o_cs);
-        t.conv_hist = conv_hist ? reinterpret_cast<void* const*>(b + o_ch) : nullptr;
-        t.k_cache = reinterpret_cast<const void* const*>(b + o_k);
-        t.v_cache = reinterpret_cast<const void* const*>(b + o_v);
-        t.k_maps = n_maps ? reinterpret_cast<const CUtensorMap*>(b + o_km) : nullptr;
-        t.v_maps = n_maps ? reinterpret_cast<const CUtensorMap*>(b + o_vm) : nullptr;
-        t.counters = reinterpret_cast<int32_t*>(b + o_ctr);   // zero in the image
-        t.mk_keys = reinterpret_cast<unsigned long long*>(b + o_mkk);   // zero in the image
-        t.mk_flags = reinterpret_cast<uint32_t*>(b + o_mkf);
-        t.mk_ctr = reinterpret_cast<uint32_t*>(b + o_mkc);
-        t.tc_work = reinterpret_cast<int32_t*>(b + o_tcw);   // zero in the image
-        rc = attn_prepare();
-        if (rc == TF_OK) rc = attn_tc_prepare();
-        if (rc != TF_OK) {
-            cudaFree(seg->blob);
-            delete seg;
-            return rc;
-        }
+    // stream 0: the conv's view (every row, one state); streams 1..T: the
+    // attention's 16-row tiles, each a window of its own causal count over
+    // the same cache
+    const int T = (rows + kPromptTileRows - 1) / kPromptTileRows;
+    const int S = 1 + T;
+    std::vector<tf_stream> tiles_as_streams;
+    for (int t = 0; t < T; ++t) {
+        const int r = std::min(kPromptTileRows, rows - t * kPromptTileRows);
+        tiles_as_streams.push_back({r, t * kPromptTileRows, keys - rows + t * kPromptTileRows + r, kv_capacity});
     }
-    *out = seg;
-    return TF_OK;
+    tf_plan plan;
+    int rc = tf_segments_plan(tiles_as_streams.data(), T, &plan);   // the attention work
+    if (rc != TF_OK) return rc;
+    plan.n_streams = 1;
+    plan.n_conv_tiles = (rows + kConvTileRows - 1) / kConvTileRows;
+
+    tf_segments* seg = new (std::nothrow) tf_segments();
+    if (!seg) return TF_ENOMEM;
+    seg->plan = plan;
+    seg->prompt = true;
+    std::vector<SegStream> ss(S);
+    std::vector<int32_t> row_stream(rows);
+    std::vector<ConvTile> tiles;
+    std::vector<AttnItem> items;
+    ss[0] = {rows, 0, keys, kv_capacity, 0, 0, 0, kMergeDirect, 0};
+    for (int r0 = 0; r0 < rows; r0 += kConvTileRows) tiles.push_back({0, r0, std::min(kConvTileRows, rows - r0), 0});
+    int64_t pbase = 0;
+    for (int t = 0; t < T; ++t) {
+        const tf_stream& st = tiles_as_streams[t];
+        SegStream& d = ss[1 + t];
+        d.rows = st.rows;
+        d.row_offset = st.row_offset;
+        d.keys = st.keys;
+        d.cap = st.kv_capacity;
+        d.chunk_keys = tf_chunk_keys(st.rows);
+        d.n_chunks = (st.keys + d.chunk_keys - 1) / d.chunk_keys;
+        d.pbase = pbase;
+        pbase += int64_t(st.rows) * TF_NQ * d.n_chunks;
+        d.merge_mode = d.n_chunks == 1 ? kMergeDirect
+                     : (4 * st.rows * d.n_chunks <= kMergeLastCtaMaxRecords ? kMergeLastCta : kMergeKernel);
+        d.pad_ = 0;
+        for (int i = 0; i < st.rows; ++i) row_stream[st.row_offset + i] = 1 + t;
+        for (int c = 0; c < d.n_chunks; ++c) items.push_back({1 + t, c});
+    }
+    // pointer arrays [layer][S]: every stream of a layer names the layer's
+    // state and caches (the conv reaches them through stream 0 only)
+    std::vector<const void*> cs(size_t(n_conv) * S), kc(size_t(n_attn) * S), vc(size_t(n_attn) * S);
+    for (int l = 0; l < n_conv; ++l)
+        for (int s = 0; s < S; ++s) cs[size_t(l) * S + s] = conv_state[l];
+    for (int l = 0; l < n_attn; ++l)
+        for (int s = 0; s < S; ++s) {
+            kc[size_t(l) * S + s] = k_cache[l];
+            vc[size_t(l) * S + s] = v_cache[l];
+        }
+    return finish_build(seg, ss, row_stream, tiles, items, n_conv ? cs.data() : nullptr, nullptr,
+                        n_attn ? kc.data() : nullptr, n_attn ? vc.data() : nullptr, n_conv, n_attn, stream, out);
 }
 
 int tf_segments_free(tf_segments* seg) {

@@ -39,6 +39,7 @@ struct AttnItem {
 };
 
 constexpr int kConvTileRows = 8;
+constexpr int kPromptTileRows = 16;   // a prompt call's attention runs in windows of this many rows
 
 // Device view of a segment table, passed to kernels by value.
 struct SegTable {
@@ -90,6 +91,7 @@ struct tf_segments {
     std::vector<unsigned char> host;   // host image of the blob (kept for the async copy)
     std::vector<tf::SegStream> streams;
     tf_plan plan{};
+    bool prompt = false;               // built by tf_prompt_build (conv + attention only)
 };
 
 namespace tf {

@@ -101,6 +101,15 @@ def workload(index, n_conv=None, n_attn=None, vocab=None):
     return w
 
 
+def prompt_workload(rows, cached, n_conv, n_attn, seed=11):
+    """One stream's prompt call: ``rows`` new rows after ``cached`` keys (their
+    K/V already appended, so the cache holds cached + rows keys); the same
+    widths and distributions as the verify workloads (no logits are needed: a
+    tiny vocabulary keeps the generator light)."""
+    return Workload(f"prompt {rows} rows after {cached} keys", [rows], [cached + rows], n_conv, n_attn,
+                    vocab=8, drafts="none", seed=seed)
+
+
 def row_offsets(rows):
     off, out = 0, []
     for r in rows:

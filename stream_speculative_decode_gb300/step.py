@@ -48,8 +48,16 @@ class DeviceStep:
     per-layer conv inputs, queries and the logits are the step's inputs.
     """
 
-    def __init__(self, inp: StepInputs, device="cuda", keep_history=True, stream=None, fused_attention=True):
+    def __init__(self, inp: StepInputs, device="cuda", keep_history=True, stream=None, fused_attention=True,
+                 prompt=False):
+        """``prompt``: one stream's prompt call (any number of rows; the table
+        from tf_prompt_build: conv over every row, attention in 16-row
+        windows; no history, no pick or accept)."""
         self.inp = inp
+        self.prompt = prompt
+        if prompt:
+            assert len(inp.streams) == 1, "a prompt call has one stream"
+            keep_history = False
         self.device = torch.device(device)
         self.S = S = len(inp.streams)
         self.R = R = inp.R
@@ -95,8 +103,12 @@ class DeviceStep:
                          for l in range(n_conv) for s in range(S)]
         kp = [self.K[l][s].data_ptr() for l in range(n_attn) for s in range(S)]
         vp = [self.V[l][s].data_ptr() for l in range(n_attn) for s in range(S)]
-        self.seg = tf.tf_segments_build(self.c_streams, conv_state, conv_hist, kp, vp, n_conv, n_attn,
-                                        stream=stream)
+        if prompt:
+            rows, _off, keys, cap = self.c_streams[0]
+            self.seg = tf.tf_prompt_build(rows, keys, cap, conv_state, kp, vp, n_conv, n_attn, stream=stream)
+        else:
+            self.seg = tf.tf_segments_build(self.c_streams, conv_state, conv_hist, kp, vp, n_conv, n_attn,
+                                            stream=stream)
         self.partials = torch.empty(max(self.seg.partials_bytes, 16), dtype=torch.uint8, device=dev)
         self.schedule = layer_schedule(n_conv, n_attn)
         self.fused_attention = fused_attention
@@ -132,7 +144,8 @@ class DeviceStep:
                 ev1.record(stream)
             else:
                 self.attn(l, stream)
-        self.head(rewind, stream)
+        if not self.prompt:
+            self.head(rewind, stream)
 
     def launches_per_step(self):
         """Kernel launches of one step: a conv per conv layer, per attention
@@ -140,7 +153,7 @@ class DeviceStep:
         then the pick and the accept."""
         p = self.seg.plan
         per_attn = p["attn_kernels"] + (p["attn_merge_launch"] if self.fused_attention else 1)
-        return self.n_conv + self.n_attn * per_attn + 2
+        return self.n_conv + self.n_attn * per_attn + (0 if self.prompt else 2)
 
     def capture(self, rewind=True, events=None):
         """Capture one step into a CUDA graph (on a side stream)."""

@@ -17,6 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libtf.so")
 
 TF_H, TF_CIN, TF_KW, TF_NQ, TF_NKV, TF_D = 2048, 6144, 3, 32, 8, 64
 TF_MAX_ROWS = 16
+TF_MAX_PROMPT_ROWS = 65536
 TF_MK = 256
 TF_DFLAG_BAD_PENDING, TF_DFLAG_BAD_DRAFT = 1, 2
 TF_OK, TF_EINVAL, TF_ERANGE, TF_ENOMEM, TF_ECUDA = 0, 1, 2, 3, 4
@@ -25,8 +26,8 @@ TF_OK, TF_EINVAL, TF_ERANGE, TF_ENOMEM, TF_ECUDA = 0, 1, 2, 3, 4
 EXPORTS = ("tf_chunk_keys", "tf_segments_plan", "tf_segments_build", "tf_segments_free",
            "tf_segments_query", "tf_partials_bytes", "tf_conv_rows", "tf_attn_partials",
            "tf_attn_merge", "tf_attn", "tf_attn_static", "tf_attn_block_partials", "tf_attn_block",
-           "tf_argmax_rows", "tf_accept", "tf_markov_chain", "tf_draft_ids", "tf_strerror",
-           "tf_last_cuda_error")
+           "tf_argmax_rows", "tf_accept", "tf_markov_chain", "tf_draft_ids", "tf_prompt_build",
+           "tf_strerror", "tf_last_cuda_error")
 TF_STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -66,6 +67,8 @@ def _load():
         "tf_segments_plan": (i32, [P(tf_stream), i32, P(tf_plan)]),
         "tf_segments_build": (i32, [P(tf_stream), i32, P(vp), P(vp), P(vp), P(vp), i32, i32, vp, P(vp)]),
         "tf_segments_free": (i32, [vp]),
+        "tf_prompt_build": (i32, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, P(vp), P(vp), P(vp), i32, i32, vp,
+                                  P(vp)]),
         "tf_segments_query": (i32, [vp, P(tf_plan)]),
         "tf_partials_bytes": (sz, [vp]),
         "tf_conv_rows": (i32, [vp, i32, vp, vp, vp, vp]),
@@ -188,6 +191,22 @@ def tf_segments_build(streams, conv_state, conv_hist, k_cache, v_cache, n_conv, 
     rc, handle = tf_segments_build_status(streams, conv_state, conv_hist, k_cache, v_cache,
                                           n_conv, n_attn, stream)
     _check("tf_segments_build", rc)
+    return Segments(handle)
+
+
+def tf_prompt_build_status(rows, keys, kv_capacity, conv_state, k_cache, v_cache, n_conv, n_attn, stream=None):
+    """Raw status and handle of tf_prompt_build; pointer lists are [layer]."""
+    out = ctypes.c_void_p()
+    rc = _lib.tf_prompt_build(rows, keys, kv_capacity, _ptr_array(conv_state), _ptr_array(k_cache),
+                              _ptr_array(v_cache), n_conv, n_attn, _stream(stream), ctypes.byref(out))
+    return rc, out.value
+
+
+def tf_prompt_build(rows, keys, kv_capacity, conv_state, k_cache, v_cache, n_conv, n_attn, stream=None):
+    """A prompt (prefill) call's table: conv over every row, attention in 16-row windows."""
+    rc, handle = tf_prompt_build_status(rows, keys, kv_capacity, conv_state, k_cache, v_cache, n_conv, n_attn,
+                                        stream)
+    _check("tf_prompt_build", rc)
     return Segments(handle)
 
 

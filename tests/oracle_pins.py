@@ -254,6 +254,18 @@ def pin_attn_causal_edge(impl):
     assert not np.allclose(out1[rows - 1], out3[rows - 1])
 
 
+def pin_attn_window_equals_rows(impl):
+    """A window of r rows is r one-row windows, row i seeing keys - r + i + 1
+    keys (what lets a prompt run in 16-row windows over one cache)."""
+    rng = np.random.default_rng(28)
+    rows, keys = 21, 60
+    q, K, V = _attn_inputs(rng, rows, keys)
+    whole = impl.attention_stream(q, K, V, keys, rows)
+    for i in range(rows):
+        one = impl.attention_stream(q[i:i + 1], K, V, keys - rows + i + 1, 1)
+        assert np.allclose(whole[i], one[0], rtol=0, atol=1e-13), i
+
+
 def pin_attn_split_merge(impl):
     """Split-K partials merged by log-sum-exp equal the unsplit softmax, for
     chunk sizes that leave empty chunks for early rows."""
@@ -480,7 +492,7 @@ ALL_PINS = [
     pin_conv_worked, pin_conv_special_taps, pin_conv_window_equals_steps,
     pin_conv_causal, pin_rewind,
     pin_attn_one_key, pin_attn_q_zero, pin_attn_two_keys_scale, pin_attn_gqa,
-    pin_attn_causal_edge, pin_attn_split_merge, pin_attn_permutation, pin_attn_brute,
+    pin_attn_causal_edge, pin_attn_split_merge, pin_attn_permutation, pin_attn_brute, pin_attn_window_equals_rows,
     pin_attn_full_q_zero, pin_attn_full_brute, pin_attn_full_split_merge, pin_attn_full_layer,
     pin_argmax_golden, pin_argmax_brute,
     pin_accept_cases, pin_accept_recipe,

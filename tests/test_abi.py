@@ -176,6 +176,21 @@ def test_draft_side_refusals(T):
     assert lib.tf_markov_chain(None, None, a, 1000, a, 1000, a, a, a, None) == T.TF_EINVAL
 
 
+def test_prompt_build_refusals(T):
+    a = 0x1000
+    kv = [a], [a + 0x100000]
+    assert T.tf_prompt_build_status(0, 10, 64, [a + 0x200000], *kv, 1, 1, 0)[0] == T.TF_EINVAL      # rows < 1
+    assert T.tf_prompt_build_status(10, 5, 64, [a + 0x200000], *kv, 1, 1, 0)[0] == T.TF_EINVAL      # keys < rows
+    assert T.tf_prompt_build_status(10, 100, 64, [a + 0x200000], *kv, 1, 1, 0)[0] == T.TF_EINVAL    # cap < keys
+    big = T.TF_MAX_PROMPT_ROWS + 1
+    assert T.tf_prompt_build_status(big, big, big + 64, [a + 0x20000000], [a], [a + 0x10000000], 1, 1, 0)[0] \
+        == T.TF_ERANGE
+    assert T.tf_prompt_build_status(10, 10, 64, [a + 8], *kv, 1, 1, 0)[0] == T.TF_EINVAL           # misaligned
+    assert T.tf_prompt_build_status(10, 10, 64, [a + 0x200000], [a], [a + 64], 1, 1, 0)[0] == T.TF_EINVAL  # K, V overlap
+    assert T.tf_prompt_build_status(10, 10, 64, None, *kv, 1, 1, 0)[0] == T.TF_EINVAL               # no state
+    assert T.tf_prompt_build_status(10, 10, 64, [a + 0x200000], None, None, 1, 1, 0)[0] == T.TF_EINVAL
+
+
 def test_argmax_refusals(T):
     lib = T.lib()
     assert lib.tf_argmax_rows(None, 0, 10, 10, None, None, None) == T.TF_OK       # empty
