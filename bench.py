@@ -18,7 +18,9 @@ on the host cores on a bounded sample of the same workload.
 windows instead of the verify step (default workload 5, the 64 x 16-row
 table): ``markov`` the Markov head's chain over every draft row
 (tf_markov_chain, one launch per step), ``block`` one layer of the
-non-causal block attention (tf_attn_block). Each prints its own JSON line.
+non-causal block attention (tf_attn_block), ``prompt`` one conv and one
+attention layer of a prompt (prefill) call of one stream (tf_prompt_build;
+2,048 rows after 14,336 cached keys by default). Each prints its own JSON line.
 """
 
 import argparse
@@ -47,7 +49,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", type=int, default=None, choices=[1, 2, 3, 4, 5],
                     help="default 2 for the verify step, 5 for --row")
-    ap.add_argument("--row", default="verify", choices=["verify", "markov", "block"])
+    ap.add_argument("--row", default="verify", choices=["verify", "markov", "block", "prompt"])
+    ap.add_argument("--prompt-rows", type=int, default=2048, help="--row prompt: rows of the prompt chunk")
+    ap.add_argument("--prompt-cached", type=int, default=14336, help="--row prompt: keys cached before it")
     ap.add_argument("--impl", default="tf", choices=["tf", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -509,6 +513,26 @@ def run_row(args, rank, world):
         launches = steps_per_call
         extra = {"markov_steps": steps_per_call, "w2_bytes": w.vocab * I.MK * 2,
                  "w2_reads_if_no_l2_reuse": steps_per_call * w.vocab * I.MK * 2}
+    elif args.row == "prompt":
+        rows, cached = args.prompt_rows, args.prompt_cached
+        w = I.prompt_workload(rows, cached, n_conv=1, n_attn=1)
+        inp = I.make_inputs(w, backend="torch", device=dev)
+        d = DeviceStep(inp, device=dev, prompt=True)
+
+        def call(st):
+            tf.tf_conv_rows(d.seg, 0, d.bcx[0], d.w[0], d.y[0], st)
+            tf.tf_attn(d.seg, 0, d.q[0], d.partials, d.out[0], st)
+
+        units, metric, unit = rows, "prompt rows/s per conv + attention layer pair", "rows/s"
+        # causal attention: row i sees cached + i + 1 keys; q.K and P.V are 2*64 flops each per
+        # (row, head, key)
+        flops = 4.0 * 64 * 32 * sum(cached + i + 1 for i in range(rows))
+        alg = flops
+        kname = "tf_attn over the prompt's 16-row windows (+ one tf_conv_rows)"
+        launches = 1 + d.seg.plan["attn_kernels"] + d.seg.plan["attn_merge_launch"]
+        extra = {"prompt_rows": rows, "cached_keys": cached, "windows": (rows + 15) // 16,
+                 "compulsory_hbm_bytes": (cached + rows) * 8 * 64 * 2 * 2 + rows * (6144 * 2 + 2048 * 4)
+                 + rows * 32 * 64 * (2 + 4)}
     else:
         w = I.workload(args.workload, n_conv=0, n_attn=1)
         inp = I.make_inputs(w, backend="torch", device=dev)
@@ -552,6 +576,15 @@ def run_row(args, rank, world):
     ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     value, ms_max = aggregate(units, ms, world, device=dev)
     achieved = alg / (ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "unit": "GB/s", "peak": peak, "peak_kind": peak_kind}
+    if args.row == "prompt":   # prefill attention is a contraction: FLOP/s against the bf16 tensor peak
+        try:
+            with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+                tpk, tkind = float(json.load(f)["bf16_tflops"]), "measured"
+        except (OSError, KeyError, ValueError):
+            tpk, tkind = 1900.0, "fallback"
+        achieved = alg / (ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "unit": "TFLOP/s", "peak": tpk, "peak_kind": tkind}
     line = {
         "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
@@ -559,9 +592,10 @@ def run_row(args, rank, world):
         "config": dict(workload_config(w), row=args.row,
                        l2="flushed: 256 MB written between timed steps, outside the events",
                        graph="one CUDA graph per step", parallelism=f"replicas x{world}", **extra),
-        "roofline": {"kernel": kname, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "algorithmic_bytes_per_call": alg,
-                     "avg_call_ms": ms, "peak_kind": peak_kind,
+        "roofline": {"kernel": kname, "bound": roof["bound"], "achieved": achieved, "peak": roof["peak"],
+                     "unit": roof["unit"], "frac": achieved / roof["peak"], "traffic": None,
+                     ("algorithmic_flops_per_call" if args.row == "prompt" else "algorithmic_bytes_per_call"): alg,
+                     "avg_call_ms": ms, "peak_kind": roof["peak_kind"],
                      "timing": "CUDA events around each graph replay (one call)"},
         "gpu_launches": launches * args.steps,
         "clocks": clocks.summary(t0, t1),
