@@ -528,9 +528,10 @@ def run_row(args, rank, world):
         # (row, head, key)
         flops = 4.0 * 64 * 32 * sum(cached + i + 1 for i in range(rows))
         alg = flops
-        kname = "tf_attn over the prompt's 16-row windows (+ one tf_conv_rows)"
+        wr = tf.TF_PROMPT_WINDOW_ROWS
+        kname = f"tf_attn over the prompt's {wr}-row windows (+ one tf_conv_rows)"
         launches = 1 + d.seg.plan["attn_kernels"] + d.seg.plan["attn_merge_launch"]
-        extra = {"prompt_rows": rows, "cached_keys": cached, "windows": (rows + 15) // 16,
+        extra = {"prompt_rows": rows, "cached_keys": cached, "windows": (rows + wr - 1) // wr,
                  "compulsory_hbm_bytes": (cached + rows) * 8 * 64 * 2 * 2 + rows * (6144 * 2 + 2048 * 4)
                  + rows * 32 * 64 * (2 + 4)}
     else:

@@ -57,6 +57,7 @@ extern "C" {
 #define TF_MAX_ROWS 16          /* window rows per stream (1 + drafts) */
 #define TF_MAX_KEYS (1 << 22)   /* cache rows per stream */
 #define TF_MAX_PROMPT_ROWS 65536  /* rows of one prompt call (tf_prompt_build) */
+#define TF_PROMPT_WINDOW_ROWS 32  /* a prompt call's attention window (tf_prompt_build) */
 #define TF_MAX_STREAMS 65536
 #define TF_MK       256         /* width of the drafter's Markov head rows (W1, W2) */
 
@@ -320,14 +321,17 @@ int tf_draft_ids(const tf_segments* seg, const int32_t* prev, const int32_t* dra
                  tf_cuda_stream stream);
 
 /* A prompt (prefill) call of one stream ([SRD]: "Prompt calls and one-stream
- * windows keep their launches"; the per-stream kernels' "own 16-row tiles"):
+ * windows keep their launches"; the per-stream kernels run them in their own
+ * 16-row tiles, here 32-row windows, which fill a 128-lane tensor-core tile
+ * with their 4 query heads per KV head):
  * `rows` new rows (row 0 first) whose K/V are already in the cache, so the
  * cache holds `keys` entries in all (keys >= rows). The returned table serves
  * tf_conv_rows (the rows in order with the stream's conv state; no history)
  * and the attention calls (tf_attn, tf_attn_partials + tf_attn_merge,
- * tf_attn_static, tf_partials_bytes): the rows run as windows of 16 rows
- * (the last may be shorter), window t seeing its causal count
- * keys - rows + 16t + i + 1 for its row i, all reading the one cache.
+ * tf_attn_static, tf_partials_bytes): the rows run as windows of
+ * W = TF_PROMPT_WINDOW_ROWS rows (the last may be shorter), window t seeing
+ * its causal count keys - rows + W*t + i + 1 for its row i, all reading the
+ * one cache.
  *   conv_state  [n_conv] -> bf16 [2][TF_H], updated in place
  *   k_cache, v_cache [n_attn] -> bf16 [TF_NKV][kv_capacity][TF_D]
  * The conv input, queries and outputs are [rows][...] as in the verify calls.

@@ -92,6 +92,7 @@ bool encode_w2_map(CUtensorMap* out, const void* w2, int rows) {
 // Attention kernel of a stream: tensor cores once its window holds 3 rows (12
 // query rows per KV head); TF_ATTN_PATH=mma|tc forces one (tests compare both).
 int attn_path_of(int rows) {
+    if (rows > 16) return kAttnTc;   // the mma.sync kernel holds at most four 16-row query tiles
     const char* e = std::getenv("TF_ATTN_PATH");
     if (e && std::strcmp(e, "mma") == 0) return kAttnMma;
     if (e && std::strcmp(e, "tc") == 0) return kAttnTc;
@@ -115,6 +116,50 @@ bool any_overlap(std::vector<Interval>& v) {
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
+}  // namespace tf
+
+namespace tf {
+
+// The plan of a set of windows, each of at most `max_window_rows` rows
+// (TF_MAX_ROWS for the verify tables, kPromptTileRows for a prompt call).
+int plan_windows(const tf_stream* streams, int n_streams, tf_plan* out, int max_window_rows) {
+    if (!out) return TF_EINVAL;
+    std::memset(out, 0, sizeof(*out));
+    if (n_streams < 0) return TF_EINVAL;
+    if (n_streams > TF_MAX_STREAMS) return TF_ERANGE;
+    if (n_streams > 0 && !streams) return TF_EINVAL;
+    int64_t R = 0, parts = 0, items = 0, tiles = 0;
+    int max_rows = 0;
+    bool any_mma = false, any_tc = false, any_merge = false;
+    for (int s = 0; s < n_streams; ++s) {
+        const tf_stream& st = streams[s];
+        if (st.rows < 1 || st.keys < 1 || st.kv_capacity < 1) return TF_EINVAL;
+        if (st.rows > max_window_rows || st.kv_capacity > TF_MAX_KEYS) return TF_ERANGE;
+        if (st.row_offset != R) return TF_EINVAL;          // packed, in order
+        if (st.keys < st.rows || st.keys > st.kv_capacity) return TF_EINVAL;
+        int64_t chunk = tf_chunk_keys(st.rows);
+        int64_t nch = (st.keys + chunk - 1) / chunk;
+        R += st.rows;
+        parts += int64_t(st.rows) * TF_NQ * nch;
+        items += nch;
+        tiles += (st.rows + tf::kConvTileRows - 1) / tf::kConvTileRows;
+        max_rows = std::max(max_rows, int(st.rows));
+        (tf::attn_path_of(st.rows) == tf::kAttnTc ? any_tc : any_mma) = true;
+        if (nch > 1 && 4 * st.rows * nch > tf::kMergeLastCtaMaxRecords) any_merge = true;
+    }
+    if (R > (1 << 24)) return TF_ERANGE;
+    out->n_streams = n_streams;
+    out->n_rows = int32_t(R);
+    out->max_rows = max_rows;
+    out->n_conv_tiles = int32_t(tiles);
+    out->n_attn_items = int32_t(items);
+    out->attn_kernels = int32_t(any_mma) + int32_t(any_tc);
+    out->attn_merge_launch = int32_t(any_merge);
+    out->n_partials = parts;
+    out->partials_bytes = parts * TF_D * 4 + parts * 8;
+    return TF_OK;
+}
+
 }  // namespace tf
 
 namespace {
@@ -262,41 +307,7 @@ extern "C" {
 int32_t tf_chunk_keys(int32_t rows) { return 256 * (rows < 4 ? 4 : rows); }
 
 int tf_segments_plan(const tf_stream* streams, int n_streams, tf_plan* out) {
-    if (!out) return TF_EINVAL;
-    std::memset(out, 0, sizeof(*out));
-    if (n_streams < 0) return TF_EINVAL;
-    if (n_streams > TF_MAX_STREAMS) return TF_ERANGE;
-    if (n_streams > 0 && !streams) return TF_EINVAL;
-    int64_t R = 0, parts = 0, items = 0, tiles = 0;
-    int max_rows = 0;
-    bool any_mma = false, any_tc = false, any_merge = false;
-    for (int s = 0; s < n_streams; ++s) {
-        const tf_stream& st = streams[s];
-        if (st.rows < 1 || st.keys < 1 || st.kv_capacity < 1) return TF_EINVAL;
-        if (st.rows > TF_MAX_ROWS || st.kv_capacity > TF_MAX_KEYS) return TF_ERANGE;
-        if (st.row_offset != R) return TF_EINVAL;          // packed, in order
-        if (st.keys < st.rows || st.keys > st.kv_capacity) return TF_EINVAL;
-        int64_t chunk = tf_chunk_keys(st.rows);
-        int64_t nch = (st.keys + chunk - 1) / chunk;
-        R += st.rows;
-        parts += int64_t(st.rows) * TF_NQ * nch;
-        items += nch;
-        tiles += (st.rows + tf::kConvTileRows - 1) / tf::kConvTileRows;
-        max_rows = std::max(max_rows, int(st.rows));
-        (tf::attn_path_of(st.rows) == tf::kAttnTc ? any_tc : any_mma) = true;
-        if (nch > 1 && 4 * st.rows * nch > tf::kMergeLastCtaMaxRecords) any_merge = true;
-    }
-    if (R > (1 << 24)) return TF_ERANGE;
-    out->n_streams = n_streams;
-    out->n_rows = int32_t(R);
-    out->max_rows = max_rows;
-    out->n_conv_tiles = int32_t(tiles);
-    out->n_attn_items = int32_t(items);
-    out->attn_kernels = int32_t(any_mma) + int32_t(any_tc);
-    out->attn_merge_launch = int32_t(any_merge);
-    out->n_partials = parts;
-    out->partials_bytes = parts * TF_D * 4 + parts * 8;
-    return TF_OK;
+    return tf::plan_windows(streams, n_streams, out, TF_MAX_ROWS);
 }
 
 int tf_segments_build(const tf_stream* streams, int n_streams,
@@ -410,8 +421,8 @@ int tf_prompt_build(int32_t rows, int32_t keys, int32_t kv_capacity, const void*
     if (any_overlap(conv_iv) || any_overlap(kv_iv)) return TF_EINVAL;
 
     // stream 0: the conv's view (every row, one state); streams 1..T: the
-    // attention's 16-row tiles, each a window of its own causal count over
-    // the same cache
+    // attention's windows of kPromptTileRows rows, each with its own causal
+    // count over the same cache
     const int T = (rows + kPromptTileRows - 1) / kPromptTileRows;
     const int S = 1 + T;
     std::vector<tf_stream> tiles_as_streams;
@@ -420,7 +431,7 @@ int tf_prompt_build(int32_t rows, int32_t keys, int32_t kv_capacity, const void*
         tiles_as_streams.push_back({r, t * kPromptTileRows, keys - rows + t * kPromptTileRows + r, kv_capacity});
     }
     tf_plan plan;
-    int rc = tf_segments_plan(tiles_as_streams.data(), T, &plan);   // the attention work
+    int rc = plan_windows(tiles_as_streams.data(), T, &plan, kPromptTileRows);   // the attention work
     if (rc != TF_OK) return rc;
     plan.n_streams = 1;
     plan.n_conv_tiles = (rows + kConvTileRows - 1) / kConvTileRows;

@@ -39,7 +39,10 @@ struct AttnItem {
 };
 
 constexpr int kConvTileRows = 8;
-constexpr int kPromptTileRows = 16;   // a prompt call's attention runs in windows of this many rows
+// A prompt call's attention runs in windows of this many rows: 32 rows x 4
+// query heads fill the 128 TMEM lanes of a tcgen05 tile (16-row tiles, those
+// of the per-stream kernels, fill half of it).
+constexpr int kPromptTileRows = TF_PROMPT_WINDOW_ROWS;
 
 // Device view of a segment table, passed to kernels by value.
 struct SegTable {

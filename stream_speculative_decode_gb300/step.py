@@ -51,8 +51,8 @@ class DeviceStep:
     def __init__(self, inp: StepInputs, device="cuda", keep_history=True, stream=None, fused_attention=True,
                  prompt=False):
         """``prompt``: one stream's prompt call (any number of rows; the table
-        from tf_prompt_build: conv over every row, attention in 16-row
-        windows; no history, no pick or accept)."""
+        from tf_prompt_build: conv over every row, attention in windows of
+        TF_PROMPT_WINDOW_ROWS rows; no history, no pick or accept)."""
         self.inp = inp
         self.prompt = prompt
         if prompt:

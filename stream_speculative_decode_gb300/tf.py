@@ -17,7 +17,10 @@ LIB_PATH = os.path.join(_HERE, "libtf.so")
 
 TF_H, TF_CIN, TF_KW, TF_NQ, TF_NKV, TF_D = 2048, 6144, 3, 32, 8, 64
 TF_MAX_ROWS = 16
+TF_MAX_KEYS = 1 << 22
+TF_MAX_STREAMS = 65536
 TF_MAX_PROMPT_ROWS = 65536
+TF_PROMPT_WINDOW_ROWS = 32
 TF_MK = 256
 TF_DFLAG_BAD_PENDING, TF_DFLAG_BAD_DRAFT = 1, 2
 TF_OK, TF_EINVAL, TF_ERANGE, TF_ENOMEM, TF_ECUDA = 0, 1, 2, 3, 4
@@ -203,7 +206,8 @@ def tf_prompt_build_status(rows, keys, kv_capacity, conv_state, k_cache, v_cache
 
 
 def tf_prompt_build(rows, keys, kv_capacity, conv_state, k_cache, v_cache, n_conv, n_attn, stream=None):
-    """A prompt (prefill) call's table: conv over every row, attention in 16-row windows."""
+    """A prompt (prefill) call's table: conv over every row, attention in
+    windows of TF_PROMPT_WINDOW_ROWS rows."""
     rc, handle = tf_prompt_build_status(rows, keys, kv_capacity, conv_state, k_cache, v_cache, n_conv, n_attn,
                                         stream)
     _check("tf_prompt_build", rc)

@@ -31,6 +31,17 @@ def test_exports_every_declared_symbol(T):
     assert set(names) == set(T.EXPORTS)
 
 
+def test_header_constants_match_binding(T):
+    """Every numeric #define of include/tf.h has the same value in the binding."""
+    text = open(os.path.join(ROOT, "include", "tf.h")).read()
+    defs = re.findall(r"^#define\s+(TF_[A-Z0-9_]+)\s+(\d+u?|\(\d+u? << \d+\))", text, flags=re.M)
+    assert len(defs) >= 15
+    for name, val in defs:
+        m = re.fullmatch(r"\(?(\d+)u?(?: << (\d+))?\)?", val)
+        value = int(m.group(1)) << int(m.group(2) or 0)
+        assert getattr(T, name) == value, name
+
+
 def test_strerror(T):
     for code in range(5):
         assert T.tf_strerror(code).startswith("TF_")

@@ -1,7 +1,7 @@
 """Prompt (prefill) calls through the C ABI against the oracle.
 
 A prompt call's table (tf_prompt_build) runs the conv over every row with the
-stream's state and the attention in 16-row windows over the one cache; the
+stream's state and the attention in 32-row windows over the one cache; the
 oracle replays the conv row by row and computes float64 causal attention of
 every row, whatever the windows.
 """
@@ -36,11 +36,13 @@ def _check_prompt(inp, res):
         check_attn(res["out"][l], ref, f"prompt attention layer {l}")
 
 
-@pytest.mark.parametrize("rows,cached", [(1, 0), (16, 5), (17, 40), (300, 1700), (41, 3000)])
+@pytest.mark.parametrize("rows,cached", [(1, 0), (16, 5), (17, 40), (32, 7), (45, 100), (300, 1700),
+                                         (41, 3000), (64, 8200)])
 def test_prompt_small(mods, rows, cached):
-    """Ragged last windows (1, 17, 41, 300 rows), a prompt that starts the
-    cache (no cached keys), windows on both kernels (16 rows: tensor cores;
-    the shorter last window: mma.sync)."""
+    """Ragged last windows (1, 16, 17, 13 of 45, 9 of 41, 12 of 300 rows), a
+    prompt that starts the cache (no cached keys), windows on both kernels
+    (13 rows and up: tensor cores; shorter: mma.sync), windows of two key
+    chunks (64 rows after 8,200 keys: 8,192-key chunks)."""
     tf, inputs, step, torch = mods
     w = inputs.prompt_workload(rows, cached, n_conv=2, n_attn=2, seed=rows + cached)
     inp = inputs.make_inputs(w, backend="numpy")
@@ -65,7 +67,7 @@ def test_prompt_forced_kernel(mods, path, monkeypatch):
 
 def test_prompt_two_call_and_static_forms(mods):
     """tf_attn_partials + tf_attn_merge and tf_attn_static on a prompt table,
-    with long windows (merge kernel: windows of 16 rows over 9,000 keys)."""
+    with windows of several key chunks (32 and 16 rows over 9,000 keys)."""
     tf, inputs, step, torch = mods
     w = inputs.prompt_workload(48, 9000, n_conv=0, n_attn=1, seed=4)
     inp = inputs.make_inputs(w, backend="numpy")
@@ -79,6 +81,19 @@ def test_prompt_two_call_and_static_forms(mods):
         tf.tf_attn_static(d.seg, 0, d.q[0], out)
         torch.cuda.synchronize()
         check_attn(out.cpu().numpy(), ref, "prompt, static scratch")
+    d.free()
+
+
+def test_prompt_merge_kernel(mods):
+    """Windows of 32 rows over more than 32,768 keys: five chunks or more,
+    past the last-CTA merge's 512 records, so the merge kernel finishes them."""
+    tf, inputs, step, torch = mods
+    w = inputs.prompt_workload(40, 36000, n_conv=0, n_attn=1, seed=7)
+    inp = inputs.make_inputs(w, backend="numpy")
+    d = step.DeviceStep(inp, prompt=True)
+    assert d.seg.plan["attn_merge_launch"] == 1
+    d.run()
+    _check_prompt(inp, d.results())
     d.free()
 
 
@@ -118,7 +133,7 @@ def test_prompt_full_size_sampled(mods):
     K = inputs.to_numpy_bits(inp.K[0][0])
     V = inputs.to_numpy_bits(inp.V[0][0])
     cached = 14336
-    for i in (0, 15, 16, 1000, 2047):
+    for i in (0, 15, 16, 31, 32, 1000, 2047):
         ref = O.attention_stream(q[i:i + 1], K, V, cached + i + 1, 1)
         check_attn(res["out"][0][i:i + 1], ref, f"prompt row {i}")
     d.free()
