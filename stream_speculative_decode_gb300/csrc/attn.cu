@@ -384,14 +384,18 @@ constexpr int kMergeSplit = 4;                       // warps per (row, query he
 constexpr int kMergeHeads = 2;                       // query heads per CTA
 constexpr int kMergeThreads = kMergeSplit * kMergeHeads * 32;
 constexpr int kMergeCtasPerRow = TF_NQ / kMergeHeads;
-constexpr int kMergeUnroll = 16;
+constexpr int kMergeLoads = 12;                      // 16-byte record loads in flight per lane
+constexpr int kMergeBatch = 2 * kMergeLoads;         // records per warp batch (a half-warp reads one)
 
 // kMergeSplit warps share one (row, query head): warp k takes the chunks
-// c = k, k + kMergeSplit, ...; lanes read those chunks' (m, l) in parallel,
-// then the o records kMergeUnroll at a time with independent loads (lane j
-// holding dimensions 2j and 2j+1). The warps' (M, L, o) are combined through
-// shared memory at the end.
-__global__ void __launch_bounds__(kMergeThreads)
+// c = k, k + kMergeSplit, ...; it reads them kMergeBatch at a time in one
+// round trip: lane j the (m, l) of the batch's chunk j, and each half-warp
+// every other chunk's o (lane holding dimensions 4*(lane%16) .. +3), all
+// loads issued before any is used. The batch's weights take a running max
+// (earlier batches rescaled when it grows). The warps' (M, L, o) are combined
+// through shared memory at the end. 3 CTAs per SM: the long-context
+// workload's 24 rows x 16 head pairs fit one wave.
+__global__ void __launch_bounds__(kMergeThreads, 3)
 attn_merge_kernel(SegTable t, const float* __restrict__ part_o, const float2* __restrict__ part_ml,
                   float* __restrict__ out, int kernel_mode_only) {
     const int row = blockIdx.x / kMergeCtasPerRow;
@@ -411,80 +415,88 @@ attn_merge_kernel(SegTable t, const float* __restrict__ part_o, const float2* __
     const int64_t base = st.pbase + int64_t(g) * nq + i * 4 + hh;
     const int C = st.n_chunks;
     const int nc = C > split ? (C - split + kMergeSplit - 1) / kMergeSplit : 0;   // this warp's chunks
+    const int half = lane >> 4, d4 = (lane & 15) * 4;
     pdl_wait();
 
     // chunk j of this warp is c = split + j * kMergeSplit
-    float M = -INFINITY;
-    for (int j = lane; j < nc; j += 32) {
-        const float2 ml = part_ml[base + int64_t(split + j * kMergeSplit) * stride];
-        if (ml.y > 0.f) M = fmaxf(M, ml.x);
-    }
+    float M = -INFINITY;                              // running max over the batches so far
+    float lsum = 0.f;                                 // this lane's share of the weight sum
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);     // dimensions d4.., chunks of parity `half`
+    for (int j0 = 0; j0 < nc; j0 += kMergeBatch) {
+        const int n = min(kMergeBatch, nc - j0);
+        float2 ml = make_float2(-INFINITY, 0.f);
+        if (lane < n) ml = part_ml[base + int64_t(split + (j0 + lane) * kMergeSplit) * stride];
+        float4 v[kMergeLoads];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
-
-    float2 acc = make_float2(0.f, 0.f);
-    float lsum = 0.f;
-    for (int j0 = 0; j0 < nc; j0 += 32) {
-        float wj = 0.f;
-        if (j0 + lane < nc) {
-            const float2 ml = part_ml[base + int64_t(split + (j0 + lane) * kMergeSplit) * stride];
-            if (ml.y > 0.f) {
-                wj = ex2(ml.x - M);
-                lsum += wj * ml.y;
-            }
+        for (int k = 0; k < kMergeLoads; ++k) {
+            const int j = 2 * k + half;
+            v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (j < n)
+                v[k] = *reinterpret_cast<const float4*>(
+                    part_o + (base + int64_t(split + (j0 + j) * kMergeSplit) * stride) * TF_D + d4);
         }
-        const int n = min(32, nc - j0);
-        for (int j = 0; j < n; j += kMergeUnroll) {
-            float2 v[kMergeUnroll];
-            float wk[kMergeUnroll];
+        float mb = ml.y > 0.f ? ml.x : -INFINITY;   // empty partials (l = 0) carry no weight
 #pragma unroll
-            for (int k = 0; k < kMergeUnroll; ++k) {
-                wk[k] = __shfl_sync(0xFFFFFFFFu, wj, (j + k) & 31);
-                v[k] = make_float2(0.f, 0.f);
-                if (j + k < n) {
-                    const int64_t rec = base + int64_t(split + (j0 + j + k) * kMergeSplit) * stride;
-                    v[k] = *reinterpret_cast<const float2*>(part_o + rec * TF_D + 2 * lane);
-                }
-            }
+        for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, o));
+        const float Mn = fmaxf(M, mb);
+        if (Mn == -INFINITY) continue;               // nothing visible yet (warp-uniform)
+        if (M != -INFINITY && Mn > M) {
+            const float f = ex2(M - Mn);
+            lsum *= f;
+            acc.x *= f;
+            acc.y *= f;
+            acc.z *= f;
+            acc.w *= f;
+        }
+        M = Mn;
+        const float wj = ml.y > 0.f ? ex2(ml.x - M) : 0.f;
+        lsum += wj * ml.y;
 #pragma unroll
-            for (int k = 0; k < kMergeUnroll; ++k) {
-                if (j + k < n) {
-                    acc.x += wk[k] * v[k].x;
-                    acc.y += wk[k] * v[k].y;
-                }
-            }
+        for (int k = 0; k < kMergeLoads; ++k) {
+            const float wk = __shfl_sync(0xFFFFFFFFu, wj, 2 * k + half);
+            acc.x += wk * v[k].x;
+            acc.y += wk * v[k].y;
+            acc.z += wk * v[k].z;
+            acc.w += wk * v[k].w;
         }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
+    acc.x += __shfl_xor_sync(0xFFFFFFFFu, acc.x, 16);   // the two halves' chunks
+    acc.y += __shfl_xor_sync(0xFFFFFFFFu, acc.y, 16);
+    acc.z += __shfl_xor_sync(0xFFFFFFFFu, acc.z, 16);
+    acc.w += __shfl_xor_sync(0xFFFFFFFFu, acc.w, 16);
     pdl_trigger();
 
     // combine the kMergeSplit warps of each head
     __shared__ float sM[kMergeHeads][kMergeSplit], sL[kMergeHeads][kMergeSplit];
-    __shared__ float2 sO[kMergeHeads][kMergeSplit][32];
+    __shared__ float4 sO[kMergeHeads][kMergeSplit][16];
     if (lane == 0) {
         sM[hl][split] = M;
         sL[hl][split] = lsum;
     }
-    sO[hl][split][lane] = acc;
+    if (lane < 16) sO[hl][split][lane] = acc;
     __syncthreads();
-    if (split == 0) {
+    if (split == 0 && lane < 16) {
         float Mt = -INFINITY;
 #pragma unroll
         for (int k = 0; k < kMergeSplit; ++k) Mt = fmaxf(Mt, sM[hl][k]);
         float L = 0.f;
-        float2 o2 = make_float2(0.f, 0.f);
+        float4 o4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < kMergeSplit; ++k) {
             if (sM[hl][k] == -INFINITY) continue;   // no visible key in this warp's chunks
             const float f = ex2(sM[hl][k] - Mt);
             L += f * sL[hl][k];
-            o2.x += f * sO[hl][k][lane].x;
-            o2.y += f * sO[hl][k][lane].y;
+            const float4 w4 = sO[hl][k][lane];
+            o4.x += f * w4.x;
+            o4.y += f * w4.y;
+            o4.z += f * w4.z;
+            o4.w += f * w4.w;
         }
         const float inv = 1.f / L;
-        *reinterpret_cast<float2*>(out + (size_t(row) * TF_NQ + h) * TF_D + 2 * lane) =
-            make_float2(o2.x * inv, o2.y * inv);
+        *reinterpret_cast<float4*>(out + (size_t(row) * TF_NQ + h) * TF_D + d4) =
+            make_float4(o4.x * inv, o4.y * inv, o4.z * inv, o4.w * inv);
     }
 }
 
