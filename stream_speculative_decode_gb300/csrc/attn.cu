@@ -8,13 +8,14 @@
 // scratch's attention partials hold each stream's apart). PR #1391: the
 // target's attention keeps its causal count.
 //
-// Partials kernel: one CTA per (work item = stream key chunk, KV head). The
-// chunk length depends on the stream alone (256 * rows keys), so a stream's
-// partials do not depend on the other streams of the round. The CTA streams
-// the chunk's K and V (64 keys a stage, 4-stage cp.async pipeline into
-// XOR-swizzled shared memory) once, for all 4*rows query rows of the KV head
-// (GQA: query head h reads KV head h/4) -- the whole window shares one read of
-// the cache. Four warps split each stage's keys (16 each); every warp keeps an
+// Partials kernel: one CTA per (work item = stream key chunk and group of at
+// most 8 window rows, KV head). The chunk length depends on the stream alone
+// (256 * rows keys), so a stream's partials do not depend on the other streams
+// of the round. The CTA streams the chunk's K and V (64 keys a stage, 4-stage
+// cp.async pipeline into XOR-swizzled shared memory) once, for the group's
+// query rows of the KV head (GQA: query head h reads KV head h/4) -- a window
+// of up to 8 rows shares one read of the cache; a wider one reads it once per
+// group, the later groups from L2. Four warps split each stage's keys (16 each); every warp keeps an
 // online softmax over its keys for all query rows; the warps are combined at
 // the end. q.k runs on bf16 tensor-core MMAs with fp32 accumulation (exact
 // products); P.V runs with P and V in fp16 (V's bf16 values convert exactly
@@ -93,10 +94,12 @@ __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) {
 __device__ __forceinline__ uint32_t swz(int r, int ch) { return uint32_t(r * kRowB + ((ch ^ (r & 7)) << 4)); }
 
 // One and two query m-tiles fit three CTAs per SM (<= 170 registers, 66 KB of
-// smem each; measured 12% faster on 6-row windows than two CTAs); three and
-// four m-tiles keep their registers (squeezed to three CTAs they spill).
+// smem each; measured 12% faster on 6-row windows than two CTAs). Wider
+// windows run as several items of at most two m-tiles: a third m-tile needs
+// 230 registers (two CTAs per SM), squeezed to three CTAs it spills, and
+// either way the whole launch ran slower.
 template <int MT>
-__global__ void __launch_bounds__(kThreads, MT <= 2 ? 3 : 1)
+__global__ void __launch_bounds__(kThreads, 3)
 attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
                      float* __restrict__ part_o, float2* __restrict__ part_ml, float* __restrict__ out,
                      int full) {
@@ -106,7 +109,9 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
     const int g = blockIdx.x % TF_NKV;
     const AttnItem item = t.items[item_idx];
     const SegStream st = t.streams[item.stream];
-    const int nq = st.rows * 4;
+    const int nq_all = st.rows * 4;
+    const int q0 = item.q0;                   // the group's first query row (a multiple of 32)
+    const int nq = min(16 * MT, nq_all - q0);   // the group's query rows
     const int c0 = item.chunk * st.chunk_keys;
     const int nkeys = min(st.chunk_keys, st.keys - c0);
     const int nst = (nkeys + kKT - 1) / kKT;
@@ -119,11 +124,13 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     pdl_wait();   // the table above; queries and caches below
 
-    // query rows qi = 4*i + hh (window row i, head 4g + hh); rows past nq are zero
+    // group query rows qi: q0 + qi = 4*i + hh (window row i, head 4g + hh);
+    // rows past nq are zero
     for (int idx = tid; idx < 16 * MT * 8; idx += kThreads) {
         const int qi = idx >> 3, ch = idx & 7;
         const bool valid = qi < nq;
-        const uint16_t* src = q + ((size_t(st.row_offset + (qi >> 2)) * TF_NQ + 4 * g + (qi & 3)) * TF_D + ch * 8);
+        const uint16_t* src =
+            q + ((size_t(st.row_offset + ((q0 + qi) >> 2)) * TF_NQ + 4 * g + (qi & 3)) * TF_D + ch * 8);
         cp_async16(sQ32 + swz(qi, ch), valid ? src : q, valid);
     }
     auto issue = [&](int s) {
@@ -149,9 +156,9 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
     float o[MT][8][4];
     float m[MT][2], l[MT][2], mtrue[MT][2];   // m: reference max; mtrue: running max
     int lim[MT][2];
-    // keys every real row sees (chunk-local): row 0's causal count, or every
-    // key for a FULL block
-    const int lim_all = (full ? st.keys : st.keys - st.rows + 1) - c0;
+    // keys every real row of the group sees (chunk-local): its first row's
+    // causal count, or every key for a FULL block
+    const int lim_all = (full ? st.keys : st.keys - st.rows + (q0 >> 2) + 1) - c0;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
 #pragma unroll
@@ -166,7 +173,7 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
             const int qi = mt * 16 + g8 + 8 * r;
             // chunk-local bound of the keys row qi/4 sees (causal, or all keys
             // for a FULL block), 0 for padding rows
-            const int vis = (full ? st.keys : st.keys - st.rows + (qi >> 2) + 1) - c0;
+            const int vis = (full ? st.keys : st.keys - st.rows + ((q0 + qi) >> 2) + 1) - c0;
             lim[mt][r] = qi < nq ? max(0, min(vis, nkeys)) : 0;
         }
     }
@@ -344,7 +351,7 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
     }
     __syncthreads();
     const int mode = out ? st.merge_mode : kMergeKernel;   // records only in the two-call form
-    const int64_t rec0 = st.pbase + (int64_t(item.chunk) * TF_NKV + g) * nq;
+    const int64_t rec0 = st.pbase + (int64_t(item.chunk) * TF_NKV + g) * nq_all + q0;
     for (int idx = tid; idx < nq * (TF_D / 4); idx += kThreads) {
         const int qi = idx >> 4, d4 = (idx & 15) * 4;
         float M = -INFINITY;
@@ -367,7 +374,7 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
         }
         if (mode == kMergeDirect) {   // the stream's only chunk: the output itself
             const float inv = 1.f / L;
-            *reinterpret_cast<float4*>(out_row(out, st, g, qi) + d4) =
+            *reinterpret_cast<float4*>(out_row(out, st, g, q0 + qi) + d4) =
                 make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
         } else {
             *reinterpret_cast<float4*>(part_o + (rec0 + qi) * TF_D + d4) = acc;
@@ -512,9 +519,7 @@ int prepare_one() {
 int attn_prepare() {
     int rc;
     if ((rc = prepare_one<1>()) != TF_OK) return rc;
-    if ((rc = prepare_one<2>()) != TF_OK) return rc;
-    if ((rc = prepare_one<3>()) != TF_OK) return rc;
-    return prepare_one<4>();
+    return prepare_one<2>();
 }
 
 // Launchers for other translation units: the partials and the merge of one
@@ -524,12 +529,12 @@ int launch_attn_partials(const SegTable& t, int layer, const uint16_t* q, float*
     if (t.n_items_mma > 0) {
         const dim3 grid(t.n_items_mma * TF_NKV);
         int rc;
-        switch (t.mma_mt) {
-            case 1: rc = launch_pdl(attn_partials_kernel<1>, grid, dim3(kThreads), smem_bytes(1), stream, t, layer, q, po, pml, out, full); break;
-            case 2: rc = launch_pdl(attn_partials_kernel<2>, grid, dim3(kThreads), smem_bytes(2), stream, t, layer, q, po, pml, out, full); break;
-            case 3: rc = launch_pdl(attn_partials_kernel<3>, grid, dim3(kThreads), smem_bytes(3), stream, t, layer, q, po, pml, out, full); break;
-            default: rc = launch_pdl(attn_partials_kernel<4>, grid, dim3(kThreads), smem_bytes(4), stream, t, layer, q, po, pml, out, full); break;
-        }
+        if (t.mma_mt == 1)
+            rc = launch_pdl(attn_partials_kernel<1>, grid, dim3(kThreads), smem_bytes(1), stream, t, layer, q, po, pml,
+                            out, full);
+        else
+            rc = launch_pdl(attn_partials_kernel<2>, grid, dim3(kThreads), smem_bytes(2), stream, t, layer, q, po, pml,
+                            out, full);
         if (rc != TF_OK) return rc;
     }
     if (t.n_items_mma < t.n_items) return launch_attn_partials_tc(t, layer, q, po, pml, stream, out, full);

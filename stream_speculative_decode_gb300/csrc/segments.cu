@@ -176,6 +176,20 @@ int finish_build(tf_segments* seg, std::vector<tf::SegStream>& ss, std::vector<i
     const int R = int(row_stream.size());
     const tf_plan& plan = seg->plan;
     int rc = TF_OK;
+    // mma.sync streams wider than kMmaGroupRows rows: one item per group of
+    // rows and chunk, the groups of a chunk next to each other
+    {
+        std::vector<AttnItem> groups;
+        groups.reserve(items.size());
+        for (SegStream& d : ss) d.n_qg = 1;
+        for (const AttnItem& it : items) {
+            SegStream& d = ss[it.stream];
+            const int ng = attn_path_of(d.rows) == kAttnMma ? (d.rows + kMmaGroupRows - 1) / kMmaGroupRows : 1;
+            d.n_qg = ng;
+            for (int gi = 0; gi < ng; ++gi) groups.push_back({it.stream, it.chunk, 4 * kMmaGroupRows * gi, 0});
+        }
+        items.swap(groups);
+    }
     // mma.sync items first, then tensor-core items; within each, largest
     // chunks first so the long work starts early in the grid
     std::stable_sort(items.begin(), items.end(), [&](const AttnItem& a, const AttnItem& b) {
@@ -193,7 +207,7 @@ int finish_build(tf_segments* seg, std::vector<tf::SegStream>& ss, std::vector<i
     for (const AttnItem& it : items)
         if (attn_path_of(ss[it.stream].rows) == kAttnMma) {
             ++n_items_mma;
-            mma_rows = std::max(mma_rows, ss[it.stream].rows);
+            mma_rows = std::max(mma_rows, std::min(ss[it.stream].rows - it.q0 / 4, kMmaGroupRows));
         }
 
     size_t off = 0;
@@ -382,11 +396,11 @@ int tf_segments_build(const tf_stream* streams, int n_streams,
         pbase += int64_t(st.rows) * TF_NQ * d.n_chunks;
         d.merge_mode = d.n_chunks == 1 ? kMergeDirect
                      : (4 * st.rows * d.n_chunks <= kMergeLastCtaMaxRecords ? kMergeLastCta : kMergeKernel);
-        d.pad_ = 0;
+        d.n_qg = 1;
         for (int i = 0; i < st.rows; ++i) row_stream[st.row_offset + i] = s;
         for (int r0 = 0; r0 < st.rows; r0 += kConvTileRows)
             tiles.push_back({s, r0, std::min(kConvTileRows, st.rows - r0), 0});
-        for (int c = 0; c < d.n_chunks; ++c) items.push_back({s, c});
+        for (int c = 0; c < d.n_chunks; ++c) items.push_back({s, c, 0, 0});
     }
     return finish_build(seg, ss, row_stream, tiles, items, conv_state, conv_hist, k_cache, v_cache, n_conv, n_attn,
                         stream, out);
@@ -444,7 +458,7 @@ int tf_prompt_build(int32_t rows, int32_t keys, int32_t kv_capacity, const void*
     std::vector<int32_t> row_stream(rows);
     std::vector<ConvTile> tiles;
     std::vector<AttnItem> items;
-    ss[0] = {rows, 0, keys, kv_capacity, 0, 0, 0, kMergeDirect, 0};
+    ss[0] = {rows, 0, keys, kv_capacity, 0, 0, 0, kMergeDirect, 1};
     for (int r0 = 0; r0 < rows; r0 += kConvTileRows) tiles.push_back({0, r0, std::min(kConvTileRows, rows - r0), 0});
     int64_t pbase = 0;
     for (int t = 0; t < T; ++t) {
@@ -460,9 +474,9 @@ int tf_prompt_build(int32_t rows, int32_t keys, int32_t kv_capacity, const void*
         pbase += int64_t(st.rows) * TF_NQ * d.n_chunks;
         d.merge_mode = d.n_chunks == 1 ? kMergeDirect
                      : (4 * st.rows * d.n_chunks <= kMergeLastCtaMaxRecords ? kMergeLastCta : kMergeKernel);
-        d.pad_ = 0;
+        d.n_qg = 1;
         for (int i = 0; i < st.rows; ++i) row_stream[st.row_offset + i] = 1 + t;
-        for (int c = 0; c < d.n_chunks; ++c) items.push_back({1 + t, c});
+        for (int c = 0; c < d.n_chunks; ++c) items.push_back({1 + t, c, 0, 0});
     }
     // pointer arrays [layer][S]: every stream of a layer names the layer's
     // state and caches (the conv reaches them through stream 0 only)

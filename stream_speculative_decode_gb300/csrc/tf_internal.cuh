@@ -19,7 +19,7 @@ struct SegStream {
     int32_t chunk_keys, n_chunks;
     int64_t pbase;            // first partial record of the stream
     int32_t merge_mode;       // in one-call attention: kMergeDirect / kMergeLastCta / kMergeKernel
-    int32_t pad_;
+    int32_t n_qg;             // query groups: items per key chunk (mma.sync path: one per 8 window rows)
 };
 
 // How the one-call attention (tf_attn) finishes a stream's chunks.
@@ -33,10 +33,19 @@ struct ConvTile {
     int32_t stream, row0, nrows, pad;
 };
 
-// An attention work item: one key chunk of one stream (for every KV head).
+// An attention work item: one key chunk of one stream (for every KV head) and,
+// on the mma.sync path, one group of at most kMmaGroupRows window rows: query
+// rows [q0, q0 + 4*kMmaGroupRows) of the KV head (q0 = 0 on the tensor-core
+// path, which takes the whole window).
 struct AttnItem {
-    int32_t stream, chunk;
+    int32_t stream, chunk, q0, pad;
 };
+
+// Window rows of one mma.sync item: two 16-row query m-tiles, the most that
+// keep three CTAs per SM. Wider windows run as several items over the same
+// chunk, next to each other in the grid (the second read of the chunk comes
+// from L2).
+constexpr int kMmaGroupRows = 8;
 
 constexpr int kConvTileRows = 8;
 // A prompt call's attention runs in windows of this many rows: 32 rows x 4
@@ -59,7 +68,7 @@ struct SegTable {
     int32_t S, R, n_tiles, n_items, n_conv, n_attn, max_rows, has_hist;
     int32_t n_items_mma;              // items [0, n_items_mma) run on the mma.sync kernel,
                                       // [n_items_mma, n_items) on the tcgen05 kernel
-    int32_t mma_mt;                   // 16-row query tiles of the mma.sync kernel's widest stream
+    int32_t mma_mt;                   // 16-row query tiles of the mma.sync kernel's widest item (1 or 2)
     int64_t n_partials;
     int32_t* counters;                // [n_attn][S][8] arrivals per (stream, KV head), self-resetting
     int32_t n_merge_rows;             // rows of kMergeKernel streams
@@ -240,7 +249,7 @@ __device__ __forceinline__ void finish_last_cta(const SegTable& t, int layer, in
     __threadfence();
     __syncthreads();
     int* ctr = t.counters + (size_t(layer) * t.S + s) * TF_NKV + g;
-    if (threadIdx.x == 0) *smem_flag = (atomicAdd(ctr, 1) == st.n_chunks - 1);
+    if (threadIdx.x == 0) *smem_flag = (atomicAdd(ctr, 1) == st.n_chunks * st.n_qg - 1);
     __syncthreads();
     if (*smem_flag) {
         __threadfence();
