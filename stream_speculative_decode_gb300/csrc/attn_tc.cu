@@ -123,7 +123,10 @@ __device__ __forceinline__ Unit unit_of(const SegTable& t, int layer, int u) {
 }
 
 // State of one softmax thread for one unit: query row qi = per*(lane quadrant)
-// + lane sits on TMEM lane quadrant*32 + lane (lanes past `per` hold zero rows).
+// + lane sits on TMEM lane quadrant*32 + lane (lanes past `per` hold zero
+// rows). Windows of at most 16 rows (per <= 16) run dual: lanes L and L + 16
+// of a quadrant hold the same query, lane L scoring keys 0-31 of each tile
+// and lane L + 16 keys 32-63, so every lane does useful softmax work.
 struct SoftState {
     Bars* bars;
     volatile uint32_t* abortp;
@@ -135,9 +138,14 @@ struct SoftState {
     float l;             // sum of 2^(s*log2e/8 - mref) over the keys so far
 };
 
-template <int KC>
+// DUAL: this thread owns half of each tile's keys (the other half of its
+// lane's row is written as P = 0, so P.V sums over its half only); the row's
+// max is shared with the partner lane (lane ^ 16) so both use one reference.
+template <int KC, bool DUAL>
 __device__ __forceinline__ void softmax_tiles(SoftState& st) {
     const int lane = threadIdx.x & 31;
+    const int half = DUAL ? (lane >> 4) : 0;
+    constexpr int NV = DUAL ? KC / 2 : KC;   // scores this thread owns per tile
     Bars* bars = st.bars;
     for (int j = 0; j < st.T; ++j) {
         const int gj = st.g0 + j;
@@ -146,18 +154,18 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
         if (!mbar_wait(su32(&bars->s_full[b]), (gj / kSBuf) & 1, st.abortp)) break;
         tc_fence_after();
         if (st.wact) {
-            const int k0 = j * kKT;                  // chunk-local first key of the tile
-            float v[KC];
+            const int k0 = j * kKT + half * NV;      // chunk-local key of v[0]
+            float v[NV];
             {
                 uint32_t r[KC];
                 tc_ld_n<KC>(st.trow + colS, r);
                 tc_wait_ld();
 #pragma unroll
-                for (int c = 0; c < KC; ++c) v[c] = __uint_as_float(r[c]);
+                for (int c = 0; c < NV; ++c) v[c] = __uint_as_float(half ? r[NV + c] : r[c]);
             }
             if (j * kKT + kKT > st.lim_all) {   // the causal edge or the chunk's end lies in this tile
 #pragma unroll
-                for (int c = 0; c < KC; ++c)
+                for (int c = 0; c < NV; ++c)
                     if (k0 + c >= st.lim) v[c] = -INFINITY;
             }
             float m8[8];
@@ -165,10 +173,11 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
             for (int a = 0; a < 8; ++a) {
                 m8[a] = v[a];
 #pragma unroll
-                for (int c = a + 8; c < KC; c += 8) m8[a] = fmaxf(m8[a], v[c]);
+                for (int c = a + 8; c < NV; c += 8) m8[a] = fmaxf(m8[a], v[c]);
             }
-            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            if (DUAL) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));   // the row's two halves
             const float mxs = mx * kLog2e8;
             st.mtrue = fmaxf(st.mtrue, mxs);
             const bool resc = mxs > st.mref + kTau;
@@ -201,16 +210,26 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
                 }
             }
             const float mu = (st.mref == -INFINITY) ? 0.f : st.mref;
-            uint32_t own[KC / 2];
+            uint32_t own[NV / 2];
             float s4[4] = {0.f, 0.f, 0.f, 0.f};   // four independent sums
 #pragma unroll
-            for (int c = 0; c < KC / 2; ++c) {
+            for (int c = 0; c < NV / 2; ++c) {
                 const float p0 = ex2(fmaf(v[2 * c], kLog2e8, -mu));
                 const float p1 = ex2(fmaf(v[2 * c + 1], kLog2e8, -mu));
                 s4[c & 3] += p0 + p1;
                 own[c] = pack_h2(p0, p1);
             }
-            tc_st_n<KC / 2>(st.trow + colS, own);   // P (fp16 pairs) over the first KC/2 columns of S
+            if constexpr (DUAL) {   // this half's P and zeros for the partner's half
+                uint32_t w[KC / 2];
+#pragma unroll
+                for (int c = 0; c < NV / 2; ++c) {
+                    w[c] = half ? 0u : own[c];
+                    w[NV / 2 + c] = half ? own[c] : 0u;
+                }
+                tc_st_n<KC / 2>(st.trow + colS, w);   // P (fp16 pairs) over the first KC/2 columns of S
+            } else {
+                tc_st_n<KC / 2>(st.trow + colS, own);
+            }
             st.l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
             tc_wait_st();
         }
@@ -249,13 +268,15 @@ __device__ __forceinline__ bool group_sync(Bars* bars, int& ph, volatile uint32_
 }
 
 // The unit's queries into shared memory (cp.async, zero rows past 4*rows),
-// swizzled K-major: lane L holds query qi = per*(L/32) + L%32 when L%32 < per.
+// swizzled K-major: lane L holds query qi = per*(L/32) + L%32 when L%32 < per
+// (dual, per <= 16: qi = per*(L/32) + L%16 when L%16 < per).
 __device__ __forceinline__ void load_q_async(uint32_t sQ, const uint16_t* q, const Unit& U, int tid) {
     const int nq = U.st.rows * 4, per = (nq + 3) / 4;
+    const int lmask = per <= 16 ? 15 : 31;
     for (int idx = tid; idx < kQRows * 8; idx += 128) {
         const int L = idx >> 3, ch = idx & 7;
-        const int qq = per * (L >> 5) + (L & 31);
-        const bool valid = (L & 31) < per && qq < nq;
+        const int qq = per * (L >> 5) + (L & lmask);
+        const bool valid = (L & lmask) < per && qq < nq;
         const uint16_t* src = q + ((size_t(U.st.row_offset + (qq >> 2)) * TF_NQ + 4 * U.g + (qq & 3)) * TF_D + ch * 8);
         cp_async16(sQ + L * 128 + ((ch ^ (L & 7)) << 4), valid ? src : q, valid);
     }
@@ -447,8 +468,11 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
             const Unit U = unit_of(t, layer, u);
             const SegStream& st = U.st;
             const int nq = st.rows * 4, per = (nq + 3) / 4;
-            const int qi = per * warp + lane;
-            const bool qvalid = lane < per && qi < nq;
+            const bool dual = per <= 16;
+            const int ql = dual ? (lane & 15) : lane;   // the lane's query within the quadrant
+            const int qi = per * warp + ql;
+            const bool qvalid = ql < per && qi < nq;
+            const bool owner = qvalid && (!dual || lane < 16);   // writes the row's record
             const bool wact = per * warp < nq;      // the warp holds at least one real row
             const int mode = out ? st.merge_mode : kMergeKernel;   // records only in the two-call form
             SoftState ss;
@@ -465,7 +489,10 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
             ss.mref = -INFINITY;
             ss.mtrue = -INFINITY;
             ss.l = 0.f;
-            softmax_tiles<kKT>(ss);
+            if (dual)
+                softmax_tiles<kKT, true>(ss);
+            else
+                softmax_tiles<kKT, false>(ss);
             gt += U.T;
             // every q.K of this unit is done (the softmax read each S): the next
             // unit's queries may overwrite the buffer while this one finishes
@@ -481,8 +508,15 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                 uint32_t ro[64];
                 tc_ld64(trow + kColO, ro);
                 tc_wait_ld();
-                const float lsum = ss.l;
-                if (qvalid && mode == kMergeDirect) {   // the stream's only chunk: the output itself
+                float lsum = ss.l;
+                if (dual) {   // the row's two halves (lanes L and L + 16)
+#pragma unroll
+                    for (int c = 0; c < 64; ++c)
+                        ro[c] = __float_as_uint(__uint_as_float(ro[c]) +
+                                                __uint_as_float(__shfl_xor_sync(0xFFFFFFFFu, ro[c], 16)));
+                    lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 16);
+                }
+                if (owner && mode == kMergeDirect) {   // the stream's only chunk: the output itself
                     const float inv = aborted ? NAN : 1.f / lsum;   // a row always sees key 0 of its stream
                     float4* dst = reinterpret_cast<float4*>(out_row(out, st, U.g, qi));
 #pragma unroll
@@ -490,7 +524,7 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                         dst[c] = make_float4(__uint_as_float(ro[4 * c]) * inv, __uint_as_float(ro[4 * c + 1]) * inv,
                                              __uint_as_float(ro[4 * c + 2]) * inv,
                                              __uint_as_float(ro[4 * c + 3]) * inv);
-                } else if (qvalid) {
+                } else if (owner) {
                     const int64_t rec = st.pbase + (int64_t(U.chunk) * TF_NKV + U.g) * nq + qi;
                     const bool empty = ss.mtrue == -INFINITY;
                     float4* dst = reinterpret_cast<float4*>(part_o + rec * TF_D);
