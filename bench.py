@@ -42,6 +42,26 @@ UNIT = "rows/s"
 L2_FLUSH_BYTES = 256 << 20      # > 129 MB L2
 
 
+class L2Flush:
+    """Evicts the step's data from L2 between timed steps (outside the events):
+    256 MB written; with mode "clean" (the default) a second 256 MB buffer is
+    then read, so the dirty lines of the write are written back before the
+    timed region instead of inside it."""
+
+    def __init__(self, torch, dev, mode):
+        self.mode = mode
+        self.wbuf = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+        self.rbuf = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev) if mode == "clean" else None
+        self.desc = ("flushed: 256 MB written, then 256 MB of another buffer read, between timed steps, "
+                     "outside the events" if mode == "clean"
+                     else "flushed: 256 MB written between timed steps, outside the events")
+
+    def __call__(self):
+        self.wbuf.zero_()
+        if self.rbuf is not None:
+            self.rbuf.max()
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -53,6 +73,9 @@ def parse():
     ap.add_argument("--prompt-rows", type=int, default=2048, help="--row prompt: rows of the prompt chunk")
     ap.add_argument("--prompt-cached", type=int, default=14336, help="--row prompt: keys cached before it")
     ap.add_argument("--impl", default="tf", choices=["tf", "reference"])
+    ap.add_argument("--flush", default="clean", choices=["clean", "write"],
+                    help="L2 flush between timed steps: write 256 MB then read another 256 MB (clean), "
+                         "or only write (leaves the write's dirty lines to the timed step)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--conv-layers", type=int, default=None, help="override (small profiling runs)")
@@ -341,13 +364,13 @@ def run_tf(args, rank, world):
     # attention call, replayed in a loop of its own
     g_ev = d.capture(events=evs) if graph_events else None
     d.capture()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev, args.flush)
     stream = torch.cuda.current_stream(dev)
 
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         d.graph.replay()
     torch.cuda.synchronize()
 
@@ -357,7 +380,7 @@ def run_tf(args, rank, world):
     torch.cuda.synchronize()
     t_wall0 = time.time()
     for k in range(args.steps):
-        flush.zero_()                       # L2 flushed between timed steps (outside the events)
+        flush()                       # L2 flushed between timed steps (outside the events)
         ev[k][0].record(stream)
         d.graph.replay()
         ev[k][1].record(stream)
@@ -367,7 +390,7 @@ def run_tf(args, rank, world):
     step_ms = [a.elapsed_time(b) for a, b in ev]
     if graph_events:                        # the attention calls, timed inside the step
         for _ in range(args.steps):
-            flush.zero_()
+            flush()
             g_ev.replay()
             torch.cuda.synchronize()
             part_ms.extend(a.elapsed_time(b) for a, b in evs["attn"])
@@ -379,7 +402,7 @@ def run_tf(args, rank, world):
         # no event nodes in graphs on this PyTorch: time eager launches of the same kernel
         for _ in range(min(args.steps, 20)):
             for l in range(w.n_attn):
-                flush.zero_()
+                flush()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(stream)
                 d.attn(l)
@@ -412,7 +435,7 @@ def run_tf(args, rank, world):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(workload_config(w), l2="flushed: 256 MB written between timed steps, outside the events",
+        "config": dict(workload_config(w), l2=flush.desc,
                        graph="one CUDA graph per step", parallelism=f"replicas x{world}"),
         "hbm": {"step_algorithmic_bytes": ab["total"], "achieved_gbs": step_gbs, "peak_gbs": peak,
                 "frac": step_gbs / peak, "peak_kind": peak_kind},
@@ -465,7 +488,7 @@ def run_e2e(d, args, stream, flush):
     torch.cuda.synchronize()
     ts = []
     for _ in range(steps):
-        flush.zero_()
+        flush()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         one()
@@ -563,11 +586,11 @@ def run_row(args, rank, world):
     cap = torch.cuda.Stream(dev)
     with torch.cuda.graph(g, stream=cap):
         call(cap)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev, args.flush)
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         g.replay()
     torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
@@ -575,7 +598,7 @@ def run_row(args, rank, world):
     torch.cuda.synchronize()
     t0 = time.time()
     for k in range(args.steps):
-        flush.zero_()
+        flush()
         ev[k][0].record(stream)
         g.replay()
         ev[k][1].record(stream)
@@ -600,7 +623,7 @@ def run_row(args, rank, world):
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(workload_config(w), row=args.row,
-                       l2="flushed: 256 MB written between timed steps, outside the events",
+                       l2=flush.desc,
                        graph="one CUDA graph per step", parallelism=f"replicas x{world}", **extra),
         "roofline": {"kernel": kname, "bound": roof["bound"], "achieved": achieved, "peak": roof["peak"],
                      "unit": roof["unit"], "frac": achieved / roof["peak"], "traffic": None,
