@@ -394,6 +394,29 @@ def run_tf(args, rank, world):
             g_ev.replay()
             torch.cuda.synchronize()
             part_ms.extend(a.elapsed_time(b) for a, b in evs["attn"])
+    # the same attention calls back to back (a graph of the step's attention
+    # layers alone, no event between them): the call's duration when the
+    # launches overlap as they do in the step
+    b2b_ms = None
+    if w.n_attn > 0:
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(stream)
+        g_b2b = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cap):
+            with torch.cuda.graph(g_b2b, stream=cap):
+                for l in range(w.n_attn):
+                    d.attn(l, torch.cuda.current_stream(dev))
+        stream.wait_stream(cap)
+        ts = []
+        for _ in range(min(args.steps, 50)):
+            flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g_b2b.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b) / w.n_attn)
+        b2b_ms = statistics.median(ts)
     clocks_sum = clocks.summary(t_wall0, t_wall1)
     ms = sum(step_ms) / len(step_ms)
     value, ms_max = aggregate(R, ms, world, device=dev)
@@ -445,6 +468,11 @@ def run_tf(args, rank, world):
                      "algorithmic_bytes_per_launch": attn_alg, "avg_launch_ms": part_avg_ms,
                      "launches_per_call": d.seg.plan["attn_kernels"] + d.seg.plan["attn_merge_launch"],
                      "launches_timed": len(part_ms), "peak_kind": peak_kind,
+                     "back_to_back": None if b2b_ms is None else
+                     {"avg_call_ms": b2b_ms, "achieved": attn_alg / (b2b_ms * 1e-3) / 1e9,
+                      "frac": attn_alg / (b2b_ms * 1e-3) / 1e9 / peak,
+                      "timing": "median over replays of a graph of the step's attention calls alone, L2 flushed "
+                                "between replays, one event pair per replay"},
                      "timing": "CUDA events around each attention call inside a copy of the step graph, "
                                "replayed K times after the timed region (the timed graph has no event nodes)"
                      if graph_events else "CUDA events around eager launches after the timed region"},

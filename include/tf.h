@@ -107,9 +107,10 @@ typedef struct {
 typedef struct tf_segments tf_segments;
 
 /* Split-K chunk of a stream: keys [c*chunk, (c+1)*chunk). The chunk length is
- * 256 * max(rows, 4) keys (partial records stay near 1/64 of the K/V bytes);
- * it depends on the stream alone, so a stream's results do not depend on
- * which other streams share the round. */
+ * 256 * max(rows, 4) keys (partial records stay near 1/64 of the K/V bytes),
+ * and 512 * rows for windows of 13 to 16 rows (the tensor-core kernel: fewer,
+ * longer units measured faster there); it depends on the stream alone, so a
+ * stream's results do not depend on which other streams share the round. */
 int32_t tf_chunk_keys(int32_t rows);
 
 /* Validate `streams` and compute the table's sizes. Host only; touches no GPU.

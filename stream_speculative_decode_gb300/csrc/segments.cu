@@ -318,7 +318,10 @@ int finish_build(tf_segments* seg, std::vector<tf::SegStream>& ss, std::vector<i
 
 extern "C" {
 
-int32_t tf_chunk_keys(int32_t rows) { return 256 * (rows < 4 ? 4 : rows); }
+int32_t tf_chunk_keys(int32_t rows) {
+    if (rows >= 13 && rows <= TF_MAX_ROWS) return 512 * rows;   // verify windows on the tensor-core kernel
+    return 256 * (rows < 4 ? 4 : rows);
+}
 
 int tf_segments_plan(const tf_stream* streams, int n_streams, tf_plan* out) {
     return tf::plan_windows(streams, n_streams, out, TF_MAX_ROWS);

@@ -48,16 +48,21 @@ def test_strerror(T):
     assert "unknown" in T.tf_strerror(99)
 
 
+def _chunk(rows):
+    """The documented chunk rule."""
+    return 512 * rows if 13 <= rows <= 16 else 256 * max(rows, 4)
+
+
 def test_chunk_rule(T):
-    for r in range(1, 17):
-        assert T.tf_chunk_keys(r) == 256 * max(r, 4)
+    for r in range(1, 33):
+        assert T.tf_chunk_keys(r) == _chunk(r)
 
 
 def _plan_expect(streams):
     """The partial count from the documented rule: rows * 32 * chunks."""
     n = 0
     for rows, _, keys, _ in streams:
-        chunk = 256 * max(rows, 4)
+        chunk = _chunk(rows)
         n += rows * 32 * (-(-keys // chunk))
     return n
 

@@ -71,7 +71,7 @@ def test_static_scratch_refuses_oversized_table(mods):
     """A table whose partials exceed the fixed array is refused with TF_ERANGE
     before anything is launched."""
     tf, inputs, step, torch = mods
-    rows, keys = 16, 520_000  # one 16-row stream: 127 chunks of 4,096 keys -> 17.2 MB of partials
+    rows, keys = 12, 520_000  # one 12-row stream: 170 chunks of 3,072 keys -> 17.2 MB of partials
     cap = inputs.kv_capacity(keys)
     K = torch.zeros((8, cap, 64), dtype=torch.bfloat16, device="cuda")
     V = torch.zeros((8, cap, 64), dtype=torch.bfloat16, device="cuda")
