@@ -5,13 +5,17 @@
 // over every row from the segment table, each row's arithmetic that of the
 // per-stream conv; streams longer than 8 rows are folded into 8-row tiles.
 //
-// Work split: a CTA of 64 threads owns one 8-row tile of one stream and 512
-// channels; a thread owns 8 consecutive channels (16-byte loads of B, C, x and
-// of the 3 taps) and walks the tile's rows in order. The two rows before a
-// tile come from the conv state (first tile) or are recomputed from the
-// input rows (later tiles), so tiles are independent. Only the first tile of a
-// stream reads the state and only it writes the new state, so the in-place
-// update needs no ordering between CTAs.
+// Work split: a CTA owns one 8-row tile of one stream and 512 channels; its
+// 256 threads are 64 channel groups (8 consecutive channels, 16-byte loads of
+// B, C, x and the 3 taps) x 4 row slots, slot k taking the tile's rows k and
+// k + 4. Every thread loads its rows at once, gates them (bx = B*x) into
+// shared memory, and after one barrier convolves each row with the two
+// entries before it, so the rows of a tile run in parallel rather than one
+// after the other. The two entries before a tile come from the conv state
+// (first tile) or are recomputed from the input rows (later tiles), so tiles
+// are independent. Only the first tile of a stream reads the state (rows 0
+// and 1, before the barrier) and writes the new state (after it), so the
+// in-place update needs no ordering between CTAs.
 //
 // HBM bound: per row 6144*2 B read + 2048*4 B written (+ state/history).
 #include "tf_internal.cuh"
@@ -19,9 +23,11 @@
 namespace tf {
 namespace {
 
-constexpr int kThreads = 64;
-constexpr int kChan = 8;                       // channels per thread
-constexpr int kChanPerCta = kThreads * kChan;  // 512
+constexpr int kGroups = 64;                     // channel groups per CTA
+constexpr int kChan = 8;                        // channels per group
+constexpr int kChanPerCta = kGroups * kChan;    // 512
+constexpr int kSlots = kConvTileRows / 2;       // row slots: rows k and k + kSlots
+constexpr int kThreads = kGroups * kSlots;      // 256
 
 __device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -47,106 +53,127 @@ __device__ __forceinline__ uint4 gate8(const uint4& b, const uint4& x) {
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-__global__ void __launch_bounds__(kThreads)
+// bf16 element e (0..23) of the three packed tap vectors, as fp32
+__device__ __forceinline__ float tap(const uint4 (&w)[3], int e) {
+    const uint4& v = w[e >> 3];
+    const int k = e & 7;
+    const uint32_t word = (k >> 1) == 0 ? v.x : (k >> 1) == 1 ? v.y : (k >> 1) == 2 ? v.z : v.w;
+    return __uint_as_float((k & 1) ? (word & 0xFFFF0000u) : (word << 16));
+}
+
+// y = C * (w0*e0 + w1*e1 + w2*bx) for 8 channels (entries oldest first), fp32
+__device__ __forceinline__ void conv8(const uint4 (&w)[3], const uint4& e0, const uint4& e1, const uint4& bx,
+                                      const uint4& cg, float o[8]) {
+    float f0[8], f1[8], f2[8], fc[8];
+    unpack8(e0, f0);
+    unpack8(e1, f1);
+    unpack8(bx, f2);
+    unpack8(cg, fc);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {   // taps of channel k: elements 3k, 3k+1, 3k+2
+        float conv = tap(w, 3 * k) * f0[k];
+        conv = fmaf(tap(w, 3 * k + 1), f1[k], conv);
+        conv = fmaf(tap(w, 3 * k + 2), f2[k], conv);
+        o[k] = fc[k] * conv;
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 4)
 conv_rows_kernel(SegTable t, int layer, const uint16_t* __restrict__ bcx,
                  const uint16_t* __restrict__ w, float* __restrict__ y) {
+    __shared__ uint4 sbx[kConvTileRows][kGroups];   // the tile's gated entries (8 KB)
     const ConvTile tile = t.tiles[blockIdx.x];
     const SegStream st = t.streams[tile.stream];
-    const int c = blockIdx.y * kChanPerCta + threadIdx.x * kChan;
-    const size_t slot = size_t(layer) * t.S + tile.stream;
-    uint16_t* state = static_cast<uint16_t*>(t.conv_state[slot]);
-    uint16_t* hist = t.has_hist ? static_cast<uint16_t*>(t.conv_hist[slot]) : nullptr;
+    const int grp = threadIdx.x % kGroups, slot = threadIdx.x / kGroups;
+    const int c = blockIdx.y * kChanPerCta + grp * kChan;
+    const size_t sl = size_t(layer) * t.S + tile.stream;
+    uint16_t* state = static_cast<uint16_t*>(t.conv_state[sl]);
+    uint16_t* hist = t.has_hist ? static_cast<uint16_t*>(t.conv_hist[sl]) : nullptr;
     const int n = tile.nrows;
     const int row_base = st.row_offset + tile.row0;
+    const bool first = tile.row0 == 0;
     pdl_wait();   // the table above; the data below may come from the previous kernel
 
-    // taps of channels c..c+7: 24 bf16, element (channel j, tap k) at 3*j+k
-    float wt[24];
-    {
-        const uint4* wp = reinterpret_cast<const uint4*>(w + size_t(c) * 3);
-        float a[8], b[8], d[8];
-        unpack8(__ldg(wp + 0), a);
-        unpack8(__ldg(wp + 1), b);
-        unpack8(__ldg(wp + 2), d);
+    // this thread's rows slot and slot + kSlots (loads issued before any arithmetic)
+    uint4 B[2], C[2], X[2];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            wt[k] = a[k];
-            wt[8 + k] = b[k];
-            wt[16 + k] = d[k];
-        }
-    }
-
-    // the window rows of this tile (loads issued before any arithmetic)
-    uint4 B[kConvTileRows], C[kConvTileRows], X[kConvTileRows];
-#pragma unroll
-    for (int j = 0; j < kConvTileRows; ++j) {
+    for (int k = 0; k < 2; ++k) {
+        const int j = slot + k * kSlots;
         if (j < n) {
             const uint16_t* row = bcx + size_t(row_base + j) * TF_CIN + c;
-            B[j] = __ldcs(reinterpret_cast<const uint4*>(row));
-            C[j] = __ldcs(reinterpret_cast<const uint4*>(row + TF_H));
-            X[j] = __ldcs(reinterpret_cast<const uint4*>(row + 2 * TF_H));
+            B[k] = __ldcs(reinterpret_cast<const uint4*>(row));
+            C[k] = __ldcs(reinterpret_cast<const uint4*>(row + TF_H));
+            X[k] = __ldcs(reinterpret_cast<const uint4*>(row + 2 * TF_H));
         }
     }
-
-    // the two sequence entries before the tile
-    uint4 s0, s1;
-    if (tile.row0 == 0) {
-        s0 = *reinterpret_cast<const uint4*>(state + c);
-        s1 = *reinterpret_cast<const uint4*>(state + TF_H + c);
-    } else {
-        const uint16_t* r2 = bcx + size_t(row_base - 2) * TF_CIN + c;
-        const uint16_t* r1 = bcx + size_t(row_base - 1) * TF_CIN + c;
-        s0 = gate8(*reinterpret_cast<const uint4*>(r2), *reinterpret_cast<const uint4*>(r2 + 2 * TF_H));
-        s1 = gate8(*reinterpret_cast<const uint4*>(r1), *reinterpret_cast<const uint4*>(r1 + 2 * TF_H));
+    uint4 wv[3];   // taps of channels c..c+7: 24 bf16, element (channel j, tap k) at 3*j+k
+    {
+        const uint4* wp = reinterpret_cast<const uint4*>(w + size_t(c) * 3);
+        wv[0] = __ldg(wp + 0);
+        wv[1] = __ldg(wp + 1);
+        wv[2] = __ldg(wp + 2);
     }
-    const uint4 old0 = s0, old1 = s1;
+    // the two entries before the tile (rows 0 and 1 use them): the old state
+    // for the first tile, else recomputed from the two input rows before it
+    uint4 pm2 = make_uint4(0, 0, 0, 0), pm1 = make_uint4(0, 0, 0, 0);
+    if (slot < 2 && slot < n) {
+        if (first) {
+            if (slot == 0) pm2 = *reinterpret_cast<const uint4*>(state + c);
+            pm1 = *reinterpret_cast<const uint4*>(state + TF_H + c);
+        } else {
+            const uint16_t* r1 = bcx + size_t(row_base - 1) * TF_CIN + c;
+            pm1 = gate8(*reinterpret_cast<const uint4*>(r1), *reinterpret_cast<const uint4*>(r1 + 2 * TF_H));
+            if (slot == 0) {
+                const uint16_t* r2 = bcx + size_t(row_base - 2) * TF_CIN + c;
+                pm2 = gate8(*reinterpret_cast<const uint4*>(r2), *reinterpret_cast<const uint4*>(r2 + 2 * TF_H));
+            }
+        }
+    }
+    // a window that continues past its first tile: its last two entries (the new state)
+    uint4 nl2 = make_uint4(0, 0, 0, 0), nl1 = make_uint4(0, 0, 0, 0);
+    const bool writes_state = first && slot == 0;
+    if (writes_state && st.rows > n) {
+        const uint16_t* r2 = bcx + size_t(st.row_offset + st.rows - 2) * TF_CIN + c;
+        const uint16_t* r1 = bcx + size_t(st.row_offset + st.rows - 1) * TF_CIN + c;
+        nl2 = gate8(*reinterpret_cast<const uint4*>(r2), *reinterpret_cast<const uint4*>(r2 + 2 * TF_H));
+        nl1 = gate8(*reinterpret_cast<const uint4*>(r1), *reinterpret_cast<const uint4*>(r1 + 2 * TF_H));
+    }
     pdl_trigger();
 
-    float f0[8], f1[8];
-    unpack8(s0, f0);
-    unpack8(s1, f1);
+    uint4 bx[2];
 #pragma unroll
-    for (int j = 0; j < kConvTileRows; ++j) {
+    for (int k = 0; k < 2; ++k) {
+        const int j = slot + k * kSlots;
         if (j < n) {
-            const uint4 bx = gate8(B[j], X[j]);
-            float f2[8], fc[8];
-            unpack8(bx, f2);
-            unpack8(C[j], fc);
-            float o[8];
+            bx[k] = gate8(B[k], X[k]);
+            sbx[j][grp] = bx[k];
+        }
+    }
+    __syncthreads();   // every entry of the tile is in; every read of the old state is done
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                float conv = wt[3 * k] * f0[k];
-                conv = fmaf(wt[3 * k + 1], f1[k], conv);
-                conv = fmaf(wt[3 * k + 2], f2[k], conv);
-                o[k] = fc[k] * conv;
-            }
+    for (int k = 0; k < 2; ++k) {
+        const int j = slot + k * kSlots;
+        if (j < n) {
+            const uint4 e0 = j >= 2 ? sbx[j - 2][grp] : (j == 1 ? pm1 : pm2);
+            const uint4 e1 = j >= 1 ? sbx[j - 1][grp] : pm1;
+            float o[8];
+            conv8(wv, e0, e1, bx[k], C[k], o);
             float4* yp = reinterpret_cast<float4*>(y + size_t(row_base + j) * TF_H + c);
             __stcs(yp, make_float4(o[0], o[1], o[2], o[3]));
             __stcs(yp + 1, make_float4(o[4], o[5], o[6], o[7]));
-            if (hist)
-                *reinterpret_cast<uint4*>(hist + size_t(tile.row0 + j + 2) * TF_H + c) = bx;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                f0[k] = f1[k];
-                f1[k] = f2[k];
-            }
-            s0 = s1;
-            s1 = bx;
+            if (hist) *reinterpret_cast<uint4*>(hist + size_t(tile.row0 + j + 2) * TF_H + c) = bx[k];
         }
     }
-
-    if (tile.row0 == 0) {
-        if (hist) {
-            *reinterpret_cast<uint4*>(hist + c) = old0;
-            *reinterpret_cast<uint4*>(hist + TF_H + c) = old1;
+    if (writes_state) {
+        if (hist) {   // history rows 0, 1: the old state
+            *reinterpret_cast<uint4*>(hist + c) = pm2;
+            *reinterpret_cast<uint4*>(hist + TF_H + c) = pm1;
         }
         // new state = the last two entries of [state0, state1, bx_0 .. bx_{r-1}]
-        uint4 n0 = s0, n1 = s1;
-        if (st.rows > n) {   // the window continues in later tiles
-            const uint16_t* r2 = bcx + size_t(st.row_offset + st.rows - 2) * TF_CIN + c;
-            const uint16_t* r1 = bcx + size_t(st.row_offset + st.rows - 1) * TF_CIN + c;
-            n0 = gate8(*reinterpret_cast<const uint4*>(r2), *reinterpret_cast<const uint4*>(r2 + 2 * TF_H));
-            n1 = gate8(*reinterpret_cast<const uint4*>(r1), *reinterpret_cast<const uint4*>(r1 + 2 * TF_H));
+        uint4 n0 = nl2, n1 = nl1;
+        if (st.rows <= n) {   // the window ends in this tile
+            n0 = n >= 2 ? sbx[n - 2][grp] : pm1;
+            n1 = sbx[n - 1][grp];
         }
         *reinterpret_cast<uint4*>(state + c) = n0;
         *reinterpret_cast<uint4*>(state + TF_H + c) = n1;
