@@ -444,7 +444,7 @@ def run_tf(args, rank, world):
     # end to end through the C ABI with host buffers
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(d, args, stream, flush)
+        e2e = run_e2e(d, args, stream, flush, ab["total"])
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
@@ -491,25 +491,32 @@ def run_tf(args, rank, world):
     return 0
 
 
-def run_e2e(d, args, stream, flush):
+L2_BYTES = 129 << 20
+
+
+def run_e2e(d, args, stream, flush, step_bytes):
     """Same metric through the public API with host buffers: every step copies
-    its inputs (conv inputs, queries, logits, ids) from pinned host memory and
-    reads back the picks, flags and per-stream accept results."""
+    its inputs (conv inputs, queries, logits, ids: the step's input buffer)
+    from pinned host memory and reads back the picks, flags and per-stream
+    accept results (the step's result buffer).
+
+    Serial: copy in, step, copy out, one step at a time, L2 flushed between
+    steps (outside the events). Pipelined (the value, where the step's data
+    exceed twice the L2, so no flush is needed between steps): the serving
+    loop's form, two buffer sets and a copy stream each way, step k+1's inputs
+    copied in and step k-1's results read back while step k runs; timed over
+    the whole loop."""
     import torch
-    host_in = [(t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True).copy_(t)) for t in
-               d.bcx + d.q + [d.logits, d.ids]]
-    outs = [d.pick, d.flag, d.accept_len, d.next_token, d.new_keys, d.sflag]
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    h2d = sum(h.numel() * h.element_size() for _, h in host_in)
-    d2h = sum(h.numel() * h.element_size() for h in host_out)
+    host_in = torch.empty(d.in_arena.shape, dtype=torch.uint8, pin_memory=True).copy_(d.in_arena)
+    host_out = torch.empty(d.out_arena.shape, dtype=torch.uint8, pin_memory=True)
+    h2d = host_in.numel()
+    d2h = host_out.numel()
     steps = max(3, min(args.steps, 50))
 
     def one():
-        for dv, hv in host_in:
-            dv.copy_(hv, non_blocking=True)
+        d.in_arena.copy_(host_in, non_blocking=True)
         d.graph.replay()
-        for dv, hv in zip(outs, host_out):
-            hv.copy_(dv, non_blocking=True)
+        host_out.copy_(d.out_arena, non_blocking=True)
 
     for _ in range(3):
         one()
@@ -523,9 +530,66 @@ def run_e2e(d, args, stream, flush):
         b.record(stream)
         b.synchronize()
         ts.append(a.elapsed_time(b))
-    ms = sum(ts) / len(ts)
-    return {"value": d.R / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": ms, "steps": steps}
+    serial_ms = sum(ts) / len(ts)
+    res = {"value": d.R / (serial_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": serial_ms, "steps": steps, "form": "serial (copy in, step, copy out; L2 flushed between "
+                                                             "steps)"}
+    if step_bytes <= 2 * L2_BYTES:
+        return res
+
+    # pipelined: buffer set b = k % 2 for step k
+    g0 = d.graph
+    k1 = d.add_io_set()
+    d.use_io(k1)
+    g1 = d.capture()
+    d.use_io(0)
+    d.graph = g0
+    graphs = [g0, g1]
+    arenas_in = [d._io[0]["in_arena"], d._io[k1]["in_arena"]]
+    arenas_out = [d._io[0]["out_arena"], d._io[k1]["out_arena"]]
+    hosts_out = [host_out, torch.empty(d.out_arena.shape, dtype=torch.uint8, pin_memory=True)]
+    s_in, s_out = torch.cuda.Stream(device=stream.device), torch.cuda.Stream(device=stream.device)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    done = [torch.cuda.Event() for _ in range(2)]
+    read = [torch.cuda.Event() for _ in range(2)]
+
+    def loop(n):
+        for k in range(n):
+            b = k % 2
+            if k >= 2:
+                s_in.wait_event(done[b])      # step k-2 has read this input buffer
+            with torch.cuda.stream(s_in):
+                arenas_in[b].copy_(host_in, non_blocking=True)
+            copied[b].record(s_in)
+            stream.wait_event(copied[b])
+            if k >= 2:
+                stream.wait_event(read[b])    # step k-2's results are read back
+            graphs[b].replay()
+            done[b].record(stream)
+            s_out.wait_event(done[b])
+            with torch.cuda.stream(s_out):
+                hosts_out[b].copy_(arenas_out[b], non_blocking=True)
+            read[b].record(s_out)
+        stream.wait_event(read[(n - 1) % 2])
+        if n >= 2:
+            stream.wait_event(read[(n - 2) % 2])
+
+    loop(4)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    s_in.wait_event(a)
+    s_out.wait_event(a)
+    loop(steps)
+    b.record(stream)
+    b.synchronize()
+    ms = a.elapsed_time(b) / steps
+    res.update({"value": d.R / (ms * 1e-3), "ms_per_step": ms,
+                "form": "pipelined: two buffer sets, step k+1's inputs copied in and step k-1's results read "
+                        "back while step k runs (a copy stream each way); the step's data exceed twice the L2, "
+                        "so no flush between steps; timed over the whole loop",
+                "serial": {"value": d.R / (serial_ms * 1e-3), "ms_per_step": serial_ms}})
+    return res
 
 
 def run_row(args, rank, world):

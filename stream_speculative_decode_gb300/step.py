@@ -41,11 +41,27 @@ def _dev_bf16(x, device):
     return t.view(BF16).to(device)
 
 
+def _arena(specs, device):
+    """One uint8 device allocation holding tensors of the given (shape, dtype),
+    each at a 256-byte aligned offset: (buffer, [views])."""
+    offs, off = [], 0
+    for shape, dt in specs:
+        n = int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
+        offs.append((off, n))
+        off = (off + n + 255) // 256 * 256
+    buf = torch.empty(max(off, 256), dtype=torch.uint8, device=device)
+    views = [buf[o:o + n].view(dt).view(shape) for (o, n), (shape, dt) in zip(offs, specs)]
+    return buf, views
+
+
 class DeviceStep:
     """Device-resident inputs, outputs and segment table of one verify step.
 
     The conv states and the KV caches are the streams' persistent state; the
-    per-layer conv inputs, queries and the logits are the step's inputs.
+    per-layer conv inputs, queries and the logits are the step's inputs. The
+    step's inputs live in one device buffer (``in_arena``) and its per-step
+    results (picks, flags, accept results) in another (``out_arena``), so a
+    step with host buffers is one copy in and one copy out.
     """
 
     def __init__(self, inp: StepInputs, device="cuda", keep_history=True, stream=None, fused_attention=True,
@@ -77,22 +93,30 @@ class DeviceStep:
         self.K = [[_dev_bf16(k, dev) for k in inp.K[l]] for l in range(n_attn)]
         self.V = [[_dev_bf16(v, dev) for v in inp.V[l]] for l in range(n_attn)]
 
-        # step inputs
-        self.bcx = [_dev_bf16(b, dev) for b in inp.bcx]
+        # step inputs, one buffer
         self.w = [_dev_bf16(w, dev) for w in inp.w]
-        self.q = [_dev_bf16(q, dev) for q in inp.q]
-        self.logits = _dev_bf16(inp.logits, dev)
-        self.ids = torch.as_tensor(np.asarray(inp.ids, dtype=np.int32)).to(dev)
+        self._in_specs = ([((R, CIN), BF16)] * n_conv + [((R, NQ, D), BF16)] * n_attn +
+                          [((R, self.vocab), BF16), ((R,), torch.int32)])
+        self._out_specs = [((R,), torch.int32), ((R,), torch.uint8), ((S,), torch.int32), ((S,), torch.int32),
+                           ((S,), torch.int32), ((S,), torch.uint8)]
+        self.in_arena, views = _arena(self._in_specs, dev)
+        self.bcx = views[:n_conv]
+        self.q = views[n_conv:n_conv + n_attn]
+        self.logits, self.ids = views[n_conv + n_attn:]
+        for l in range(n_conv):
+            self.bcx[l].copy_(_dev_bf16(inp.bcx[l], dev).view(R, CIN))
+        for l in range(n_attn):
+            self.q[l].copy_(_dev_bf16(inp.q[l], dev).view(R, NQ, D))
+        self.logits.copy_(_dev_bf16(inp.logits, dev).view(R, self.vocab))
+        self.ids.copy_(torch.as_tensor(np.asarray(inp.ids, dtype=np.int32)).to(dev))
 
         # outputs
         self.y = [torch.empty((R, H), dtype=torch.float32, device=dev) for _ in range(n_conv)]
         self.out = [torch.empty((R, NQ, D), dtype=torch.float32, device=dev) for _ in range(n_attn)]
-        self.pick = torch.empty(R, dtype=torch.int32, device=dev)
-        self.flag = torch.empty(R, dtype=torch.uint8, device=dev)
-        self.accept_len = torch.empty(S, dtype=torch.int32, device=dev)
-        self.next_token = torch.empty(S, dtype=torch.int32, device=dev)
-        self.new_keys = torch.empty(S, dtype=torch.int32, device=dev)
-        self.sflag = torch.empty(S, dtype=torch.uint8, device=dev)
+        self.out_arena, (self.pick, self.flag, self.accept_len, self.next_token, self.new_keys, self.sflag) = _arena(
+            self._out_specs, dev)
+        self._io = [self._io_views()]   # buffer sets: the launches use self._io[self.io]
+        self.io = 0
 
         # segment table
         sz_state = 2 * H * 2
@@ -113,6 +137,32 @@ class DeviceStep:
         self.schedule = layer_schedule(n_conv, n_attn)
         self.fused_attention = fused_attention
         self.graph = None
+
+    # ------------------------------------------------------------ buffer sets
+    def _io_views(self):
+        return dict(in_arena=self.in_arena, bcx=self.bcx, q=self.q, logits=self.logits, ids=self.ids,
+                    out_arena=self.out_arena, pick=self.pick, flag=self.flag, accept_len=self.accept_len,
+                    next_token=self.next_token, new_keys=self.new_keys, sflag=self.sflag)
+
+    def add_io_set(self):
+        """Another pair of step-input and result buffers of the same layout (the
+        inputs copied from set 0), so a serving loop can copy step k+1's inputs
+        while step k runs. Returns its index for use_io()."""
+        in_arena, views = _arena(self._in_specs, self.device)
+        in_arena.copy_(self._io[0]["in_arena"])
+        out_arena, outs = _arena(self._out_specs, self.device)
+        n_conv, n_attn = self.n_conv, self.n_attn
+        self._io.append(dict(in_arena=in_arena, bcx=views[:n_conv], q=views[n_conv:n_conv + n_attn],
+                             logits=views[n_conv + n_attn], ids=views[n_conv + n_attn + 1], out_arena=out_arena,
+                             pick=outs[0], flag=outs[1], accept_len=outs[2], next_token=outs[3], new_keys=outs[4],
+                             sflag=outs[5]))
+        return len(self._io) - 1
+
+    def use_io(self, k):
+        """Point the launches (and capture()) at buffer set k."""
+        for name, v in self._io[k].items():
+            setattr(self, name, v)
+        self.io = k
 
     # ---------------------------------------------------------------- running
     def conv(self, l, stream=None):
