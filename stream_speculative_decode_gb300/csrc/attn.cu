@@ -122,6 +122,17 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
     unsigned char* sQ = smem + kStages * kStageB;
     const uint32_t sKV32 = smem_u32(sKV), sQ32 = smem_u32(sQ);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if constexpr (MT == 1) {
+        // narrow windows (one m-tile: short launches, one wave): the first
+        // stages' keys and values into L2 while the previous kernel finishes
+        // (measured 17.0 -> 16.0 us a layer for 16 one-row streams; the
+        // two-m-tile kernel spilled with it and ran slower)
+        if (tid == 0) {
+            const uint32_t pre = uint32_t(min(nkeys, (kStages - 1) * kKT)) * kRowB;
+            l2_prefetch_bulk(Kg, pre);
+            l2_prefetch_bulk(Vg, pre);
+        }
+    }
     pdl_wait();   // the table above; queries and caches below
 
     // group query rows qi: q0 + qi = 4*i + hh (window row i, head 4g + hh);

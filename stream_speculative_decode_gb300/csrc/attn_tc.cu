@@ -325,6 +325,13 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
         bars->abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (tid == 0 && int(blockIdx.x) < n_units) {   // the first unit's first tiles into L2 meanwhile
+        const Unit U = unit_of(t, layer, blockIdx.x);
+        for (int j = 0; j < U.T && j < kStages; ++j) {
+            tma_prefetch_3d(U.kmap, 0, U.c0 + j * kKT, U.g);
+            tma_prefetch_3d(U.vmap, 0, U.c0 + j * kKT, U.g);
+        }
+    }
     pdl_wait();   // the table above; queries and caches below
     if (warp == 4) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"

@@ -130,6 +130,13 @@ int sm_count();
 // it); after it, everything the previous kernels wrote is visible. Each kernel
 // lets its dependents launch once it has finished its main work.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Bulk prefetch of [p, p + bytes) into L2 (16-byte aligned, bytes a multiple
+// of 16). A non-binding hint, so a kernel may issue it before pdl_wait: L2 is
+// the GPU's point of coherence, and a line a previous kernel is still writing
+// is not read into the kernel early.
+__device__ __forceinline__ void l2_prefetch_bulk(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 template <typename... KArgs, typename... Args>
