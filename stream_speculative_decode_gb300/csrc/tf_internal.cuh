@@ -127,7 +127,8 @@ int sm_count();
 // serialization: it may start while the previous kernel of the stream is
 // finishing. Before griddepcontrol.wait a kernel reads nothing but the
 // segment table (immutable once built, uploaded before any launch that uses
-// it); after it, everything the previous kernels wrote is visible. Each kernel
+// it) and may issue L2 prefetches (l2_prefetch_bulk); after it, everything
+// the previous kernels wrote is visible. Each kernel
 // lets its dependents launch once it has finished its main work.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // Bulk prefetch of [p, p + bytes) into L2 (16-byte aligned, bytes a multiple

@@ -114,6 +114,27 @@ def test_step_mixed_small(mods):
     run_and_check(mods, w)
 
 
+def test_step_second_buffer_set(mods):
+    """The step replayed from a graph captured on a second input/result
+    buffer set (the pipelined serving loop's other half) matches the oracle,
+    and leaves the first set's result buffer untouched."""
+    tf, inputs, step, torch = mods
+    w = small_work(mods, rows=[2, 9, 1, 16], keys=[700, 3000, 5, 9000], seed=11)
+    inp = inputs.make_inputs(w, backend="numpy")
+    d = step.DeviceStep(inp)
+    d.out_arena.fill_(0xAB)
+    k = d.add_io_set()
+    assert k == 1
+    d.use_io(k)
+    d.capture()
+    d.graph.replay()
+    res = d.results()
+    check_step(res, O.verify_step(inp), inp)
+    d.use_io(0)
+    assert bool((d.out_arena == 0xAB).all())
+    d.free()
+
+
 @pytest.mark.parametrize("path", ["mma", "tc"])
 def test_step_forced_kernel(mods, path, monkeypatch):
     """Every stream forced onto one attention kernel (the mma.sync kernel for
@@ -146,9 +167,11 @@ def test_step_merge_modes(mods, fused):
 
 
 def test_step_chunk_edges(mods):
-    """Key counts at, just below and just above split-K chunk multiples."""
-    rows = [1, 1, 1, 2, 2, 4, 4, 8, 6]
-    keys = [1024, 1023, 1025, 2048, 2049, 1024, 1023, 2049, 1537]
+    """Key counts at, just below and just above split-K chunk multiples
+    (256*max(r, 4) keys; 512*r for the 13-16-row windows of the tensor-core
+    kernel)."""
+    rows = [1, 1, 1, 2, 2, 4, 4, 8, 6, 16, 16, 13, 13]
+    keys = [1024, 1023, 1025, 2048, 2049, 1024, 1023, 2049, 1537, 8192, 8193, 6656, 6657]
     run_and_check(mods, small_work(mods, rows, keys, n_conv=1, n_attn=1, seed=6))
 
 
