@@ -53,7 +53,7 @@ class Workload:
 
 
 def workload(index, n_conv=None, n_attn=None, vocab=None):
-    """Workload ``index`` (1..5) with its shapes drawn from PCG64(index).
+    """Workload ``index`` (1..6) with its shapes drawn from PCG64(index).
 
     1: 1 stream, window 4, 512 keys, 1 conv + 1 attention layer, a planted tie
        and one NaN row, 3 random drafts.
@@ -65,6 +65,8 @@ def workload(index, n_conv=None, n_attn=None, vocab=None):
     5: 64 streams of 16 rows (1,024 rows), keys log-uniform on [16, 32768]
        (rounded, raised to the window), drafts accepted with geometric length
        (p = 0.7 per draft).
+    6: the other reading of workload 5 (labelled as such): the same key draw,
+       rows U{1..16} per stream, not rescaled to 1,024 (R about 544).
     """
     rng = np.random.Generator(np.random.PCG64(index))
     if index == 1:
@@ -83,14 +85,17 @@ def workload(index, n_conv=None, n_attn=None, vocab=None):
     elif index == 4:
         w = Workload("4-stream long context, 6-row windows", [6] * 4,
                      [65536, 65536, 130816, 130816], 30, 10, drafts="random", inf_frac=0.01)
-    elif index == 5:
-        rows = [16] * 64
+    elif index in (5, 6):
+        if index == 6:   # the key draw of workload 5, then the rows
+            rng = np.random.Generator(np.random.PCG64(5))
         lk = rng.uniform(math.log(16), math.log(32768), size=64)
+        rows = [16] * 64 if index == 5 else [int(r) for r in rng.integers(1, 17, size=64)]
         keys = [max(int(round(math.exp(v))), r) for v, r in zip(lk, rows)]
-        w = Workload("64x16-row drafted windows, log-uniform keys", rows, keys, 30, 10,
-                     drafts="geom=0.7")
+        name = ("64x16-row drafted windows, log-uniform keys" if index == 5 else
+                "64 streams of U{1..16} rows (workload 5 unscaled), log-uniform keys")
+        w = Workload(name, rows, keys, 30, 10, drafts="geom=0.7")
     else:
-        raise ValueError("workload index must be 1..5")
+        raise ValueError("workload index must be 1..6")
     w.seed = index
     if n_conv is not None:
         w.n_conv = n_conv

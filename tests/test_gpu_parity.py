@@ -294,9 +294,9 @@ def test_refusals_on_device(mods):
     d.free()
 
 
-# ------------------------------------------------ full-size workloads 2..5
+# ------------------------------------------------ full-size workloads 2..6
 
-@pytest.mark.parametrize("index", [2, 3, 4, 5])
+@pytest.mark.parametrize("index", [2, 3, 4, 5, 6])
 def test_workload_full_size_sampled(mods, index):
     """Full stream, row, key and vocabulary sizes with one conv and one
     attention layer (the launches the timed step makes for each layer),
