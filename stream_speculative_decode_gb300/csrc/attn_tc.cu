@@ -151,7 +151,7 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
         const int gj = st.g0 + j;
         const int b = gj % kSBuf;
         const uint32_t colS = kColS + 64 * b;
-        if (!mbar_wait(su32(&bars->s_full[b]), (gj / kSBuf) & 1, st.abortp)) break;
+        if (!mbar_wait_warp(su32(&bars->s_full[b]), (gj / kSBuf) & 1, st.abortp)) break;
         tc_fence_after();
         if (st.wact) {
             const int k0 = j * kKT + half * NV;      // chunk-local key of v[0]
@@ -183,7 +183,7 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
             const bool resc = mxs > st.mref + kTau;
             if (__any_sync(0xFFFFFFFFu, resc)) {
                 // O holds P.V of the unit's tiles < j; the last of them (j-1) must be done
-                if (j >= 1 && !mbar_wait(su32(&bars->o_done[(gj - 1) % kSBuf]), ((gj - 1) / kSBuf) & 1, st.abortp))
+                if (j >= 1 && !mbar_wait_warp(su32(&bars->o_done[(gj - 1) % kSBuf]), ((gj - 1) / kSBuf) & 1, st.abortp))
                     break;
                 tc_fence_after();
                 const float alpha = resc ? ex2(st.mref - mxs) : 1.f;
@@ -252,7 +252,7 @@ __device__ __forceinline__ int next_unit_thread(Bars* bars, int m, volatile uint
 __device__ __forceinline__ int next_unit_warp(Bars* bars, int m, volatile uint32_t* abortp) {
     const int slot = m % kUQ;
     int u = -1;
-    if (mbar_wait(su32(&bars->uq_full[slot]), (m / kUQ) & 1, abortp))
+    if (mbar_wait_warp(su32(&bars->uq_full[slot]), (m / kUQ) & 1, abortp))
         u = reinterpret_cast<volatile int32_t*>(bars->uq)[slot];
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(su32(&bars->uq_empty[slot]));
@@ -440,7 +440,7 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
             const int T = unit_of(t, layer, u).T;
             for (int j = 0; j < T; ++j, ++gt) {
                 const int s = gt % kStages;
-                if (!mbar_wait(su32(&bars->kv_full[s]), (gt / kStages) & 1, abortp)) {
+                if (!mbar_wait_warp(su32(&bars->kv_full[s]), (gt / kStages) & 1, abortp)) {
                     ok = false;
                     break;
                 }

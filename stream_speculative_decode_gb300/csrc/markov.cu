@@ -41,6 +41,9 @@
 // Every mbarrier wait is bounded (2 s of %globaltimer); on a timeout the CTA
 // raises its abort flag, drains its copies and MMAs (bounded), marks its
 // streams' rows with flag bit 1, frees its tensor memory and returns.
+#include <cstdlib>
+#include <cstring>
+
 #include "tc_ptx.cuh"
 
 namespace tf {
@@ -298,7 +301,7 @@ markov_step_kernel(SegTable t, int step, const uint16_t* __restrict__ W1, int vo
             const int b = tt & 1;
             const int v0 = (t_begin + tt) * kTileV;
             if (wact && tt + 1 < ntl) load_base_tile(brow, v0 + kTileV, vocab, nxt);
-            if (!mbar_wait(su32(&bars->acc_full[b]), (tt >> 1) & 1, abortp)) break;
+            if (!mbar_wait_warp(su32(&bars->acc_full[b]), (tt >> 1) & 1, abortp)) break;
             tc_fence_after();
             if (wact) {
 #pragma unroll
@@ -374,6 +377,328 @@ markov_step_kernel(SegTable t, int step, const uint16_t* __restrict__ W1, int vo
     }
 }
 
+// ---- the whole chain in one launch --------------------------------------
+//
+// Tables of at most 128 streams (one lane group) run every step of the chain
+// in one cooperative launch: the CTAs (one per SM, all resident) keep their
+// range of W2 tiles for every step, the TMA producer streams those tiles step
+// after step without a break (W2 does not depend on the picks), and between
+// steps the CTAs meet once: each adds its best scores to the step's per-stream
+// keys, counts its arrival, and the last to arrive writes the step's picks and
+// opens the next step (a generation word); the epilogue warps then gather the
+// next step's W1 rows while the producer is already filling the ring. Every
+// wait is bounded: an mbarrier wait or the step barrier that runs out raises
+// the CTA's abort flag and a global one (the other CTAs stop waiting), and the
+// rows of the steps not done are flagged (bit 1).
+
+struct ChainBars {
+    uint64_t full[kStages];
+    uint64_t empty[kStages];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t e_ready;       // the step's W1 rows are in E (the 128 epilogue threads)
+    uint64_t drain;
+    uint32_t tmem_base;
+    uint32_t abort_flag;
+    int32_t last;
+    int32_t stop;           // epilogue thread 0's snapshot of the abort flag, read after a barrier
+    int32_t tok[kLanes];
+    int32_t row[kLanes];
+};
+constexpr int kChainSmemBytes = 1024 + kAB + kStages * kSlabB + int(sizeof(ChainBars));
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Wait until the step barrier's generation reaches `target` (one thread).
+__device__ bool chain_wait(const uint32_t* sync, uint32_t target, volatile uint32_t* abortp) {
+    const unsigned long long t0 = gtime();
+    for (;;) {
+        uint32_t g;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(sync + 1) : "memory");
+        if (g >= target) return true;
+        if (*abortp) return false;
+        if (*reinterpret_cast<const volatile uint32_t*>(sync + 2)) {   // another CTA gave up
+            *abortp = 1;
+            return false;
+        }
+        if (gtime() - t0 > kTimeoutNs) {
+            *abortp = 1;
+            return false;
+        }
+        __nanosleep(64);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+markov_chain_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, int vocab,
+                    const uint16_t* __restrict__ base, int64_t base_stride, const int32_t* __restrict__ prev,
+                    int32_t* __restrict__ pick, uint8_t* __restrict__ flag,
+                    const __grid_constant__ CUtensorMap w2map) {
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = su32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    unsigned char* gbase = smem_raw + (sbase - raw);
+    const uint32_t sA = sbase;
+    const uint32_t sB = sbase + kAB;
+    ChainBars* bars = reinterpret_cast<ChainBars*>(gbase + kAB + kStages * kSlabB);
+    volatile uint32_t* abortp = &bars->abort_flag;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nt = (vocab + kTileV - 1) / kTileV;
+    const int t_begin = int((int64_t(blockIdx.x) * nt) / gridDim.x);
+    const int t_end = int((int64_t(blockIdx.x + 1) * nt) / gridDim.x);
+    const int ntl = t_end - t_begin;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(su32(&bars->full[s]), 1);
+            mbar_init(su32(&bars->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(su32(&bars->acc_full[b]), 1);
+            mbar_init(su32(&bars->acc_empty[b]), 4);
+        }
+        mbar_init(su32(&bars->e_ready), kLanes);
+        mbar_init(su32(&bars->drain), 1);
+        bars->abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    pdl_wait();   // previous tokens and base rows may come from the kernel just before
+    if (warp == 4) tc_alloc(su32(&bars->tmem_base), kCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    int done_steps = 0;   // epilogue: steps whose picks are written
+
+    if (warp == 5) {
+        // ------------------------------------------------------------ TMA producer, every step
+        if (lane == 0) {
+            const uint64_t keep = l2_evict_last();
+            const int total = steps * ntl * kKB;
+            int issued = 0;
+            for (int i = 0; i < total; ++i) {
+                const int s = i % kStages;
+                if (i >= kStages && !mbar_wait(su32(&bars->empty[s]), ((i / kStages) - 1) & 1, abortp)) break;
+                const int il = i % (ntl * kKB);   // k-block within the step
+                const uint32_t bar = su32(&bars->full[s]);
+                mbar_expect_tx(bar, kSlabB);
+                tma_load_2d_hint(sB + s * kSlabB, &w2map, (il % kKB) * 64, (t_begin + il / kKB) * kTileV, bar, keep);
+                ++issued;
+            }
+            if (*abortp)
+                for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+                    mbar_drain(su32(&bars->full[i % kStages]), (i / kStages) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ MMA, every step
+        if (lane == 0) {
+            bool ok = true;
+            for (int j = 0; j < steps && ok; ++j) {
+                ok = mbar_wait(su32(&bars->e_ready), j & 1, abortp);   // the step's W1 rows are in E
+                if (!ok) break;
+                tc_fence_after();
+                for (int tt = 0; tt < ntl && ok; ++tt) {
+                    const int gt = j * ntl + tt, b = gt & 1;
+                    if (gt >= 2) {
+                        ok = mbar_wait(su32(&bars->acc_empty[b]), ((gt >> 1) - 1) & 1, abortp);
+                        if (!ok) break;
+                    }
+                    tc_fence_after();
+                    for (int kb = 0; kb < kKB && ok; ++kb) {
+                        const int i = gt * kKB + kb, s = i % kStages;
+                        ok = mbar_wait(su32(&bars->full[s]), (i / kStages) & 1, abortp);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint64_t da = sdesc(sA + kb * kSlabB, 16, 1024);
+                        const uint64_t db = sdesc(sB + s * kSlabB, 16, 1024);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            tc_mma_ss(tmem + uint32_t(b * kTileV), da + 2 * k, db + 2 * k, kIdesc,
+                                      (kb | k) ? 1u : 0u);
+                        tc_commit(su32(&bars->empty[s]));
+                    }
+                    if (ok) tc_commit(su32(&bars->acc_full[b]));
+                }
+            }
+            tc_commit(su32(&bars->drain));
+            mbar_drain(su32(&bars->drain), 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue + W1 gather, every step
+        const int L = 4 * lane + warp;   // the stream on TMEM lane 32*warp + lane
+        const uint32_t tlane = tmem + (uint32_t(warp * 32) << 16);
+        // this CTA's slice of stream tid's base row of step jj into L2 (rows do
+        // not depend on the picks, so a step ahead; whole 16-byte units only)
+        auto prefetch_base = [&](int jj) {
+            if (tid < t.S && jj < steps) {
+                const SegStream st = t.streams[tid];
+                if (st.rows - 1 > jj) {
+                    const int v_begin = t_begin * kTileV;
+                    const int v_end = min(t_end * kTileV, vocab);
+                    const uint32_t bytes = uint32_t(v_end - v_begin) * 2u & ~15u;
+                    if (bytes) l2_prefetch_bulk(base + int64_t(st.row_offset - tid + jj) * base_stride + v_begin, bytes);
+                }
+            }
+        };
+        prefetch_base(0);
+        // Every exit from this loop is taken by the four warps together: the
+        // decision is thread 0's snapshot (bars->stop), written before a
+        // barrier and read after it.
+        for (int j = 0; j < steps; ++j) {
+            // the previous step's picks are written (step barrier), then this step's tokens
+            if (j > 0) {
+                if (tid == 0) {
+                    chain_wait(t.mk_sync, uint32_t(j), abortp);
+                    bars->stop = *abortp ? 1 : 0;
+                }
+                epi_sync();
+                if (bars->stop) break;
+            }
+            {
+                const int s = tid;
+                int tok = -1, row = -1;
+                if (s < t.S) {
+                    const SegStream st = t.streams[s];
+                    if (st.rows - 1 > j) {
+                        row = st.row_offset - s + j;
+                        tok = j == 0 ? prev[s] : __ldcg(pick + row - 1);
+                        if (tok < 0 || tok >= vocab) tok = -1;
+                    }
+                }
+                bars->tok[tid] = tok;
+                bars->row[tid] = row;
+            }
+            epi_sync();
+            // E = the streams' W1 rows (every MMA of the step before has completed:
+            // this warp group read each of its accumulators)
+            for (int idx = tid; idx < kLanes * (TF_MK / 8); idx += kLanes) {
+                const int Ls = idx >> 5, c = idx & 31, m = lane_of(Ls);
+                const int tok = bars->tok[Ls];
+                const uint16_t* src = tok >= 0 ? W1 + size_t(tok) * TF_MK + c * 8 : W1;
+                cp_async16(sA + (c >> 3) * kSlabB + m * 128 + (((c & 7) ^ (m & 7)) << 4), src, tok >= 0);
+            }
+            asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+            fence_async_smem();
+            mbar_arrive(su32(&bars->e_ready));
+            prefetch_base(j + 1);
+
+            const int my_tok = bars->tok[L];
+            const int my_row = bars->row[L];
+            const bool valid = my_tok >= 0;
+            const bool wact = __any_sync(0xFFFFFFFFu, valid);
+            const uint16_t* brow = base + (valid ? my_row : 0) * base_stride;
+            float best = -INFINITY;
+            int bid = 0x7FFFFFFF;
+            uint32_t nf = 0;
+            uint32_t cur[64], nxt[64];
+            if (wact && ntl > 0) load_base_tile(brow, t_begin * kTileV, vocab, cur);
+            bool ok = true;
+            for (int tt = 0; tt < ntl; ++tt) {
+                const int gt = j * ntl + tt, b = gt & 1;
+                const int v0 = (t_begin + tt) * kTileV;
+                if (wact && tt + 1 < ntl) load_base_tile(brow, v0 + kTileV, vocab, nxt);
+                if (!mbar_wait_warp(su32(&bars->acc_full[b]), (gt >> 1) & 1, abortp)) {
+                    ok = false;   // leaves the tile loop only: the step's barriers below are still met
+                    break;
+                }
+                tc_fence_after();
+                if (wact) {
+                    // two pieces of 32 columns in flight: the next one loads while
+                    // this one is scored
+                    uint32_t ra[32], rb[32];
+                    tc_ld_n<32>(tlane + uint32_t(b * kTileV), ra);
+#pragma unroll
+                    for (int p = 0; p < kTileV / 32; ++p) {
+                        tc_wait_ld();
+                        uint32_t(&r)[32] = (p & 1) ? rb : ra;
+                        if (p + 1 < kTileV / 32)
+                            tc_ld_n<32>(tlane + uint32_t(b * kTileV + 32 * (p + 1)), (p & 1) ? ra : rb);
+                        const int v = v0 + 32 * p;
+                        if (v < vocab && valid) {
+                            const int n = vocab - v < 32 ? vocab - v : 32;
+                            score_piece(r, cur + 16 * p, v, n, best, bid, nf);
+                        }
+                    }
+                    tc_wait_ld();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(su32(&bars->acc_empty[b]));
+#pragma unroll
+                for (int k = 0; k < 64; ++k) cur[k] = nxt[k];
+            }
+            nf = (nf & 0x80008000u) ? 1u : 0u;
+            if (valid && ok) {
+                if (bid != 0x7FFFFFFF)
+                    atomicMax(&t.mk_keys[L], (static_cast<unsigned long long>(ord_bf16(best)) << 32) |
+                                                 static_cast<unsigned long long>(0xFFFFFFFFu - uint32_t(bid)));
+                if (nf) atomicOr(&t.mk_flags[L], 1u);
+            }
+            __threadfence();
+            epi_sync();
+            if (tid == 0) {
+                bars->stop = *abortp ? 1 : 0;
+                bars->last = 0;
+                if (!bars->stop) {
+                    __threadfence();
+                    bars->last = atomicAdd(t.mk_sync, 1u) == uint32_t(j + 1) * gridDim.x - 1;
+                }
+            }
+            epi_sync();
+            if (bars->stop) break;
+            if (bars->last) {
+                // the step's picks and flags, then its scratch back to zero
+                __threadfence();
+                if (bars->row[tid] >= 0) {
+                    const unsigned long long key = atomicExch(&t.mk_keys[tid], 0ull);
+                    const uint32_t fl = atomicExch(&t.mk_flags[tid], 0u);
+                    int p = -1;
+                    uint8_t f = 1;
+                    if (bars->tok[tid] >= 0) {
+                        if (fl) {
+                            f = uint8_t(fl);
+                        } else {
+                            p = int(0xFFFFFFFFu - uint32_t(key & 0xFFFFFFFFull));
+                            f = 0;
+                        }
+                    }
+                    pick[bars->row[tid]] = p;
+                    flag[bars->row[tid]] = f;
+                }
+                __threadfence();
+                epi_sync();
+                if (tid == 0) {   // open the next step
+                    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(t.mk_sync + 1), "r"(uint32_t(j + 1))
+                                 : "memory");
+                }
+            }
+            done_steps = j + 1;
+        }
+        if (*abortp) {
+            // give up: the other CTAs stop waiting; this stream's rows of the
+            // steps not done are flagged
+            atomicExch(t.mk_sync + 2, 1u);
+            if (tid < t.S) {
+                const SegStream st = t.streams[tid];
+                for (int j = done_steps; j + 1 < st.rows; ++j) {
+                    pick[st.row_offset - tid + j] = -1;
+                    flag[st.row_offset - tid + j] = 2;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_trigger();
+    if (warp == 4) {
+        tc_fence_after();
+        tc_dealloc(tmem, kCols);
+    }
+}
+
 }  // namespace
 }  // namespace tf
 
@@ -397,6 +722,29 @@ extern "C" int tf_markov_chain(const tf_segments* seg, const void* W1, const voi
     const dim3 grid(gx, (t.S + kLanes - 1) / kLanes);
     const uint16_t* w1 = static_cast<const uint16_t*>(W1);
     const uint16_t* b = static_cast<const uint16_t*>(base);
+    const char* path = std::getenv("TF_MARKOV_PATH");
+    const bool per_step = (path && std::strcmp(path, "step") == 0) || t.S > kLanes;
+    if (!per_step) {
+        // the whole chain in one cooperative launch (every CTA resident: one per SM)
+        e = cudaFuncSetAttribute(markov_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChainSmemBytes);
+        if (e != cudaSuccess) return cuda_fail(e);
+        e = cudaMemsetAsync(t.mk_sync, 0, 4 * sizeof(uint32_t), stream);   // the step barrier starts at zero
+        if (e != cudaSuccess) return cuda_fail(e);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(gx);
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = kChainSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, markov_chain_kernel, t, t.max_rows - 1, w1, vocab, b, base_stride, prev, pick,
+                               flag, map);
+        if (e != cudaSuccess) return cuda_fail(e);
+        return launch_status();
+    }
     for (int j = 0; j + 1 < t.max_rows; ++j) {
         const int rc = launch_pdl(markov_step_kernel, grid, dim3(kThreads), kSmemBytes, stream, t, j, w1, vocab, b,
                                   base_stride, prev, pick, flag, map);

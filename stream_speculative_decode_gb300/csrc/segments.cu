@@ -229,6 +229,7 @@ int finish_build(tf_segments* seg, std::vector<tf::SegStream>& ss, std::vector<i
     const size_t o_mkf = off;      off = align_up(off + sizeof(uint32_t) * S, 256);
     const size_t o_mkc = off;      off = align_up(off + sizeof(uint32_t) * n_groups, 256);
     const size_t o_tcw = off;      off = align_up(off + sizeof(int32_t) * 2 * size_t(n_attn), 256);
+    const size_t o_mks = off;      off = align_up(off + sizeof(uint32_t) * 4, 256);
     const size_t total = off;
 
     seg->host.assign(total, 0);
@@ -302,6 +303,7 @@ int finish_build(tf_segments* seg, std::vector<tf::SegStream>& ss, std::vector<i
         t.mk_flags = reinterpret_cast<uint32_t*>(b + o_mkf);
         t.mk_ctr = reinterpret_cast<uint32_t*>(b + o_mkc);
         t.tc_work = reinterpret_cast<int32_t*>(b + o_tcw);   // zero in the image
+        t.mk_sync = reinterpret_cast<uint32_t*>(b + o_mks);
         rc = attn_prepare();
         if (rc == TF_OK) rc = attn_tc_prepare();
         if (rc != TF_OK) {

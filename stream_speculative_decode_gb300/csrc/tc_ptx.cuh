@@ -61,6 +61,11 @@ __device__ bool mbar_wait(uint32_t a, uint32_t parity, volatile uint32_t* abort_
         }
     }
 }
+// The same wait by a whole warp, with one outcome for all its lanes (a lane
+// that ran out would otherwise leave the warp's collective operations short).
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t a, uint32_t parity, volatile uint32_t* abort_flag) {
+    return __all_sync(0xFFFFFFFFu, mbar_wait(a, parity, abort_flag));
+}
 // Bounded wait that ignores the abort flag (draining after an abort).
 __device__ void mbar_drain(uint32_t a, uint32_t parity) {
     const unsigned long long t0 = gtime();

@@ -77,6 +77,7 @@ struct SegTable {
     uint32_t* mk_flags;               // [S] Markov step: nonfinite / gave-up bits per stream, self-resetting
     uint32_t* mk_ctr;                 // [ceil(S/128)] Markov step: CTA arrivals per stream group
     int32_t* tc_work;                 // [n_attn][2] tensor-core attention: units handed out, CTAs done (self-resetting)
+    uint32_t* mk_sync;                // [4] Markov chain in one launch: arrivals, generation, abort (zeroed per launch)
 };
 
 constexpr int kAttnMma = 0;   // mma.sync flash-decode kernel (narrow windows)

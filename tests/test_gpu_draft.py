@@ -189,23 +189,30 @@ def test_markov_golden_cases(mods):
     assert n >= 9
 
 
+@pytest.mark.parametrize("path", [None, "step"])
 @pytest.mark.parametrize("vocab,rows", [
     (1000, [3, 1, 5, 2, 16, 4]),     # 8 W2 tiles of 128, one per CTA
     (1003, [2, 7, 1, 3]),            # a ragged last tile
     (20000, [4, 4, 9]),              # several tiles per CTA
 ])
-def test_markov_random(mods, vocab, rows):
+def test_markov_random(mods, vocab, rows, path, monkeypatch):
+    """The whole chain in one launch (tables of up to 128 streams) and one
+    launch per step (TF_MARKOV_PATH=step); each twice on the same table (the
+    scratch and the step barrier reset themselves)."""
     tf, inputs, _, _ = mods
+    if path:
+        monkeypatch.setenv("TF_MARKOV_PATH", path)
     w = inputs.Workload("markov", rows, [r for r in rows], 0, 0, vocab=vocab, seed=41 + vocab)
     d = inputs.make_draft_inputs(w, nan_rows=1)
     seg = _rows_table(tf, rows)
-    pick, flag = _markov_gpu(mods, seg, d.W1, d.W2, d.base, d.prev, vocab)
-    n_rows, n_exact = _check_chains(pick, flag, d.streams, d.base, d.W1, d.W2, d.prev, f"V={vocab}")
-    assert n_rows == sum(r - 1 for r in rows)
-    assert n_exact >= n_rows - 1
-    # the planted NaN row and the rest of its chain are flagged
-    (_kind, r_nan, _i), = d.planted["nonfinite"]
-    assert flag[r_nan] == 1 and pick[r_nan] == -1
+    for _ in range(2):
+        pick, flag = _markov_gpu(mods, seg, d.W1, d.W2, d.base, d.prev, vocab)
+        n_rows, n_exact = _check_chains(pick, flag, d.streams, d.base, d.W1, d.W2, d.prev, f"V={vocab}")
+        assert n_rows == sum(r - 1 for r in rows)
+        assert n_exact >= n_rows - 1
+        # the planted NaN row and the rest of its chain are flagged
+        (_kind, r_nan, _i), = d.planted["nonfinite"]
+        assert flag[r_nan] == 1 and pick[r_nan] == -1
     seg.free()
 
 
