@@ -293,9 +293,12 @@ int tf_accept(const tf_segments* seg, const int32_t* ids, const int32_t* pick,
  *               valid previous token (outside [0, vocab), e.g. a flagged row
  *               before it); bit 1 the kernel gave up waiting for its own
  *               copies or MMAs (more than 2 s; the row is not computed)
- * One launch per step (rows_max - 1 launches), each reading W2 once for up to
- * 128 streams. The table holds the cross-CTA scratch: calls on one table must
- * not overlap on the GPU. Errors: TF_EINVAL (null, misaligned W2 or base,
+ * Tables of at most 128 streams run the whole chain in one cooperative launch
+ * (one CTA per SM, all resident; the CTAs meet between steps, every wait
+ * bounded) after a 16-byte memset of the table's step barrier; larger tables
+ * (or TF_MARKOV_PATH=step) take one launch per step (rows_max - 1 launches).
+ * Either way W2 is read once a step for up to 128 streams. The table holds the
+ * cross-CTA scratch: calls on one table must not overlap on the GPU. Errors: TF_EINVAL (null, misaligned W2 or base,
  * base_stride < vocab or not a multiple of 8, vocab < 1), TF_ERANGE
  * (vocab > 2^24). */
 int tf_markov_chain(const tf_segments* seg, const void* W1, const void* W2, int vocab,
