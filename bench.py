@@ -18,7 +18,8 @@ process per core) on a bounded sample of the same workload.
 ``--row`` measures one of the draft side's operations on a workload's table of
 windows instead of the verify step (default workload 5, the 64 x 16-row
 table): ``markov`` the Markov head's chain over every draft row
-(tf_markov_chain, one launch per step), ``block`` one layer of the
+(tf_markov_chain: the whole chain in one launch for tables of up to 128
+streams), ``block`` one layer of the
 non-causal block attention (tf_attn_block), ``prompt`` one conv and one
 attention layer of a prompt (prefill) call of one stream (tf_prompt_build;
 2,048 rows after 14,336 cached keys by default). Each prints its own JSON line.
@@ -208,12 +209,17 @@ def measured_peaks():
 
 
 def kernel_source_hash():
-    """Hash of the attention kernels' sources (a recorded ncu traffic figure is
-    reported only while it matches)."""
+    """Hash of the attention kernels' sources, comments and blank space left
+    out (a recorded ncu traffic figure is reported only while it matches: any
+    change of the code itself makes it stale)."""
+    import re
     h = hashlib.sha256()
     for name in ("attn.cu", "attn_tc.cu", "tf_internal.cuh"):
-        with open(os.path.join(ROOT, "stream_speculative_decode_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "stream_speculative_decode_gb300", "csrc", name)) as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

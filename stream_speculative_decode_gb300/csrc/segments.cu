@@ -92,7 +92,7 @@ bool encode_w2_map(CUtensorMap* out, const void* w2, int rows) {
 // Attention kernel of a stream: tensor cores once its window holds 3 rows (12
 // query rows per KV head); TF_ATTN_PATH=mma|tc forces one (tests compare both).
 int attn_path_of(int rows) {
-    if (rows > 16) return kAttnTc;   // the mma.sync kernel holds at most four 16-row query tiles
+    if (rows > 16) return kAttnTc;   // prompt windows (17-32 rows): the tensor cores, whatever is forced
     const char* e = std::getenv("TF_ATTN_PATH");
     if (e && std::strcmp(e, "mma") == 0) return kAttnMma;
     if (e && std::strcmp(e, "tc") == 0) return kAttnTc;

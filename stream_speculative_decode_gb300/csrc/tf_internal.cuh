@@ -83,7 +83,7 @@ struct SegTable {
 constexpr int kAttnMma = 0;   // mma.sync flash-decode kernel (narrow windows)
 constexpr int kAttnTc = 1;    // tcgen05 + TMA kernel (windows of 13 rows or more)
 // Measured on GB300: the mma.sync kernel streams faster up to 12-row windows
-// (its 1..3 query m-tiles); from 13 rows it needs a fourth m-tile and the
+// (as one or two items of at most 8 rows); from 13 rows the
 // tensor-core kernel wins clearly.
 constexpr int kTcMinRows = 13;
 

@@ -262,7 +262,8 @@ def tf_attn_block(seg, attn_layer, q, partials, out, stream=None):
 
 
 def tf_markov_chain(seg, W1, W2, vocab, base, base_stride, prev, pick, flag, stream=None):
-    """The drafter's Markov head over the table's draft rows (one launch per step)."""
+    """The drafter's Markov head over the table's draft rows (one launch for the
+    whole chain when the table has at most 128 streams, else one per step)."""
     _check("tf_markov_chain", _lib.tf_markov_chain(_h(seg), _ptr(W1), _ptr(W2), vocab, _ptr(base), base_stride,
                                                    _ptr(prev), _ptr(pick), _ptr(flag), _stream(stream)))
 
