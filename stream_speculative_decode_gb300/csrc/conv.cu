@@ -8,7 +8,9 @@
 // Work split: a CTA owns one 8-row tile of one stream and 512 channels; its
 // 256 threads are 64 channel groups (8 consecutive channels, 16-byte loads of
 // B, C, x and the 3 taps) x 4 row slots, slot k taking the tile's rows k and
-// k + 4. Every thread loads its rows at once, gates them (bx = B*x) into
+// k + 4. A table of few tiles of two rows or more on average takes one row
+// per thread instead (32 groups x 8 slots, 256 channels a CTA: twice the
+// CTAs); the arithmetic of a row is the same either way. Every thread loads its rows at once, gates them (bx = B*x) into
 // shared memory, and after one barrier convolves each row with the two
 // entries before it, so the rows of a tile run in parallel rather than one
 // after the other. The two entries before a tile come from the conv state
@@ -23,11 +25,17 @@
 namespace tf {
 namespace {
 
-constexpr int kGroups = 64;                     // channel groups per CTA
 constexpr int kChan = 8;                        // channels per group
-constexpr int kChanPerCta = kGroups * kChan;    // 512
-constexpr int kSlots = kConvTileRows / 2;       // row slots: rows k and k + kSlots
-constexpr int kThreads = kGroups * kSlots;      // 256
+constexpr int kThreads = 256;
+// The split of a CTA's 256 threads: RPT rows of the tile per thread, so
+// 8 / RPT row slots (slot k takes rows k, k + 8/RPT, ...) and 256 * RPT / 8
+// channel groups of 8 channels.
+template <int RPT>
+struct Split {
+    static constexpr int kSlots = kConvTileRows / RPT;
+    static constexpr int kGroups = kThreads / kSlots;
+    static constexpr int kChanPerCta = kGroups * kChan;   // 512 (RPT 2) or 256 (RPT 1)
+};
 
 __device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -78,10 +86,13 @@ __device__ __forceinline__ void conv8(const uint4 (&w)[3], const uint4& e0, cons
     }
 }
 
+template <int RPT>
 __global__ void __launch_bounds__(kThreads, 4)
 conv_rows_kernel(SegTable t, int layer, const uint16_t* __restrict__ bcx,
                  const uint16_t* __restrict__ w, float* __restrict__ y) {
-    __shared__ uint4 sbx[kConvTileRows][kGroups];   // the tile's gated entries (8 KB)
+    constexpr int kSlots = Split<RPT>::kSlots, kGroups = Split<RPT>::kGroups;
+    constexpr int kChanPerCta = Split<RPT>::kChanPerCta;
+    __shared__ uint4 sbx[kConvTileRows][kGroups];   // the tile's gated entries (8 or 4 KB)
     const ConvTile tile = t.tiles[blockIdx.x];
     const SegStream st = t.streams[tile.stream];
     const int grp = threadIdx.x % kGroups, slot = threadIdx.x / kGroups;
@@ -94,10 +105,10 @@ conv_rows_kernel(SegTable t, int layer, const uint16_t* __restrict__ bcx,
     const bool first = tile.row0 == 0;
     pdl_wait();   // the table above; the data below may come from the previous kernel
 
-    // this thread's rows slot and slot + kSlots (loads issued before any arithmetic)
-    uint4 B[2], C[2], X[2];
+    // this thread's rows slot, slot + kSlots, ... (loads issued before any arithmetic)
+    uint4 B[RPT], C[RPT], X[RPT];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < RPT; ++k) {
         const int j = slot + k * kSlots;
         if (j < n) {
             const uint16_t* row = bcx + size_t(row_base + j) * TF_CIN + c;
@@ -140,9 +151,9 @@ conv_rows_kernel(SegTable t, int layer, const uint16_t* __restrict__ bcx,
     }
     pdl_trigger();
 
-    uint4 bx[2];
+    uint4 bx[RPT];
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < RPT; ++k) {
         const int j = slot + k * kSlots;
         if (j < n) {
             bx[k] = gate8(B[k], X[k]);
@@ -151,7 +162,7 @@ conv_rows_kernel(SegTable t, int layer, const uint16_t* __restrict__ bcx,
     }
     __syncthreads();   // every entry of the tile is in; every read of the old state is done
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < RPT; ++k) {
         const int j = slot + k * kSlots;
         if (j < n) {
             const uint4 e0 = j >= 2 ? sbx[j - 2][grp] : (j == 1 ? pm1 : pm2);
@@ -191,7 +202,15 @@ extern "C" int tf_conv_rows(const tf_segments* seg, int conv_layer, const void* 
     if (conv_layer < 0 || conv_layer >= t.n_conv) return TF_EINVAL;
     if (t.R == 0) return TF_OK;
     if (!bcx || !w || !y || !aligned16(bcx) || !aligned16(w) || !aligned16(y)) return TF_EINVAL;
-    dim3 grid(t.n_tiles, TF_H / kChanPerCta);
-    return launch_pdl(conv_rows_kernel, grid, dim3(kThreads), 0, stream, t, conv_layer,
-                      static_cast<const uint16_t*>(bcx), static_cast<const uint16_t*>(w), y);
+    const uint16_t* in = static_cast<const uint16_t*>(bcx);
+    const uint16_t* wt = static_cast<const uint16_t*>(w);
+    // tiles of two rows or more on average, and few of them: one row per
+    // thread over 256 channels a CTA (twice the CTAs, half the serial work;
+    // measured faster while the grid stays within two CTAs per SM); else two
+    // rows per thread over 512 channels
+    if (t.R >= 2 * t.n_tiles && t.n_tiles * (TF_H / Split<1>::kChanPerCta) <= 2 * sm_count())
+        return launch_pdl(conv_rows_kernel<1>, dim3(t.n_tiles, TF_H / Split<1>::kChanPerCta), dim3(kThreads), 0,
+                          stream, t, conv_layer, in, wt, y);
+    return launch_pdl(conv_rows_kernel<2>, dim3(t.n_tiles, TF_H / Split<2>::kChanPerCta), dim3(kThreads), 0,
+                      stream, t, conv_layer, in, wt, y);
 }
