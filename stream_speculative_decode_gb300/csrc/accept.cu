@@ -12,8 +12,10 @@
 // never matches and is reported. The conv state of every layer is rewound to
 // history rows a+1, a+2 -- the state after row a.
 //
-// One CTA per (stream, conv layer); every CTA recomputes the (tiny) prefix
-// length, CTAs of layer 0 write the per-stream results.
+// One CTA per (stream, conv layer); every warp finds the prefix length in one
+// round trip (lane j tests draft j + 1, a ballot gives the first rejected
+// one: windows hold at most 16 rows), CTAs of layer 0 write the per-stream
+// results.
 #include "tf_internal.cuh"
 
 namespace tf {
@@ -32,17 +34,17 @@ accept_kernel(SegTable t, const int32_t* __restrict__ ids, const int32_t* __rest
     pdl_wait();
     pdl_trigger();
 
-    int sf = 0;
-    for (int j = 1; j < st.rows; ++j) {
-        const int d = ids[o + j];
-        if (d < 0 || d >= vocab) sf |= 2;
+    const int lane = threadIdx.x & 31;
+    bool ok = false, bad = false;
+    if (lane < st.rows - 1) {   // draft lane + 1 against the pick of row lane
+        const int d = ids[o + lane + 1];
+        bad = d < 0 || d >= vocab;
+        ok = !bad && !flag[o + lane] && pick[o + lane] == d;
     }
-    int a = 0;
-    while (a < st.rows - 1) {
-        const int d = ids[o + a + 1];
-        if (d < 0 || d >= vocab || flag[o + a] || pick[o + a] != d) break;
-        ++a;
-    }
+    const unsigned ok_mask = __ballot_sync(0xFFFFFFFFu, ok);
+    const unsigned bad_mask = __ballot_sync(0xFFFFFFFFu, bad);
+    const int a = __ffs(~ok_mask) - 1;   // accepted drafts: the leading run (lane rows-1 is never ok)
+    int sf = bad_mask ? 2 : 0;
     if (layer == 0 && threadIdx.x == 0) {
         int nxt = pick[o + a];
         if (flag[o + a]) {
