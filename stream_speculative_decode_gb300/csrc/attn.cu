@@ -394,7 +394,7 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
     }
     if (mode == kMergeLastCta) {
         __shared__ int last_flag;
-        finish_last_cta<16>(t, layer, item.stream, st, g, part_o, part_ml, out, &last_flag);
+        finish_last_cta<MT == 1 ? 8 : 16>(t, layer, item.stream, st, g, part_o, part_ml, out, &last_flag);
     }
 }
 
