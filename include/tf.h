@@ -177,7 +177,9 @@ int tf_conv_rows(const tf_segments* seg, int conv_layer, const void* bcx,
  * stream's bits do not depend on its round), and a round holding both kinds
  * makes one launch of each (tf_plan.attn_kernels). The environment variable
  * TF_ATTN_PATH=mma|tc, read by tf_segments_build, forces one kernel for every
- * stream. Values of V must lie within fp16's range (|v| < 65504): P.V runs in
+ * window of at most 16 rows (a prompt table's wider windows always run on the
+ * tensor cores); the mma.sync kernel takes a window as items of at most 8
+ * rows. Values of V must lie within fp16's range (|v| < 65504): P.V runs in
  * fp16 with fp32 accumulation.
  *   q         bf16 [R][TF_NQ][TF_D]
  *   partials  device scratch of tf_partials_bytes(seg) bytes. Record of
