@@ -5,12 +5,14 @@
 // attn.cu (PR #1377 "LFM2: shared-round decode": one launch a layer over every
 // row from the segment table, per-stream partials; PR #1391: causal count),
 // used when a window holds 13 rows or more, where q.K and P.V are real
-// contractions (4*rows flops per byte of K/V each) and the mma.sync kernel
-// would need a fourth 16-row query tile. With `full` set it is the
+// contractions (4*rows flops per byte of K/V each) and this kernel measured
+// faster than the mma.sync one (which would take such a window as two 8-row
+// items reading the chunk twice). With `full` set it is the
 // drafter's non-causal block attention (PR #1391: every block row sees the
 // keys [0, len + 1)): only the per-row key bounds change.
 //
-// One CTA per (work item = one stream's key chunk, KV head), 7 warps:
+// Persistent (at most two CTAs per SM, each running (key chunk, KV head)
+// units back to back; see the kernel), 7 warps:
 //   warp 6, lane 0   TMA loads of K/V tiles (64 keys = 8 KB each, 128-byte
 //                    swizzle) into a 5-stage ring, refilling a stage as soon
 //                    as the P.V that read it completes;
@@ -28,7 +30,9 @@
 //   softmax        thread = query row: the 64 scores in registers (one TMEM
 //                  load), row max, lazy rescale of O (only when the max rises
 //                  more than 2^8), p = 2^(s*log2e/8 - m) packed to fp16 in
-//                  place of S;
+//                  place of S; windows of at most 16 rows run it dual (two
+//                  lanes per query row, 32 keys each, the row's two O
+//                  halves added at the end);
 //   O += P V       A = P (fp16, tensor memory), B = V tile (fp16, smem,
 //                  MN-major), fp32 accumulate.
 // S/P has three buffers, so the q.K of tile j waits only for the P.V of
