@@ -10,14 +10,14 @@
 //
 // Partials kernel: one CTA per (work item = stream key chunk and group of at
 // most 8 window rows, KV head). The chunk length depends on the stream alone
-// (256 * rows keys), so a stream's partials do not depend on the other streams
-// of the round. The CTA streams the chunk's K and V (64 keys a stage, 4-stage
-// cp.async pipeline into XOR-swizzled shared memory) once, for the group's
-// query rows of the KV head (GQA: query head h reads KV head h/4) -- a window
-// of up to 8 rows shares one read of the cache; a wider one reads it once per
-// group, the later groups from L2. Four warps split each stage's keys (16 each); every warp keeps an
-// online softmax over its keys for all query rows; the warps are combined at
-// the end. q.k runs on bf16 tensor-core MMAs with fp32 accumulation (exact
+// (tf_chunk_keys: 256 * max(rows, 4) keys here), so a stream's partials do not
+// depend on the other streams of the round. The CTA streams the chunk's K and
+// V (64 keys a stage, 4-stage cp.async pipeline into XOR-swizzled shared
+// memory) once, for the group's query rows of the KV head (GQA: query head h
+// reads KV head h/4) -- a window of up to 8 rows shares one read of the
+// cache; a wider one reads it once per group, the later groups from L2. Four
+// warps split each stage's keys (16 each); every warp keeps an online softmax
+// over its keys for all query rows; the warps are combined at the end. q.k runs on bf16 tensor-core MMAs with fp32 accumulation (exact
 // products); P.V runs with P and V in fp16 (V's bf16 values convert exactly
 // within fp16's range) and fp32 accumulation.
 //

@@ -1,7 +1,9 @@
 // The drafter's Markov head on the 5th-generation tensor cores: per block row,
 // score[v] = bf16(base[v] + bf16(W2[v] . W1[tok])) over the vocabulary and the
-// lowest token of the largest score, one step (one block row of every stream)
-// per launch.
+// lowest token of the largest score, step after step (one block row of every
+// stream a step): the whole chain in one cooperative launch for tables of up
+// to 128 streams (markov_chain_kernel, at the end of this file), else one
+// launch a step (markov_step_kernel, described here).
 //
 // PR #1391 "lfm2: draft with LiquidAI's DSpark drafter (--drafter)": the head
 // "adds W2 W1[previous token] to each row's logits and takes the argmax, one
