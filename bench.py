@@ -6,12 +6,16 @@ greedy pick (tf_argmax_rows) and the accept step (tf_accept), captured in one
 CUDA graph. Metric: verified rows per second (rows of every stream's window,
 all ranks) and the achieved HBM bandwidth.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..6] [--impl tf|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..6] [--per-config 3,4,5,6]
+                    [--impl tf|reference]
     python bench.py --row markov|block [--workload 3|5] [--steps K] [--warmup W]
 
-Default workload: 16 streams of one row, 30 conv + 10 attention layers, key
-counts uniform in [256, 4096] (the plain shared round). The other workloads
-(1, 3, 4, 5, and 6: workload 5 with its rows not rescaled) are selectable.
+Default workload: 64 streams of 16-row windows (1,024 rows), 30 conv + 10
+attention layers, key counts log-uniform on [16, 32768]: the largest workload
+by rows. The other workloads (1-4, and 6: workload 5 with its rows not
+rescaled) are selectable. The same run also times workloads 3, 4, 5 and 6
+(``--per-config``), each with its own inputs, table and graph, and reports
+them under ``per_config`` (step time, rows/s, HBM fraction, attention fraction).
 ``--impl reference`` times the float64 CPU oracle on the host cores (one
 process per core) on a bounded sample of the same workload.
 
@@ -67,10 +71,13 @@ class L2Flush:
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", type=int, default=None, choices=[1, 2, 3, 4, 5, 6],
-                    help="default 2 for the verify step, 5 for --row")
+    ap.add_argument("--workload", type=int, default=5, choices=[1, 2, 3, 4, 5, 6],
+                    help="the headline workload (default 5: 64 streams x 16 rows, the largest by rows)")
+    ap.add_argument("--per-config", default="3,4,5,6",
+                    help="workloads also timed in the same run (own inputs, table and graph each), "
+                         "comma-separated; empty for none")
     ap.add_argument("--row", default="verify", choices=["verify", "markov", "block", "prompt"])
     ap.add_argument("--prompt-rows", type=int, default=2048, help="--row prompt: rows of the prompt chunk")
     ap.add_argument("--prompt-cached", type=int, default=14336, help="--row prompt: keys cached before it")
@@ -83,8 +90,7 @@ def parse():
     ap.add_argument("--conv-layers", type=int, default=None, help="override (small profiling runs)")
     ap.add_argument("--attn-layers", type=int, default=None, help="override (small profiling runs)")
     args = ap.parse_args()
-    if args.workload is None:
-        args.workload = 2 if args.row == "verify" else 5
+    args.per_config = [int(x) for x in args.per_config.split(",") if x.strip()]
     return args
 
 
@@ -131,7 +137,7 @@ def aggregate(rows_per_rank, ms_local, world, device="cpu"):
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons every 50 ms."""
+    """nvidia-smi samples of SM clock and throttle reasons every 20 ms."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -147,7 +153,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, ValueError):
             self.proc = None
@@ -280,43 +286,62 @@ def recorded_traffic(workload_index):
     return None if ent is None else float(ent["dram_bytes_per_launch"])
 
 
-def oracle_child(workload_index, n_streams, attn_rows, repeats):
-    """(Child process.) Time the oracle on a bounded sample of the workload and
-    scale it to one whole step: one conv layer over the first ``n_streams``
-    streams, one attention layer over the first ``attn_rows`` window rows of
-    the first stream (all 32 heads), and the greedy pick plus accept over the
-    sampled streams' rows. Each part is scaled by its work: conv and pick by
-    rows, attention by visible keys summed over rows; then times the layer
-    counts of the workload. Prints JSON with the per-repeat step estimates."""
+def _units(w, parts):
+    """The work of one conv + one attention layer and the head, split over
+    ``parts`` processes: conv and head by stream (stream s to part s % parts);
+    attention by stream when there are at least as many streams as parts, else
+    by (stream, window row) pair, the pairs dealt out in turn."""
+    S = len(w.rows)
+    if S >= parts:
+        attn = [[(s, None) for s in range(S) if s % parts == p] for p in range(parts)]
+    else:
+        pairs = [(s, i) for s in range(S) for i in range(w.rows[s])]
+        attn = [pairs[p::parts] for p in range(parts)]
+    conv = [[s for s in range(S) if s % parts == p] for p in range(parts)]
+    return conv, attn
+
+
+def oracle_child(workload_index, part, parts, repeats):
+    """(Child process.) Time part ``part`` of ``parts`` of one whole conv layer,
+    one whole attention layer and the head (greedy pick + accept) of the
+    workload on the oracle (``_units`` says which streams and rows). Inputs are
+    drawn for the streams this part touches (same shapes and distributions as
+    the workload's). Prints JSON with per-repeat seconds of each part."""
     import json as _json
     from stream_speculative_decode_gb300 import inputs as I
     from oracle import step as O
     w = I.workload(workload_index)
-    sub = I.Workload("sample", w.rows[:n_streams], w.keys[:n_streams], 1, 1, vocab=w.vocab,
-                     drafts=w.drafts, tie_rows=min(w.tie_rows, 1), nan_rows=min(w.nan_rows, 1),
-                     inf_frac=w.inf_frac, seed=w.seed)
-    inp = I.make_inputs(sub, backend="numpy")
-    R_full = sum(w.rows)
-    R_s = sum(sub.rows)
-    vis = lambda k, r, i: k - r + i + 1
-    A_full = sum(vis(k, r, i) for r, k in zip(w.rows, w.keys) for i in range(r))
-    r0, k0 = w.rows[0], w.keys[0]
-    ar = min(attn_rows, r0)
-    A_s = sum(vis(k0, r0, i) for i in range(ar))
-    est = []
-    for _ in range(repeats):
-        t0 = time.perf_counter()
-        O.conv_layer(inp.streams, inp.bcx[0], inp.w[0], inp.state[0])
-        t1 = time.perf_counter()
-        for i in range(ar):
-            O.attention_stream(inp.q[0][i:i + 1], inp.K[0][0], inp.V[0][0], vis(k0, r0, i), 1)
-        t2 = time.perf_counter()
-        pick, flag = O.argmax_rows(inp.logits)
-        O.accept_all(inp.streams, inp.ids, pick, flag, w.vocab)
-        t3 = time.perf_counter()
-        est.append(w.n_conv * (t1 - t0) * R_full / R_s + w.n_attn * (t2 - t1) * A_full / A_s
-                   + (t3 - t2) * R_full / R_s)
-    print(_json.dumps(dict(step_s=est, rows=R_full)))
+    conv_u, attn_u = _units(w, parts)
+    mine_c, mine_a = conv_u[part], attn_u[part]
+    touched = sorted(set(mine_c) | {s for s, _ in mine_a})
+    res = dict(conv=[0.0] * repeats, attn=[0.0] * repeats, head=[0.0] * repeats, rows=sum(w.rows))
+    if touched:
+        sub = I.Workload("sample", [w.rows[s] for s in touched], [w.keys[s] for s in touched], 1, 1,
+                         vocab=w.vocab, drafts=w.drafts, inf_frac=w.inf_frac, seed=w.seed)
+        inp = I.make_inputs(sub, backend="numpy")
+        j_of = {s: j for j, s in enumerate(touched)}
+        for k in range(repeats):
+            t0 = time.perf_counter()
+            for s in mine_c:
+                r, off, _ = inp.streams[j_of[s]]
+                O.short_conv_stream(inp.bcx[0][off:off + r], inp.w[0], inp.state[0][j_of[s]])
+            t1 = time.perf_counter()
+            for s, i in mine_a:
+                j = j_of[s]
+                r, off, keys = inp.streams[j]
+                if i is None:    # the stream's whole window
+                    O.attention_stream(inp.q[0][off:off + r], inp.K[0][j], inp.V[0][j], keys, r)
+                else:            # one window row: its causal count of keys
+                    O.attention_stream(inp.q[0][off + i:off + i + 1], inp.K[0][j], inp.V[0][j],
+                                       keys - r + i + 1, 1)
+            t2 = time.perf_counter()
+            for s in mine_c:
+                r, off, keys = inp.streams[j_of[s]]
+                pick, flag = O.argmax_rows(inp.logits[off:off + r])
+                O.accept_stream(inp.ids[off:off + r], pick, flag, r, keys, w.vocab)
+            t3 = time.perf_counter()
+            res["conv"][k], res["attn"][k], res["head"][k] = t1 - t0, t2 - t1, t3 - t2
+    print(_json.dumps(res))
 
 
 def host_cores():
@@ -327,42 +352,41 @@ def host_cores():
 
 
 def oracle_sample(workload_index, repeats, procs=1):
-    """Run ``oracle_child`` in ``procs`` fresh child processes at once, one
-    BLAS thread each (the step's work is independent per stream and layer, so
-    the host's throughput is the sum of theirs). Returns, per repeat, the step
-    time at the summed throughput, and the rows of a step."""
-    n, ar = SAMPLE[workload_index]
-    code = (f"import sys; sys.path.insert(0, {ROOT!r}); import bench; "
-            f"bench.oracle_child({workload_index}, {n}, {ar}, {repeats})")
+    """One whole conv layer, one whole attention layer and the head of the
+    workload on the oracle, split over ``procs`` fresh child processes that run
+    at once (one BLAS thread each). Per repeat the step time is the layer
+    counts times the slowest part of each layer, plus the slowest head part.
+    Returns (per-repeat step seconds, rows of a step)."""
+    from stream_speculative_decode_gb300 import inputs as I
+    w = I.workload(workload_index)
     env = dict(os.environ)
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NUMEXPR_NUM_THREADS"):
         env[v] = "1"
-    kids = [subprocess.Popen([sys.executable, "-c", code], env=env, stdout=subprocess.PIPE,
-                             stderr=subprocess.PIPE, text=True) for _ in range(procs)]
+    kids = []
+    for p in range(procs):
+        code = (f"import sys; sys.path.insert(0, {ROOT!r}); import bench; "
+                f"bench.oracle_child({workload_index}, {p}, {procs}, {repeats})")
+        kids.append(subprocess.Popen([sys.executable, "-c", code], env=env, stdout=subprocess.PIPE,
+                                     stderr=subprocess.PIPE, text=True))
     outs = []
     for k in kids:
         so, se = k.communicate(timeout=3600)
         if k.returncode != 0:
             raise RuntimeError("oracle sample failed: " + se[-2000:])
         outs.append(json.loads(so.strip().splitlines()[-1]))
-    rows = outs[0]["rows"]
-    per_repeat = [rows / sum(rows / o["step_s"][j] for o in outs) for j in range(repeats)]
-    return per_repeat, rows
+    per_repeat = [w.n_conv * max(o["conv"][j] for o in outs) + w.n_attn * max(o["attn"][j] for o in outs)
+                  + max(o["head"][j] for o in outs) for j in range(repeats)]
+    return per_repeat, outs[0]["rows"]
 
 
-# streams in the conv / pick sample, window rows in the attention sample
-SAMPLE = {1: (1, 4), 2: (4, 1), 3: (2, 2), 4: (1, 1), 5: (2, 2), 6: (2, 2)}
-
-
-def sample_desc(w, index, procs=1):
-    n, ar = SAMPLE[index]
-    par = (f"{procs} processes at once (one per host core), one BLAS thread each, their throughputs summed"
-           if procs > 1 else "1 process, 1 BLAS thread")
-    return (f"float64 numpy oracle, {par}: one conv layer over the first {n} of {len(w.rows)} "
-            f"streams, one attention layer over {min(ar, w.rows[0])} window row(s) of stream 0 "
-            f"({w.keys[0]} keys, 32 heads), pick + accept over the sampled rows; each part scaled "
-            f"to the whole step ({w.n_conv} conv + {w.n_attn} attention layers, {sum(w.rows)} rows) "
-            f"by rows or by visible keys")
+def sample_desc(w, procs=1):
+    par = (f"split over {procs} processes running at once (one per host core, one BLAS thread each; "
+           f"conv and head by stream, attention by stream or, with fewer streams than processes, by "
+           f"window row)" if procs > 1 else "1 process, 1 BLAS thread")
+    return (f"float64 numpy oracle, {par}: one whole conv layer and one whole attention layer over all "
+            f"{len(w.rows)} streams ({sum(w.rows)} rows, {sum(w.keys)} keys), then the greedy pick + accept; "
+            f"step = {w.n_conv} x conv layer + {w.n_attn} x attention layer + head, each layer's time that "
+            f"of its slowest process")
 
 
 # -------------------------------------------------------------- arms
@@ -383,7 +407,7 @@ def run_reference(args, rank, world):
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(w),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": procs, "kind": "oracle",
-                         "sample": sample_desc(w, args.workload, procs)},
+                         "sample": sample_desc(w, procs)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -394,6 +418,72 @@ def workload_config(w):
     return {"workload": w.name, "streams": len(w.rows), "rows": sum(w.rows), "keys_total": sum(w.keys),
             "conv_layers": w.n_conv, "attn_layers": w.n_attn, "vocab": w.vocab,
             "widths": "H=2048, conv in 6144 (B,C,x), kw=3, 32 q / 8 kv heads, d=64"}
+
+
+def attn_b2b_ms(torch, d, n_attn, flush, stream, dev, replays):
+    """Median duration of one attention call with the step's attention calls
+    back to back: a graph of the step's attention layers alone, replayed with
+    the L2 flushed before each replay, one event pair per replay on the launch
+    stream; the median replay over the layers."""
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(cap):
+        with torch.cuda.graph(g, stream=cap):
+            for l in range(n_attn):
+                d.attn(l, torch.cuda.current_stream(dev))
+    stream.wait_stream(cap)
+    ts = []
+    for _ in range(replays):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) / n_attn)
+    return statistics.median(ts)
+
+
+def attn_alg_bytes(streams, R):
+    """One attention call: every stream's K and V (bf16), the queries in
+    (bf16), the output out (fp32)."""
+    return sum(k for _, _, k in streams) * 8 * 64 * 2 * 2 + R * 32 * 64 * (2 + 4)
+
+
+def measure_workload(torch, index, steps, warmup, flush, stream, dev, world, clocks, peak):
+    """One workload's step (its own inputs, table and graph), timed like the
+    headline: W warm-up replays, then K replays with the L2 flushed before
+    each. Returns the per-config record; frees everything it allocated."""
+    from stream_speculative_decode_gb300 import inputs as I
+    from stream_speculative_decode_gb300.step import DeviceStep, algorithmic_bytes
+    w = I.workload(index)
+    inp = I.make_inputs(w, backend="torch", device=dev)
+    d = DeviceStep(inp, device=dev)
+    ab = algorithmic_bytes(inp.streams, w.n_conv, w.n_attn, w.vocab)
+    d.run()
+    torch.cuda.synchronize()
+    d.capture()
+    for _ in range(warmup):
+        flush()
+        d.graph.replay()
+    torch.cuda.synchronize()
+    step_ms, w0, w1, remeasured = timed_replays(torch, d.graph.replay, flush, steps, stream, world, clocks)
+    ms = sum(step_ms) / len(step_ms)
+    b2b = attn_b2b_ms(torch, d, w.n_attn, flush, stream, dev, min(steps, 50))
+    attn_alg = attn_alg_bytes(inp.streams, inp.R)
+    cs = clocks.summary(w0, w1)
+    rec = {"workload": w.name, "rows": inp.R, "streams": len(w.rows), "steps": steps, "warmup": warmup,
+           "ms_per_step": ms, "rows_s": inp.R / (ms * 1e-3),
+           "step_algorithmic_bytes": ab["total"], "hbm_gbs": ab["total"] / (ms * 1e-3) / 1e9,
+           "hbm_frac": ab["total"] / (ms * 1e-3) / 1e9 / peak,
+           "attn_ms_back_to_back": b2b, "attn_frac": attn_alg / (b2b * 1e-3) / 1e9 / peak,
+           "attn_launches_per_call": d.seg.plan["attn_kernels"] + d.seg.plan["attn_merge_launch"],
+           "clocks": dict(cs or {}, remeasured=remeasured)}
+    d.free()
+    del d, inp
+    torch.cuda.empty_cache()
+    return rec
 
 
 def run_tf(args, rank, world):
@@ -445,38 +535,18 @@ def run_tf(args, rank, world):
     # L2 flushed between timed steps (outside the events)
     step_ms, t_wall0, t_wall1, remeasured = timed_replays(torch, d.graph.replay, flush, args.steps, stream, world,
                                                           clocks)
+    clocks_sum = clocks.summary(t_wall0, t_wall1)
+    if clocks_sum is not None:
+        clocks_sum["remeasured"] = remeasured
     if graph_events:                        # the attention calls, timed inside the step
         for _ in range(args.steps):
             flush()
             g_ev.replay()
             torch.cuda.synchronize()
             part_ms.extend(a.elapsed_time(b) for a, b in evs["attn"])
-    # the same attention calls back to back (a graph of the step's attention
-    # layers alone, no event between them): the call's duration when the
-    # launches overlap as they do in the step
-    b2b_ms = None
-    if w.n_attn > 0:
-        cap = torch.cuda.Stream(device=dev)
-        cap.wait_stream(stream)
-        g_b2b = torch.cuda.CUDAGraph()
-        with torch.cuda.stream(cap):
-            with torch.cuda.graph(g_b2b, stream=cap):
-                for l in range(w.n_attn):
-                    d.attn(l, torch.cuda.current_stream(dev))
-        stream.wait_stream(cap)
-        ts = []
-        for _ in range(min(args.steps, 50)):
-            flush()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            g_b2b.replay()
-            b.record(stream)
-            torch.cuda.synchronize()
-            ts.append(a.elapsed_time(b) / w.n_attn)
-        b2b_ms = statistics.median(ts)
-    clocks_sum = clocks.summary(t_wall0, t_wall1)
-    if clocks_sum is not None:
-        clocks_sum["remeasured"] = remeasured
+    # the same attention calls back to back (no event between them): the
+    # call's duration when the launches overlap as they do in the step
+    b2b_ms = attn_b2b_ms(torch, d, w.n_attn, flush, stream, dev, min(args.steps, 50)) if w.n_attn > 0 else None
     ms = sum(step_ms) / len(step_ms)
     value, ms_max = aggregate(R, ms, world, device=dev)
 
@@ -491,11 +561,9 @@ def run_tf(args, rank, world):
                 b.record(stream)
                 torch.cuda.synchronize()
                 part_ms.append(a.elapsed_time(b))
-    clocks.stop()
 
     peak, peak_kind = measured_peaks()
-    # one attention call: every stream's K and V (bf16), the queries in (bf16), the output out (fp32)
-    attn_alg = sum(k for _, _, k in inp.streams) * 8 * 64 * 2 * 2 + R * 32 * 64 * (2 + 4)
+    attn_alg = attn_alg_bytes(inp.streams, R)
     part_avg_ms = sum(part_ms) / len(part_ms) if part_ms else float("nan")
     achieved = attn_alg / (part_avg_ms * 1e-3) / 1e9
     if b2b_ms is None:   # no attention layer
@@ -507,17 +575,33 @@ def run_tf(args, rank, world):
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(d, args, stream, flush, ab["total"])
+    attn_launches = d.seg.plan["attn_kernels"] + d.seg.plan["attn_merge_launch"]
+    launches = d.launches_per_step() * args.steps
+    d.free()
+    del d, inp, g_ev
+    torch.cuda.empty_cache()
+
+    # the other multi-layer workloads of the target set, each in its own run
+    # of the same timing (more steps than the headline where K is small, so
+    # that the clock record covers each)
+    per_config = {}
+    if args.per_config and args.conv_layers is None and args.attn_layers is None:
+        pc_steps = max(args.steps, 200)
+        for idx in args.per_config:
+            per_config[str(idx)] = measure_workload(torch, idx, pc_steps, max(args.warmup, 3), flush, stream, dev,
+                                                    world, clocks, peak)
+    clocks.stop()
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and world == 1:
-        times1, rows = oracle_sample(args.workload, 3)
         procs = host_cores()
+        times1, rows = oracle_sample(args.workload, 1)
         timesn, _ = oracle_sample(args.workload, 3, procs) if procs > 1 else (times1, rows)
         sec1 = sum(times1) / len(times1)
         secn = sum(timesn) / len(timesn)
         cpu = {"value": rows / secn, "unit": UNIT, "cores": procs, "kind": "oracle",
-               "sample": sample_desc(w, args.workload, procs) + "; mean of 3 samples",
-               "single_core": {"value": rows / sec1, "cores": 1}}
+               "sample": sample_desc(w, procs) + "; mean of 3 repeats",
+               "single_core": {"value": rows / sec1, "cores": 1, "sample": sample_desc(w, 1) + "; one repeat"}}
 
     step_gbs = ab["total"] / (ms_max * 1e-3) / 1e9
     line = {
@@ -532,7 +616,7 @@ def run_tf(args, rank, world):
                      "achieved": b2b_achieved, "peak": peak,
                      "unit": "GB/s", "frac": b2b_achieved / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": attn_alg, "avg_launch_ms": b2b_ms,
-                     "launches_per_call": d.seg.plan["attn_kernels"] + d.seg.plan["attn_merge_launch"],
+                     "launches_per_call": attn_launches,
                      "peak_kind": peak_kind,
                      "timing": "the step's attention calls back to back: a graph of the step's attention layers "
                                "alone, replayed after the timed region with the L2 flushed between replays, one "
@@ -547,13 +631,13 @@ def run_tf(args, rank, world):
                                          "CUDA events around eager launches after the timed region"}},
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": d.launches_per_step() * args.steps,
+        "gpu_launches": launches,
         "clocks": clocks_sum,
         "wall_s_timed": t_wall1 - t_wall0,
+        "per_config": per_config,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
-    d.free()
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

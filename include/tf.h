@@ -252,7 +252,8 @@ int tf_attn_static(const tf_segments* seg, int attn_layer, const void* q, float*
  *   flag        uint8 [R]: 1 if the row holds a NaN, +Inf or -Inf, else 0
  * Needs no table. R == 0 is a no-op. Errors: TF_EINVAL (null, V < 1,
  * row_stride < V), TF_ERANGE (V > 2^30, R > 2^24). Rows are read with 16-byte
- * vector loads when logits and row_stride allow it. */
+ * vector loads when logits and row_stride allow it. One launch takes at most
+ * 65,535 rows (the grid's y extent); larger R runs as several launches. */
 int tf_argmax_rows(const void* logits, int R, int V, int64_t row_stride,
                    int32_t* pick, uint8_t* flag, tf_cuda_stream stream);
 

@@ -172,7 +172,6 @@ extern "C" int tf_argmax_rows(const void* logits, int R, int V, int64_t row_stri
     if (R == 0) return TF_OK;
     if (!logits || !pick || !flag || V < 1 || row_stride < V) return TF_EINVAL;
     if (V > (1 << 30) || R > (1 << 24)) return TF_ERANGE;
-    if (R > 65535) return TF_ERANGE;   // grid.y limit
     const bool vec = aligned16(logits) && (row_stride % 8) == 0;
     // CTAs per row: enough to fill every SM about 8 CTAs deep, at most 8
     const int target = sm_count() * 8;
@@ -183,8 +182,9 @@ extern "C" int tf_argmax_rows(const void* logits, int R, int V, int64_t row_stri
     cl = (V + chunk - 1) / chunk;   // no empty CTA
     if (cl < 1) cl = 1;
 
+    // rows go in grid.y, at most 65,535 a launch: larger R takes several launches
+    constexpr int kRowsPerLaunch = 65535;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(cl, R, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
@@ -197,9 +197,17 @@ extern "C" int tf_argmax_rows(const void* logits, int R, int V, int64_t row_stri
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    const uint16_t* lg = static_cast<const uint16_t*>(logits);
-    cudaError_t e = vec ? cudaLaunchKernelEx(&cfg, argmax_rows_kernel<true>, lg, V, row_stride, chunk, pick, flag)
-                        : cudaLaunchKernelEx(&cfg, argmax_rows_kernel<false>, lg, V, row_stride, chunk, pick, flag);
-    if (e != cudaSuccess) return cuda_fail(e);
-    return launch_status();
+    for (int r0 = 0; r0 < R; r0 += kRowsPerLaunch) {
+        const int nr = R - r0 < kRowsPerLaunch ? R - r0 : kRowsPerLaunch;
+        cfg.gridDim = dim3(cl, nr, 1);
+        const uint16_t* lg = static_cast<const uint16_t*>(logits) + size_t(r0) * size_t(row_stride);
+        int32_t* pk = pick + r0;
+        uint8_t* fl = flag + r0;
+        cudaError_t e = vec ? cudaLaunchKernelEx(&cfg, argmax_rows_kernel<true>, lg, V, row_stride, chunk, pk, fl)
+                            : cudaLaunchKernelEx(&cfg, argmax_rows_kernel<false>, lg, V, row_stride, chunk, pk, fl);
+        if (e != cudaSuccess) return cuda_fail(e);
+        const int st = launch_status();
+        if (st != TF_OK) return st;
+    }
+    return TF_OK;
 }

@@ -72,6 +72,7 @@ def test_argmax_golden_rows(mods):
     (4, 128000, 128003, 0),     # stride not a multiple of 8: scalar path
     (4, 5000, None, 3),         # unaligned base: scalar path
     (2, 70001, 70008, 0),       # ragged tail on the vector path
+    (70000, 24, None, 0),       # more rows than one launch's grid.y (65,535): two launches
 ])
 def test_argmax_random(mods, R, V, stride, offset):
     rng = np.random.default_rng(R * 1000 + V)
