@@ -66,7 +66,8 @@ typedef enum {
     TF_EINVAL = 1,   /* null pointer, bad shape, unpacked rows, aliasing, misalignment */
     TF_ERANGE = 2,   /* a size beyond the limits above */
     TF_ENOMEM = 3,   /* the library's own table allocation failed */
-    TF_ECUDA = 4     /* a CUDA call or launch failed (see tf_last_cuda_error) */
+    TF_ECUDA = 4,    /* a CUDA call or launch failed (see tf_last_cuda_error) */
+    TF_ETIMEOUT = 5  /* a kernel gave up a bounded device wait (tf_segments_status) */
 } tf_status;
 
 struct CUstream_st;                       /* cudaStream_t is struct CUstream_st* */
@@ -350,6 +351,46 @@ int tf_prompt_build(int32_t rows, int32_t keys, int32_t kv_capacity,
                     const void* const* conv_state, const void* const* k_cache,
                     const void* const* v_cache, int n_conv, int n_attn,
                     tf_cuda_stream stream, tf_segments** out);
+
+/* ---- failures on the device ------------------------------------------------
+ * The tensor-core attention kernel (tf_attn*, streams of 13 rows or more and
+ * prompt windows) and the Markov chain (tf_markov_chain) wait on barriers
+ * that other warps or CTAs of the same launch complete. Every such wait is
+ * bounded by the wait limit below. A CTA whose wait runs out gives up: it
+ * lets its own copies and MMAs in flight land, writes NaN in place of the
+ * results it could not compute (attention records; Markov rows get pick -1
+ * and flag bit 1), sets a bit in the table's status word and returns. Nothing
+ * faults and the context stays usable; the launch itself still reports
+ * success, so the failure is read with tf_segments_status. No library
+ * counterpart on the pages' side: the pages' Metal kernels have no device
+ * waits of this kind.
+ *
+ * tf_set_wait_limit_ns sets the limit (process-wide) for every later launch;
+ * a launch captured in a CUDA graph keeps the limit it was captured with.
+ * Default TF_WAIT_LIMIT_DEFAULT_NS (2 s), at most TF_WAIT_LIMIT_MAX_NS
+ * (TF_ERANGE beyond). 0 makes a kernel give up at the first wait that is
+ * not already complete when first tested: a way to exercise the failure
+ * path, not a setting for real work. tf_wait_limit_ns returns the current
+ * limit. */
+#define TF_WAIT_LIMIT_DEFAULT_NS 2000000000ull
+#define TF_WAIT_LIMIT_MAX_NS 60000000000ull
+int tf_set_wait_limit_ns(uint64_t ns);
+uint64_t tf_wait_limit_ns(void);
+
+/* Status word bits of a table. */
+#define TF_STATUS_ATTN_TIMEOUT   1u   /* the tensor-core attention kernel gave up a wait */
+#define TF_STATUS_MARKOV_TIMEOUT 2u   /* the Markov chain gave up a wait */
+
+/* Read and clear a table's status word. Synchronises `stream` (so it must not
+ * be called during stream capture), copies the word to *bits (if bits is not
+ * NULL) and, when it is nonzero, zeroes the table's cross-CTA scratch
+ * (attention merge counters, work counters, Markov step keys and barrier) and
+ * the word itself, so the next calls on the table start clean. No call on the
+ * table may be in flight on another stream meanwhile.
+ * Returns TF_OK (no kernel gave up since the last check), TF_ETIMEOUT (one
+ * did: every result the table's calls wrote since the last check is invalid),
+ * TF_EINVAL (NULL table) or TF_ECUDA. */
+int tf_segments_status(tf_segments* seg, tf_cuda_stream stream, uint32_t* bits);
 
 /* Name of a status code. */
 const char* tf_strerror(int status);

@@ -15,11 +15,11 @@
 // V (64 keys a stage, 4-stage cp.async pipeline into XOR-swizzled shared
 // memory) once, for the group's query rows of the KV head (GQA: query head h
 // reads KV head h/4) -- a window of up to 8 rows shares one read of the
-// cache; a wider one reads it once per group, the later groups from L2. Four
-// warps split each stage's keys (16 each); every warp keeps an online softmax
-// over its keys for all query rows; the warps are combined at the end. q.k runs on bf16 tensor-core MMAs with fp32 accumulation (exact
-// products); P.V runs with P and V in fp16 (V's bf16 values convert exactly
-// within fp16's range) and fp32 accumulation.
+// cache; a wider one reads it once per group, the later groups from L2. The
+// item's arithmetic (attn_item.cuh): four warps split each stage's keys, q.k
+// on bf16 mma.sync with fp32 accumulation, P.V in fp16, and the item
+// recomputed with V in bf16 (exact in V) when the fp16 pass left a partial
+// sum that is not finite or every partial output below 2^-10.
 //
 // HBM bound: 256 bytes of K+V per key per KV head; the window's queries ride
 // along. Arithmetic intensity 4*rows flops per byte for each of q.k and P.V.
@@ -29,69 +29,14 @@
 // keys [0, len + 1)): with `full` set every window row sees all of the
 // stream's keys instead of its causal count; nothing else changes, and the
 // merge is shared (it reads only the records).
-#include "tf_internal.cuh"
+#include "attn_item.cuh"
 
 namespace tf {
 namespace {
 
-constexpr int kKT = 64;                 // keys per stage
-constexpr int kStages = 4;
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kRowB = TF_D * 2;         // 128 bytes per cache row
-constexpr int kStageB = 2 * kKT * kRowB;  // K then V: 16 KB
-constexpr int kOStride = 68;            // floats per row of the warp-combine buffer
-constexpr float kLog2e8 = 0.18033688011112042f;   // log2(e) / sqrt(64)
-constexpr float kTau = 8.f;             // lazy-rescale threshold, log2 units
-
-__host__ __device__ constexpr int smem_bytes(int mt) { return kStages * kStageB + 16 * mt * kRowB; }
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-    const int sz = valid ? 16 : 0;   // 0: fill the 16 bytes with zeros
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(sz));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
-
-__device__ __forceinline__ void ldsm_x4(uint32_t r[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t r[4], uint32_t addr) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
-                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void mma_f16(float d[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
-    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-                 "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
-                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ float ex2(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ uint32_t pack_h2(float a, float b) {
-    __half2 h = __floats2half2_rn(a, b);
-    return *reinterpret_cast<uint32_t*>(&h);
-}
-// two bf16 -> two fp16 (exact for |v| in fp16's normal range)
-__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w) {
-    return pack_h2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
-}
-// byte offset of 16-byte chunk `ch` of row `r` in a swizzled 128-byte-row tile
-__device__ __forceinline__ uint32_t swz(int r, int ch) { return uint32_t(r * kRowB + ((ch ^ (r & 7)) << 4)); }
+using item::kThreads;
+using item::smem_bytes;
+using item::ex2;
 
 // One and two query m-tiles fit three CTAs per SM (<= 170 registers, 66 KB of
 // smem each; measured 12% faster on 6-row windows than two CTAs). Wider
@@ -104,297 +49,30 @@ attn_partials_kernel(SegTable t, int layer, const uint16_t* __restrict__ q,
                      float* __restrict__ part_o, float2* __restrict__ part_ml, float* __restrict__ out,
                      int full) {
     extern __shared__ __align__(128) unsigned char smem[];
-    constexpr bool kQReg = MT <= 2;
-    const int item_idx = blockIdx.x / TF_NKV;
     const int g = blockIdx.x % TF_NKV;
-    const AttnItem item = t.items[item_idx];
-    const SegStream st = t.streams[item.stream];
-    const int nq_all = st.rows * 4;
-    const int q0 = item.q0;                   // the group's first query row (a multiple of 32)
-    const int nq = min(16 * MT, nq_all - q0);   // the group's query rows
-    const int c0 = item.chunk * st.chunk_keys;
-    const int nkeys = min(st.chunk_keys, st.keys - c0);
-    const int nst = (nkeys + kKT - 1) / kKT;
-    const size_t slot = size_t(layer) * t.S + item.stream;
-    const uint16_t* Kg = static_cast<const uint16_t*>(t.k_cache[slot]) + (size_t(g) * st.cap + c0) * TF_D;
-    const uint16_t* Vg = static_cast<const uint16_t*>(t.v_cache[slot]) + (size_t(g) * st.cap + c0) * TF_D;
-    unsigned char* sKV = smem;
-    unsigned char* sQ = smem + kStages * kStageB;
-    const uint32_t sKV32 = smem_u32(sKV), sQ32 = smem_u32(sQ);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const AttnItem it = t.items[blockIdx.x / TF_NKV];
+    const SegStream st = t.streams[it.stream];
     if constexpr (MT == 1) {
         // narrow windows (one m-tile: short launches, one wave): the first
         // stages' keys and values into L2 while the previous kernel finishes
         // (measured 17.0 -> 16.0 us a layer for 16 one-row streams; the
         // two-m-tile kernel spilled with it and ran slower)
-        if (tid == 0) {
-            const uint32_t pre = uint32_t(min(nkeys, (kStages - 1) * kKT)) * kRowB;
-            l2_prefetch_bulk(Kg, pre);
-            l2_prefetch_bulk(Vg, pre);
+        if (threadIdx.x == 0) {
+            const int c0 = it.chunk * st.chunk_keys;
+            const int nkeys = min(st.chunk_keys, st.keys - c0);
+            const size_t slot = size_t(layer) * t.S + it.stream;
+            const size_t off = (size_t(g) * st.cap + c0) * TF_D;
+            const uint32_t pre = uint32_t(min(nkeys, (item::kStages - 1) * item::kKT)) * item::kRowB;
+            l2_prefetch_bulk(static_cast<const uint16_t*>(t.k_cache[slot]) + off, pre);
+            l2_prefetch_bulk(static_cast<const uint16_t*>(t.v_cache[slot]) + off, pre);
         }
     }
     pdl_wait();   // the table above; queries and caches below
-
-    // group query rows qi: q0 + qi = 4*i + hh (window row i, head 4g + hh);
-    // rows past nq are zero
-    for (int idx = tid; idx < 16 * MT * 8; idx += kThreads) {
-        const int qi = idx >> 3, ch = idx & 7;
-        const bool valid = qi < nq;
-        const uint16_t* src =
-            q + ((size_t(st.row_offset + ((q0 + qi) >> 2)) * TF_NQ + 4 * g + (qi & 3)) * TF_D + ch * 8);
-        cp_async16(sQ32 + swz(qi, ch), valid ? src : q, valid);
-    }
-    auto issue = [&](int s) {
-        const uint32_t buf = sKV32 + (s % kStages) * kStageB;
-        const int key0 = s * kKT;
-#pragma unroll
-        for (int k = 0; k < (kKT * 8) / kThreads; ++k) {
-            const int idx = tid + k * kThreads;
-            const int r = idx >> 3, ch = idx & 7;
-            const bool valid = key0 + r < nkeys;
-            const size_t off = size_t(key0 + r) * TF_D + ch * 8;
-            cp_async16(buf + swz(r, ch), valid ? Kg + off : Kg, valid);
-            cp_async16(buf + kKT * kRowB + swz(r, ch), valid ? Vg + off : Vg, valid);
-        }
-    };
-#pragma unroll
-    for (int s = 0; s < kStages - 1; ++s) {
-        if (s < nst) issue(s);
-        cp_async_commit();
-    }
-
-    const int g8 = lane >> 2, t4 = lane & 3;
-    float o[MT][8][4];
-    float m[MT][2], l[MT][2], mtrue[MT][2];   // m: reference max; mtrue: running max
-    int lim[MT][2];
-    // keys every real row of the group sees (chunk-local): its first row's
-    // causal count, or every key for a FULL block
-    const int lim_all = (full ? st.keys : st.keys - st.rows + (q0 >> 2) + 1) - c0;
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-        for (int dt = 0; dt < 8; ++dt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) o[mt][dt][e] = 0.f;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            m[mt][r] = -INFINITY;
-            mtrue[mt][r] = -INFINITY;
-            l[mt][r] = 0.f;
-            const int qi = mt * 16 + g8 + 8 * r;
-            // chunk-local bound of the keys row qi/4 sees (causal, or all keys
-            // for a FULL block), 0 for padding rows
-            const int vis = (full ? st.keys : st.keys - st.rows + ((q0 + qi) >> 2) + 1) - c0;
-            lim[mt][r] = qi < nq ? max(0, min(vis, nkeys)) : 0;
-        }
-    }
-    uint32_t qf[kQReg ? MT : 1][4][4];
-
-    for (int it = 0; it < nst; ++it) {
-        if (it + kStages - 1 < nst) issue(it + kStages - 1);
-        cp_async_commit();
-        cp_async_wait<kStages - 1>();
-        __syncthreads();
-        if (kQReg && it == 0) {
-#pragma unroll
-            for (int mt = 0; mt < (kQReg ? MT : 0); ++mt)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const int mi = lane >> 3;
-                    const int row = mt * 16 + (mi & 1) * 8 + (lane & 7);
-                    ldsm_x4(qf[mt][ks], sQ32 + swz(row, ks * 2 + (mi >> 1)));
-                }
-        }
-        const int kw0 = it * kKT + warp * 16;   // chunk-local first key of this warp
-        if (kw0 < nkeys) {
-            const uint32_t bufK = sKV32 + (it % kStages) * kStageB;
-            const uint32_t bufV = bufK + kKT * kRowB;
-            uint32_t kb[4][4];
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const int mi = lane >> 3;
-                const int r = warp * 16 + (mi >> 1) * 8 + (lane & 7);
-                ldsm_x4(kb[ks], bufK + swz(r, ks * 2 + (mi & 1)));
-            }
-            uint32_t vb[8][2];
-#pragma unroll
-            for (int dp = 0; dp < 4; ++dp) {
-                const int mi = lane >> 3;
-                const int r = warp * 16 + (mi & 1) * 8 + (lane & 7);
-                uint32_t x[4];
-                ldsm_x4_t(x, bufV + swz(r, dp * 2 + (mi >> 1)));
-                vb[2 * dp][0] = bf2_to_h2(x[0]);
-                vb[2 * dp][1] = bf2_to_h2(x[1]);
-                vb[2 * dp + 1][0] = bf2_to_h2(x[2]);
-                vb[2 * dp + 1][1] = bf2_to_h2(x[3]);
-            }
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-                if (mt * 16 < nq) {
-                    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-                    for (int ks = 0; ks < 4; ++ks) {
-                        uint32_t a[4];
-                        if (kQReg) {
-#pragma unroll
-                            for (int k = 0; k < 4; ++k) a[k] = qf[kQReg ? mt : 0][ks][k];
-                        } else {
-                            const int mi = lane >> 3;
-                            const int row = mt * 16 + (mi & 1) * 8 + (lane & 7);
-                            ldsm_x4(a, sQ32 + swz(row, ks * 2 + (mi >> 1)));
-                        }
-                        mma_bf16(s[0], a, kb[ks][0], kb[ks][1]);
-                        mma_bf16(s[1], a, kb[ks][2], kb[ks][3]);
-                    }
-                    // scores of row 0 and every later row are all visible up to
-                    // lim_all; past it (the causal edge, the chunk's end) mask
-                    if (kw0 + 16 > lim_all) {
-#pragma unroll
-                        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int key = kw0 + nt * 8 + 2 * t4 + (e & 1);
-                                if (key >= lim[mt][e >> 1]) s[nt][e] = -INFINITY;
-                            }
-                    }
-                    float mx[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) mx[e >> 1] = fmaxf(mx[e >> 1], s[nt][e]);
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], 1));
-                        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xFFFFFFFFu, mx[r], 2));
-                    }
-                    // lazy rescale: the reference max moves only when a row's max
-                    // rises more than kTau (log2 units) above it, so p <= 2^kTau
-                    float alpha[2] = {1.f, 1.f}, muse[2];
-                    bool resc = false;
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        const float mxs = mx[r] * kLog2e8;
-                        mtrue[mt][r] = fmaxf(mtrue[mt][r], mxs);
-                        if (mxs > m[mt][r] + kTau) {
-                            alpha[r] = ex2(m[mt][r] - mxs);
-                            m[mt][r] = mxs;
-                            resc = true;
-                        }
-                        muse[r] = (m[mt][r] == -INFINITY) ? 0.f : m[mt][r];
-                    }
-                    if (__any_sync(0xFFFFFFFFu, resc)) {
-#pragma unroll
-                        for (int r = 0; r < 2; ++r) l[mt][r] *= alpha[r];
-#pragma unroll
-                        for (int dt = 0; dt < 8; ++dt) {
-                            o[mt][dt][0] *= alpha[0];
-                            o[mt][dt][1] *= alpha[0];
-                            o[mt][dt][2] *= alpha[1];
-                            o[mt][dt][3] *= alpha[1];
-                        }
-                    }
-                    float ps[2] = {0.f, 0.f};
-#pragma unroll
-                    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float p = ex2(fmaf(s[nt][e], kLog2e8, -muse[e >> 1]));
-                            s[nt][e] = p;
-                            ps[e >> 1] += p;
-                        }
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) l[mt][r] += ps[r];
-                    uint32_t pa[4];
-                    pa[0] = pack_h2(s[0][0], s[0][1]);
-                    pa[1] = pack_h2(s[0][2], s[0][3]);
-                    pa[2] = pack_h2(s[1][0], s[1][1]);
-                    pa[3] = pack_h2(s[1][2], s[1][3]);
-#pragma unroll
-                    for (int dt = 0; dt < 8; ++dt) mma_f16(o[mt][dt], pa, vb[dt][0], vb[dt][1]);
-                }
-            }
-        }
-        __syncthreads();
-    }
-    cp_async_wait<0>();
-    __syncthreads();
-    pdl_trigger();
-
-    // renormalise each row to its true running max (exact partial format)
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            if (mtrue[mt][r] > m[mt][r]) {
-                const float f = ex2(m[mt][r] - mtrue[mt][r]);
-                l[mt][r] *= f;
-#pragma unroll
-                for (int dt = 0; dt < 8; ++dt) {
-                    o[mt][dt][2 * r] *= f;
-                    o[mt][dt][2 * r + 1] *= f;
-                }
-            }
-            m[mt][r] = mtrue[mt][r];
-        }
-
-    // ---- combine the four warps (shared memory reused)
-    float* sO = reinterpret_cast<float*>(smem);                     // [4][16*MT][kOStride]
-    float* sM = sO + kWarps * 16 * MT * kOStride;                    // [4][16*MT]
-    float* sL = sM + kWarps * 16 * MT;                               // [4][16*MT]
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            float lr = l[mt][r];
-            lr += __shfl_xor_sync(0xFFFFFFFFu, lr, 1);
-            lr += __shfl_xor_sync(0xFFFFFFFFu, lr, 2);
-            const int qi = mt * 16 + g8 + 8 * r;
-            if (t4 == 0) {
-                sM[warp * 16 * MT + qi] = m[mt][r];
-                sL[warp * 16 * MT + qi] = lr;
-            }
-            float* row = sO + (size_t(warp) * 16 * MT + qi) * kOStride;
-#pragma unroll
-            for (int dt = 0; dt < 8; ++dt)
-                *reinterpret_cast<float2*>(row + dt * 8 + 2 * t4) =
-                    make_float2(o[mt][dt][2 * r], o[mt][dt][2 * r + 1]);
-        }
-    }
-    __syncthreads();
     const int mode = out ? st.merge_mode : kMergeKernel;   // records only in the two-call form
-    const int64_t rec0 = st.pbase + (int64_t(item.chunk) * TF_NKV + g) * nq_all + q0;
-    for (int idx = tid; idx < nq * (TF_D / 4); idx += kThreads) {
-        const int qi = idx >> 4, d4 = (idx & 15) * 4;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) M = fmaxf(M, sM[w * 16 * MT + qi]);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        float L = 0.f;
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float mw = sM[w * 16 * MT + qi];
-                const float wt = (mw == -INFINITY) ? 0.f : ex2(mw - M);
-                L += wt * sL[w * 16 * MT + qi];
-                const float4 v = *reinterpret_cast<const float4*>(sO + (size_t(w) * 16 * MT + qi) * kOStride + d4);
-                acc.x += wt * v.x;
-                acc.y += wt * v.y;
-                acc.z += wt * v.z;
-                acc.w += wt * v.w;
-            }
-        }
-        if (mode == kMergeDirect) {   // the stream's only chunk: the output itself
-            const float inv = 1.f / L;
-            *reinterpret_cast<float4*>(out_row(out, st, g, q0 + qi) + d4) =
-                make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-        } else {
-            *reinterpret_cast<float4*>(part_o + (rec0 + qi) * TF_D + d4) = acc;
-            if (d4 == 0) part_ml[rec0 + qi] = make_float2(M, L);
-        }
-    }
+    item::attn_item<MT, true, 0>(t, layer, it, st, g, q, part_o, part_ml, out, mode, full, smem, threadIdx.x, true);
     if (mode == kMergeLastCta) {
         __shared__ int last_flag;
-        finish_last_cta<MT == 1 ? 8 : 16>(t, layer, item.stream, st, g, part_o, part_ml, out, &last_flag);
+        finish_last_cta<MT == 1 ? 8 : 16>(t, layer, it.stream, st, g, part_o, part_ml, out, &last_flag);
     }
 }
 

@@ -40,11 +40,13 @@
 // At the end (m, l, O) is renormalised to the true running max and written
 // as the chunk's partial records.
 //
-// Every wait on an mbarrier is bounded (2 s of %globaltimer); on a timeout the
-// CTA raises a shared abort flag, waits (bounded) for its TMA copies and MMAs
-// in flight, writes NaN records (so the merged output shows the failure),
-// frees its tensor memory and returns.
+// Every wait on an mbarrier is bounded (the library's wait limit, 2 s of
+// %globaltimer unless tf_set_wait_limit_ns changed it); on a timeout the CTA
+// raises a shared abort flag, waits (bounded) for its TMA copies and MMAs in
+// flight, writes NaN records, sets TF_STATUS_ATTN_TIMEOUT in the table's
+// status word, frees its tensor memory and returns.
 #include "tc_ptx.cuh"
+#include "attn_item.cuh"
 
 namespace tf {
 namespace {
@@ -81,7 +83,9 @@ struct Bars {
     uint64_t grp;                // the four softmax warps meet here (last-CTA merges)
     uint64_t drain;
     uint32_t tmem_base;
-    uint32_t abort_flag;
+    WaitCtl wc;                  // abort flag and wait limit of the CTA's bounded waits
+    int32_t redo_m;              // the CTA's last unit (running index) queued for the exact recompute
+    int32_t is_last;             // this CTA finished last (it runs the exact recomputes)
     int32_t last;
 };
 constexpr int kSmemBytes = 1024 + kQB + kStages * kStageB + int(sizeof(Bars));
@@ -133,7 +137,7 @@ __device__ __forceinline__ Unit unit_of(const SegTable& t, int layer, int u) {
 // and lane L + 16 keys 32-63, so every lane does useful softmax work.
 struct SoftState {
     Bars* bars;
-    volatile uint32_t* abortp;
+    volatile WaitCtl* abortp;
     uint32_t trow;       // TMEM address of the warp's lane quadrant
     int g0;              // the CTA's running tile count at the unit's first tile
     int T, lim, lim_all;
@@ -245,7 +249,7 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
 
 // The m-th unit the producer handed this CTA after its first (blockIdx.x), or
 // -1: no more (or the CTA gave up). Single-thread consumer (the MMA thread).
-__device__ __forceinline__ int next_unit_thread(Bars* bars, int m, volatile uint32_t* abortp) {
+__device__ __forceinline__ int next_unit_thread(Bars* bars, int m, volatile WaitCtl* abortp) {
     const int slot = m % kUQ;
     if (!mbar_wait(su32(&bars->uq_full[slot]), (m / kUQ) & 1, abortp)) return -1;
     const int u = reinterpret_cast<volatile int32_t*>(bars->uq)[slot];
@@ -253,7 +257,7 @@ __device__ __forceinline__ int next_unit_thread(Bars* bars, int m, volatile uint
     return u;
 }
 // The same for a whole warp: every lane reads, then lane 0 releases the slot.
-__device__ __forceinline__ int next_unit_warp(Bars* bars, int m, volatile uint32_t* abortp) {
+__device__ __forceinline__ int next_unit_warp(Bars* bars, int m, volatile WaitCtl* abortp) {
     const int slot = m % kUQ;
     int u = -1;
     if (mbar_wait_warp(su32(&bars->uq_full[slot]), (m / kUQ) & 1, abortp))
@@ -264,7 +268,7 @@ __device__ __forceinline__ int next_unit_warp(Bars* bars, int m, volatile uint32
 }
 
 // The four softmax warps (128 threads) meet; bounded like every wait here.
-__device__ __forceinline__ bool group_sync(Bars* bars, int& ph, volatile uint32_t* abortp) {
+__device__ __forceinline__ bool group_sync(Bars* bars, int& ph, volatile WaitCtl* abortp) {
     mbar_arrive(su32(&bars->grp));
     const bool ok = mbar_wait(su32(&bars->grp), ph & 1, abortp);
     ++ph;
@@ -287,6 +291,42 @@ __device__ __forceinline__ void load_q_async(uint32_t sQ, const uint16_t* q, con
     cp_async_commit();
 }
 
+// The exact recompute of the units the launch queued (rare: V beyond fp16's
+// range, or so small that fp16 would cost relative precision), by the last
+// CTA's warps 0-3 (128 threads, named barrier 1) once every other CTA is done:
+// each unit's window rows in groups of 8 (32 query rows) with the mma.sync
+// item code on its exact path (V in bf16, P split into two bf16 parts),
+// writing the unit's records or output again; then the unit's deferred merge
+// arrival (a last-CTA merge runs here when it completes the count).
+__device__ __noinline__ void recompute_exact(const SegTable& t, int layer, const uint16_t* q, float* part_o,
+                                             float2* part_ml, float* out, int full, unsigned char* smem, int tid) {
+    const int n = *reinterpret_cast<volatile const int32_t*>(t.tc_redo);
+    __shared__ int last_flag;
+    for (int k = 0; k < n; ++k) {
+        const Unit U = unit_of(t, layer, __ldcg(t.tc_redo + 1 + k));
+        const int mode = out ? U.st.merge_mode : kMergeKernel;
+        for (int q0 = 0; q0 < 4 * U.st.rows; q0 += 32) {
+            const AttnItem it{U.stream, U.chunk, q0, 0};
+            item::attn_item<2, false, 1>(t, layer, it, U.st, U.g, q, part_o, part_ml, out, mode, full, smem, tid,
+                                         false);
+            item::bar_sync(1);   // the item's shared memory is reused by the next group
+        }
+        if (mode == kMergeLastCta) {
+            __threadfence();
+            item::bar_sync(1);
+            int* ctr = t.counters + (size_t(layer) * t.S + U.stream) * TF_NKV + U.g;
+            if (tid == 0) last_flag = atomicAdd(ctr, 1) == U.st.n_chunks - 1;
+            item::bar_sync(1);
+            if (last_flag) {
+                __threadfence();
+                merge_stream_head<4>(U.st, U.g, part_o, part_ml, out, tid, 128);
+                if (tid == 0) atomicExch(ctr, 0);
+            }
+            item::bar_sync(1);
+        }
+    }
+}
+
 // Persistent: one launch of at most two CTAs per SM; each CTA runs its units
 // back to back. A CTA starts with unit blockIdx.x; whenever its TMA producer
 // has issued a unit's last tile it takes the next unit of the launch (an atomic
@@ -305,7 +345,7 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
     const uint32_t sQ = base;
     const uint32_t sStage = base + kQB;
     Bars* bars = reinterpret_cast<Bars*>(gbase + kQB + kStages * kStageB);
-    volatile uint32_t* abortp = &bars->abort_flag;
+    volatile WaitCtl* abortp = &bars->wc;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     if (tid == 0) {
@@ -326,7 +366,9 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
         }
         mbar_init(su32(&bars->grp), 128);
         mbar_init(su32(&bars->drain), 1);
-        bars->abort_flag = 0;
+        bars->wc.flag = 0;
+        bars->wc.limit_ns = t.wait_ns;
+        bars->redo_m = -1;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (tid == 0 && int(blockIdx.x) < n_units) {   // the first unit's first tiles into L2 meanwhile
@@ -431,7 +473,7 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                 mbar_arrive(su32(&bars->uq_full[slot]));   // release: the index is visible to the waiters
                 u = un;
             }
-            if (*abortp)   // let the copies in flight land before the CTA exits
+            if (abortp->flag)   // let the copies in flight land before the CTA exits
                 for (int k = gt > kStages ? gt - kStages : 0; k < gt; ++k)
                     mbar_drain(su32(&bars->kv_full[k % kStages]), (k / kStages) & 1);
         }
@@ -509,11 +551,11 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
             // unit's queries may overwrite the buffer while this one finishes
             const int un = next_unit_warp(bars, m, abortp);
             if (un >= 0) load_q_async(sQ, q, unit_of(t, layer, un), tid);
-            if (!*abortp) mbar_wait(su32(&bars->o_done[(gt - 1) % kSBuf]), ((gt - 1) / kSBuf) & 1, abortp);
+            if (!abortp->flag) mbar_wait(su32(&bars->o_done[(gt - 1) % kSBuf]), ((gt - 1) / kSBuf) & 1, abortp);
             tc_fence_after();
             if (wact) {
                 // (m, l, O) renormalised to the true running max -> the chunk's record
-                const bool aborted = *abortp != 0;
+                const bool aborted = abortp->flag != 0;
                 float f = 1.f;
                 if (ss.mtrue > ss.mref && ss.mref != -INFINITY) f = ex2(ss.mref - ss.mtrue);
                 uint32_t ro[64];
@@ -527,6 +569,27 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                                                 __uint_as_float(__shfl_xor_sync(0xFFFFFFFFu, ro[c], 16)));
                     lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 16);
                 }
+                // P.V ran with V in fp16. A row whose O is not finite (a V of
+                // 65,536 or more has no fp16 value), or a warp whose rows'
+                // outputs |o| / l all lie below 2^-10 (fp16's subnormal steps
+                // of 2^-24 would cost relative precision), sends the unit to
+                // the exact recompute at the end of the launch; its records
+                // are rewritten there and its merge waits for them.
+                bool nonfinite = false, big = false;
+                if (qvalid && lsum > 0.f) {
+                    nonfinite = !isfinite(lsum);
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) {
+                        const float v = __uint_as_float(ro[c]);
+                        nonfinite |= !isfinite(v);
+                        big |= fabsf(v) >= 0x1p-10f * lsum;
+                    }
+                }
+                const bool seen = __any_sync(0xFFFFFFFFu, qvalid && lsum > 0.f);
+                const bool redo = !aborted && (__any_sync(0xFFFFFFFFu, nonfinite) ||
+                                               (seen && !__any_sync(0xFFFFFFFFu, big)));
+                if (redo && lane == 0 && atomicMax(&bars->redo_m, m) < m)
+                    t.tc_redo[1 + atomicAdd(t.tc_redo, 1)] = u;
                 if (owner && mode == kMergeDirect) {   // the stream's only chunk: the output itself
                     const float inv = aborted ? NAN : 1.f / lsum;   // a row always sees key 0 of its stream
                     float4* dst = reinterpret_cast<float4*>(out_row(out, st, U.g, qi));
@@ -566,7 +629,10 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                 __threadfence();
                 if (group_sync(bars, gph, abortp)) {
                     int* ctr = t.counters + (size_t(layer) * t.S + U.stream) * TF_NKV + U.g;
-                    if (tid == 0) bars->last = (atomicAdd(ctr, 1) == st.n_chunks - 1);
+                    // a unit queued for the exact recompute arrives after it
+                    if (tid == 0)
+                        bars->last = *reinterpret_cast<volatile int32_t*>(&bars->redo_m) == m
+                                         ? 0 : (atomicAdd(ctr, 1) == st.n_chunks - 1);
                     if (group_sync(bars, gph, abortp) && bars->last) {
                         __threadfence();
                         merge_stream_head<4>(st, U.g, part_o, part_ml, out, tid, 128);
@@ -581,18 +647,30 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
     __syncthreads();   // every role is done
     tc_fence_after();
     if (tid == 0) {
+        // a CTA that gave up a wait reports it in the table's status word
+        // (tf_segments_status reads it and resets the table's counters)
+        if (abortp->flag) atomicOr(t.status, uint32_t(TF_STATUS_ATTN_TIMEOUT));
         // the last CTA to finish (every unit has been handed out by then) resets
-        // the work counters for the next launch
+        // the work counters for the next launch and runs the exact recomputes
         __threadfence();
-        if (atomicAdd(&t.tc_work[2 * layer + 1], 1) == int(gridDim.x) - 1) {
+        const bool last = atomicAdd(&t.tc_work[2 * layer + 1], 1) == int(gridDim.x) - 1;
+        if (last) {
             atomicExch(&t.tc_work[2 * layer], 0);
             atomicExch(&t.tc_work[2 * layer + 1], 0);
         }
+        bars->is_last = last ? 1 : 0;
     }
     pdl_trigger();
     if (warp == 4) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kCols) : "memory");
+    }
+    __syncthreads();
+    if (bars->is_last) {
+        __threadfence();   // every CTA queued its units before it counted itself done
+        if (warp < 4) recompute_exact(t, layer, q, part_o, part_ml, out, full, gbase, tid);
+        __syncthreads();
+        if (tid == 0) t.tc_redo[0] = 0;
     }
 }
 
@@ -604,9 +682,11 @@ int attn_tc_prepare() {
     return e == cudaSuccess ? TF_OK : cuda_fail(e);
 }
 
-int launch_attn_partials_tc(const SegTable& t, int layer, const uint16_t* q, float* po, float2* pml,
+int launch_attn_partials_tc(const SegTable& t0, int layer, const uint16_t* q, float* po, float2* pml,
                             cudaStream_t stream, float* out, int full) {
-    if (!t.k_maps || !t.v_maps) return TF_EINVAL;
+    if (!t0.k_maps || !t0.v_maps) return TF_EINVAL;
+    SegTable t = t0;
+    t.wait_ns = wait_limit_ns();
     const int n_units = (t.n_items - t.n_items_mma) * TF_NKV;
     const int slots = 2 * sm_count();   // two CTAs per SM, all resident
     const int grid = n_units < slots ? n_units : slots;

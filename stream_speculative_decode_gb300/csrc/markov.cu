@@ -40,9 +40,11 @@
 // picks and resets the scratch. The next step's launch reads those picks as
 // its previous tokens.
 //
-// Every mbarrier wait is bounded (2 s of %globaltimer); on a timeout the CTA
+// Every mbarrier wait is bounded (the library's wait limit, 2 s of
+// %globaltimer unless tf_set_wait_limit_ns changed it); on a timeout the CTA
 // raises its abort flag, drains its copies and MMAs (bounded), marks its
-// streams' rows with flag bit 1, frees its tensor memory and returns.
+// streams' rows with flag bit 1, sets TF_STATUS_MARKOV_TIMEOUT in the table's
+// status word, frees its tensor memory and returns.
 #include <cstdlib>
 #include <cstring>
 
@@ -71,7 +73,7 @@ struct Bars {
     uint64_t acc_empty[2];
     uint64_t drain;
     uint32_t tmem_base;
-    uint32_t abort_flag;
+    WaitCtl wc;             // abort flag and wait limit of the CTA's bounded waits
     int32_t last;
     int32_t tok[kLanes];    // previous token of the lane's stream, -1 if none or invalid
     int32_t row[kLanes];    // draft row of the lane's stream in this step, -1 if it has none
@@ -178,7 +180,7 @@ markov_step_kernel(SegTable t, int step, const uint16_t* __restrict__ W1, int vo
     const uint32_t sA = sbase;
     const uint32_t sB = sbase + kAB;
     Bars* bars = reinterpret_cast<Bars*>(gbase + kAB + kStages * kSlabB);
-    volatile uint32_t* abortp = &bars->abort_flag;
+    volatile WaitCtl* abortp = &bars->wc;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int group = blockIdx.y;
     const int s0 = group * kLanes;
@@ -197,7 +199,8 @@ markov_step_kernel(SegTable t, int step, const uint16_t* __restrict__ W1, int vo
             mbar_init(su32(&bars->acc_empty[b]), 4);   // the 4 epilogue warps
         }
         mbar_init(su32(&bars->drain), 1);
-        bars->abort_flag = 0;
+        bars->wc.flag = 0;
+        bars->wc.limit_ns = t.wait_ns;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     pdl_wait();   // previous tokens may be the picks of the step just before
@@ -255,7 +258,7 @@ markov_step_kernel(SegTable t, int step, const uint16_t* __restrict__ W1, int vo
                 tma_load_2d_hint(sB + s * kSlabB, &w2map, (i % kKB) * 64, (t_begin + i / kKB) * kTileV, bar, keep);
                 ++issued;
             }
-            if (*abortp)   // let the copies in flight land before the CTA exits
+            if (abortp->flag)   // let the copies in flight land before the CTA exits
                 for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
                     mbar_drain(su32(&bars->full[i % kStages]), (i / kStages) & 1);
         }
@@ -334,7 +337,7 @@ markov_step_kernel(SegTable t, int step, const uint16_t* __restrict__ W1, int vo
     // this CTA's best of each stream, met across CTAs in the table's scratch
     if (warp < 4 && my_tok >= 0) {
         const int s = s0 + L;
-        if (*abortp) {
+        if (abortp->flag) {
             atomicOr(&t.mk_flags[s], 2u);
         } else {
             if (bid != 0x7FFFFFFF)
@@ -373,6 +376,7 @@ markov_step_kernel(SegTable t, int step, const uint16_t* __restrict__ W1, int vo
         if (tid == 0) atomicExch(&t.mk_ctr[group], 0u);
     }
     __syncthreads();
+    if (tid == 0 && abortp->flag) atomicOr(t.status, uint32_t(TF_STATUS_MARKOV_TIMEOUT));
     if (warp == 4) {
         tc_fence_after();
         tc_dealloc(tmem, kCols);
@@ -401,7 +405,7 @@ struct ChainBars {
     uint64_t e_ready;       // the step's W1 rows are in E (the 128 epilogue threads)
     uint64_t drain;
     uint32_t tmem_base;
-    uint32_t abort_flag;
+    WaitCtl wc;             // abort flag and wait limit of the CTA's bounded waits
     int32_t last;
     int32_t stop;           // epilogue thread 0's snapshot of the abort flag, read after a barrier
     int32_t tok[kLanes];
@@ -412,19 +416,19 @@ constexpr int kChainSmemBytes = 1024 + kAB + kStages * kSlabB + int(sizeof(Chain
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // Wait until the step barrier's generation reaches `target` (one thread).
-__device__ bool chain_wait(const uint32_t* sync, uint32_t target, volatile uint32_t* abortp) {
-    const unsigned long long t0 = gtime();
+__device__ bool chain_wait(const uint32_t* sync, uint32_t target, volatile WaitCtl* abortp) {
+    const unsigned long long t0 = gtime(), limit = abortp->limit_ns;
     for (;;) {
         uint32_t g;
         asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(sync + 1) : "memory");
         if (g >= target) return true;
-        if (*abortp) return false;
+        if (abortp->flag) return false;
         if (*reinterpret_cast<const volatile uint32_t*>(sync + 2)) {   // another CTA gave up
-            *abortp = 1;
+            abortp->flag = 1;
             return false;
         }
-        if (gtime() - t0 > kTimeoutNs) {
-            *abortp = 1;
+        if (gtime() - t0 > limit) {
+            abortp->flag = 1;
             return false;
         }
         __nanosleep(64);
@@ -443,7 +447,7 @@ markov_chain_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, int 
     const uint32_t sA = sbase;
     const uint32_t sB = sbase + kAB;
     ChainBars* bars = reinterpret_cast<ChainBars*>(gbase + kAB + kStages * kSlabB);
-    volatile uint32_t* abortp = &bars->abort_flag;
+    volatile WaitCtl* abortp = &bars->wc;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nt = (vocab + kTileV - 1) / kTileV;
     const int t_begin = int((int64_t(blockIdx.x) * nt) / gridDim.x);
@@ -461,7 +465,8 @@ markov_chain_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, int 
         }
         mbar_init(su32(&bars->e_ready), kLanes);
         mbar_init(su32(&bars->drain), 1);
-        bars->abort_flag = 0;
+        bars->wc.flag = 0;
+        bars->wc.limit_ns = t.wait_ns;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     pdl_wait();   // previous tokens and base rows may come from the kernel just before
@@ -487,7 +492,7 @@ markov_chain_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, int 
                 tma_load_2d_hint(sB + s * kSlabB, &w2map, (il % kKB) * 64, (t_begin + il / kKB) * kTileV, bar, keep);
                 ++issued;
             }
-            if (*abortp)
+            if (abortp->flag)
                 for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
                     mbar_drain(su32(&bars->full[i % kStages]), (i / kStages) & 1);
         }
@@ -553,7 +558,7 @@ markov_chain_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, int 
             if (j > 0) {
                 if (tid == 0) {
                     chain_wait(t.mk_sync, uint32_t(j), abortp);
-                    bars->stop = *abortp ? 1 : 0;
+                    bars->stop = abortp->flag ? 1 : 0;
                 }
                 epi_sync();
                 if (bars->stop) break;
@@ -641,7 +646,7 @@ markov_chain_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, int 
             __threadfence();
             epi_sync();
             if (tid == 0) {
-                bars->stop = *abortp ? 1 : 0;
+                bars->stop = abortp->flag ? 1 : 0;
                 bars->last = 0;
                 if (!bars->stop) {
                     __threadfence();
@@ -678,7 +683,7 @@ markov_chain_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, int 
             }
             done_steps = j + 1;
         }
-        if (*abortp) {
+        if (abortp->flag) {
             // give up: the other CTAs stop waiting; this stream's rows of the
             // steps not done are flagged
             atomicExch(t.mk_sync + 2, 1u);
@@ -695,6 +700,7 @@ markov_chain_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, int 
     __syncthreads();
     tc_fence_after();
     pdl_trigger();
+    if (tid == 0 && abortp->flag) atomicOr(t.status, uint32_t(TF_STATUS_MARKOV_TIMEOUT));
     if (warp == 4) {
         tc_fence_after();
         tc_dealloc(tmem, kCols);
@@ -713,8 +719,9 @@ extern "C" int tf_markov_chain(const tf_segments* seg, const void* W1, const voi
     if (!aligned16(W1) || !aligned16(W2) || !aligned16(base) || base_stride < vocab || base_stride % 8 != 0)
         return TF_EINVAL;
     if (!seg || seg->prompt) return TF_EINVAL;
-    const SegTable& t = seg->dev;
-    if (t.S == 0 || t.R == t.S) return TF_OK;   // no window holds a draft
+    if (seg->dev.S == 0 || seg->dev.R == seg->dev.S) return TF_OK;   // no window holds a draft
+    SegTable t = seg->dev;
+    t.wait_ns = wait_limit_ns();
     cudaError_t e = cudaFuncSetAttribute(markov_step_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return cuda_fail(e);
     CUtensorMap map;

@@ -8,6 +8,7 @@
 // residency concern (a table reaching buffers nobody declared) becomes here a
 // host check that the table's buffers are valid, aligned and never overlap.
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -20,6 +21,9 @@
 namespace tf {
 
 static thread_local int g_last_cuda_error = 0;
+static std::atomic<unsigned long long> g_wait_ns{TF_WAIT_LIMIT_DEFAULT_NS};
+
+unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
 
 int cuda_fail(cudaError_t e) {
     g_last_cuda_error = static_cast<int>(e);
@@ -230,7 +234,12 @@ int finish_build(tf_segments* seg, std::vector<tf::SegStream>& ss, std::vector<i
     const size_t o_mkc = off;      off = align_up(off + sizeof(uint32_t) * n_groups, 256);
     const size_t o_tcw = off;      off = align_up(off + sizeof(int32_t) * 2 * size_t(n_attn), 256);
     const size_t o_mks = off;      off = align_up(off + sizeof(uint32_t) * 4, 256);
+    const size_t n_tc_units = (items.size() - size_t(n_items_mma)) * TF_NKV;
+    const size_t o_redo = off;     off = align_up(off + sizeof(int32_t) * (1 + n_tc_units), 256);
+    const size_t o_st = off;       off = align_up(off + sizeof(uint32_t), 256);
     const size_t total = off;
+    seg->scratch_off = o_ctr;      // counters .. status word: zero in the image
+    seg->scratch_bytes = total - o_ctr;
 
     seg->host.assign(total, 0);
     unsigned char* h = seg->host.data();
@@ -304,6 +313,8 @@ int finish_build(tf_segments* seg, std::vector<tf::SegStream>& ss, std::vector<i
         t.mk_ctr = reinterpret_cast<uint32_t*>(b + o_mkc);
         t.tc_work = reinterpret_cast<int32_t*>(b + o_tcw);   // zero in the image
         t.mk_sync = reinterpret_cast<uint32_t*>(b + o_mks);
+        t.tc_redo = reinterpret_cast<int32_t*>(b + o_redo);   // zero in the image
+        t.status = reinterpret_cast<uint32_t*>(b + o_st);   // zero in the image
         rc = attn_prepare();
         if (rc == TF_OK) rc = attn_tc_prepare();
         if (rc != TF_OK) {
@@ -525,10 +536,38 @@ const char* tf_strerror(int status) {
         case TF_ERANGE: return "TF_ERANGE: size out of the supported range";
         case TF_ENOMEM: return "TF_ENOMEM: device allocation of the segment table failed";
         case TF_ECUDA: return "TF_ECUDA: a CUDA call or kernel launch failed";
+        case TF_ETIMEOUT: return "TF_ETIMEOUT: a kernel gave up a bounded device wait; the table's results since the "
+                                 "last check are not valid";
         default: return "unknown tf status";
     }
 }
 
 int tf_last_cuda_error(void) { return tf::g_last_cuda_error; }
+
+int tf_set_wait_limit_ns(uint64_t ns) {
+    if (ns > TF_WAIT_LIMIT_MAX_NS) return TF_ERANGE;
+    tf::g_wait_ns.store(ns);
+    return TF_OK;
+}
+
+uint64_t tf_wait_limit_ns(void) { return tf::g_wait_ns.load(); }
+
+int tf_segments_status(tf_segments* seg, tf_cuda_stream stream, uint32_t* bits) {
+    if (bits) *bits = 0;
+    if (!seg) return TF_EINVAL;
+    if (!seg->blob) return TF_OK;   // an empty round launches nothing
+    uint32_t h = 0;
+    cudaError_t e = cudaMemcpyAsync(&h, seg->dev.status, sizeof(h), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return tf::cuda_fail(e);
+    if (bits) *bits = h;
+    if (h == 0) return TF_OK;
+    // a CTA that gave up may have left the cross-CTA counters and merge
+    // scratch mid-count: back to the image's zeros, status word included
+    e = cudaMemsetAsync(static_cast<unsigned char*>(seg->blob) + seg->scratch_off, 0, seg->scratch_bytes, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return tf::cuda_fail(e);
+    return TF_ETIMEOUT;
+}
 
 }  // extern "C"

@@ -2,8 +2,10 @@
 // memory matrix descriptors, mbarriers with bounded waits, TMA tile loads and
 // the tcgen05 MMA / commit / tensor-memory load and store forms they use.
 //
-// Every wait here is bounded by %globaltimer: mbar_wait gives up after
-// kTimeoutNs (raising the caller's abort flag), mbar_drain after kDrainNs.
+// Every wait here is bounded by %globaltimer: mbar_wait gives up after the
+// CTA's wait limit (tf_set_wait_limit_ns, passed in the table; raising the
+// CTA's abort flag), mbar_drain after kDrainNs whatever that limit is, so
+// that a CTA which gave up still lets its own copies and MMAs land.
 #pragma once
 
 #include "tf_internal.cuh"
@@ -11,8 +13,16 @@
 namespace tf {
 namespace {
 
-constexpr unsigned long long kTimeoutNs = 2000000000ull;
 constexpr unsigned long long kDrainNs = 200000000ull;
+
+// What a CTA's bounded waits share, in shared memory: the abort flag a wait
+// that runs out raises (the CTA's other waits then give up at once), and the
+// wait limit in nanoseconds.
+struct WaitCtl {
+    uint32_t flag;
+    uint32_t pad_;
+    unsigned long long limit_ns;
+};
 
 // Shared-memory matrix descriptor: start address, leading / stride byte
 // offsets (16-byte units), descriptor version 1, 128-byte swizzle (layout 2).
@@ -49,22 +59,22 @@ __device__ __forceinline__ bool mbar_test(uint32_t a, uint32_t parity) {
 }
 // Bounded wait; false on timeout (raises the abort flag) or when another
 // thread raised it.
-__device__ bool mbar_wait(uint32_t a, uint32_t parity, volatile uint32_t* abort_flag) {
+__device__ bool mbar_wait(uint32_t a, uint32_t parity, volatile WaitCtl* wc) {
     if (mbar_test(a, parity)) return true;
-    const unsigned long long t0 = gtime();
+    const unsigned long long t0 = gtime(), limit = wc->limit_ns;
     for (;;) {
         if (mbar_test(a, parity)) return true;
-        if (*abort_flag) return false;
-        if (gtime() - t0 > kTimeoutNs) {
-            *abort_flag = 1;
+        if (wc->flag) return false;
+        if (gtime() - t0 > limit) {
+            wc->flag = 1;
             return false;
         }
     }
 }
 // The same wait by a whole warp, with one outcome for all its lanes (a lane
 // that ran out would otherwise leave the warp's collective operations short).
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t a, uint32_t parity, volatile uint32_t* abort_flag) {
-    return __all_sync(0xFFFFFFFFu, mbar_wait(a, parity, abort_flag));
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t a, uint32_t parity, volatile WaitCtl* wc) {
+    return __all_sync(0xFFFFFFFFu, mbar_wait(a, parity, wc));
 }
 // Bounded wait that ignores the abort flag (draining after an abort).
 __device__ void mbar_drain(uint32_t a, uint32_t parity) {
@@ -165,12 +175,15 @@ __device__ __forceinline__ void tc_st8(uint32_t taddr, const uint32_t (&r)[8]) {
 }
 template <int N>
 __device__ __forceinline__ void tc_st_n(uint32_t taddr, const uint32_t (&r)[N]) {
-    if constexpr (N == 8) {
+    if constexpr (N == 4) {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};"
+                     ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]) : "memory");
+    } else if constexpr (N == 8) {
         tc_st8(taddr, r);
     } else if constexpr (N == 32) {
         tc_st32(taddr, r);
     } else {
-        static_assert(N == 16, "8, 16 or 32 columns");
+        static_assert(N == 16, "4, 8, 16 or 32 columns");
         asm volatile(
             "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
             ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),

@@ -78,6 +78,9 @@ struct SegTable {
     uint32_t* mk_ctr;                 // [ceil(S/128)] Markov step: CTA arrivals per stream group
     int32_t* tc_work;                 // [n_attn][2] tensor-core attention: units handed out, CTAs done (self-resetting)
     uint32_t* mk_sync;                // [4] Markov chain in one launch: arrivals, generation, abort (zeroed per launch)
+    int32_t* tc_redo;                 // tensor-core attention: [0] units queued for the exact recompute, [1..] them
+    uint32_t* status;                 // TF_STATUS_* bits: a kernel gave up a bounded wait (tf_segments_status)
+    unsigned long long wait_ns;       // limit of a device wait, set per launch from tf_set_wait_limit_ns
 };
 
 constexpr int kAttnMma = 0;   // mma.sync flash-decode kernel (narrow windows)
@@ -105,12 +108,17 @@ struct tf_segments {
     std::vector<tf::SegStream> streams;
     tf_plan plan{};
     bool prompt = false;               // built by tf_prompt_build (conv + attention only)
+    size_t scratch_off = 0;            // the blob's cross-CTA scratch and status word:
+    size_t scratch_bytes = 0;          // zero in the image, zeroed again by tf_segments_status
 };
 
 namespace tf {
 
 // Record a CUDA error for tf_last_cuda_error and map it to TF_ECUDA.
 int cuda_fail(cudaError_t e);
+
+// The current limit of a device wait (tf_set_wait_limit_ns), in nanoseconds.
+unsigned long long wait_limit_ns();
 
 // Check the launch just issued.
 inline int launch_status() {
@@ -184,6 +192,21 @@ __device__ __forceinline__ float ex2_approx(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+
+// Largest |v| of two bf16 pairs, per half (the sign bits of the result are
+// not meaningful; NaN inputs are ignored).
+__device__ __forceinline__ uint32_t absmax_bf2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+// Whether a V tile with largest magnitude bits `m` (|v| as a bf16 bit
+// pattern) takes the exact bf16 path of P.V: |v| of 65,536 or more has no
+// fp16 value (fp16's largest is 65,504), and a tile whose values all lie
+// below 2^-6 would lose relative precision to fp16's subnormals (steps of
+// 2^-24). Any other tile converts to fp16 with an absolute error of at most
+// 2^-25 per value (only values below 2^-14 round at all).
+__device__ __forceinline__ bool v_tile_exact(uint32_t m) { return m >= 0x4780u || m < 0x3C80u; }
 
 // Output address of query row qi (window row qi/4, head 4g + qi%4) of a stream.
 __device__ __forceinline__ float* out_row(float* out, const SegStream& st, int g, int qi) {

@@ -23,14 +23,18 @@ TF_MAX_PROMPT_ROWS = 65536
 TF_PROMPT_WINDOW_ROWS = 32
 TF_MK = 256
 TF_DFLAG_BAD_PENDING, TF_DFLAG_BAD_DRAFT = 1, 2
-TF_OK, TF_EINVAL, TF_ERANGE, TF_ENOMEM, TF_ECUDA = 0, 1, 2, 3, 4
+TF_OK, TF_EINVAL, TF_ERANGE, TF_ENOMEM, TF_ECUDA, TF_ETIMEOUT = 0, 1, 2, 3, 4, 5
+TF_WAIT_LIMIT_DEFAULT_NS = 2000000000
+TF_WAIT_LIMIT_MAX_NS = 60000000000
+TF_STATUS_ATTN_TIMEOUT, TF_STATUS_MARKOV_TIMEOUT = 1, 2
 
 # every symbol include/tf.h declares
 EXPORTS = ("tf_chunk_keys", "tf_segments_plan", "tf_segments_build", "tf_segments_free",
            "tf_segments_query", "tf_partials_bytes", "tf_conv_rows", "tf_attn_partials",
            "tf_attn_merge", "tf_attn", "tf_attn_static", "tf_attn_block_partials", "tf_attn_block",
            "tf_argmax_rows", "tf_accept", "tf_markov_chain", "tf_draft_ids", "tf_prompt_build",
-           "tf_strerror", "tf_last_cuda_error")
+           "tf_strerror", "tf_last_cuda_error", "tf_set_wait_limit_ns", "tf_wait_limit_ns",
+           "tf_segments_status")
 TF_STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -87,6 +91,9 @@ def _load():
         "tf_accept": (i32, [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, vp]),
         "tf_strerror": (ctypes.c_char_p, [i32]),
         "tf_last_cuda_error": (i32, []),
+        "tf_set_wait_limit_ns": (i32, [ctypes.c_uint64]),
+        "tf_wait_limit_ns": (ctypes.c_uint64, []),
+        "tf_segments_status": (i32, [vp, vp, P(ctypes.c_uint32)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -288,3 +295,22 @@ def tf_accept(seg, ids, pick, flag, vocab, accept_len, next_token, new_keys, sfl
 
 def tf_strerror(status):
     return _lib.tf_strerror(status).decode()
+
+
+def tf_set_wait_limit_ns(ns):
+    """Limit of a device wait for later launches (see include/tf.h)."""
+    _check("tf_set_wait_limit_ns", _lib.tf_set_wait_limit_ns(int(ns)))
+
+
+def tf_wait_limit_ns():
+    return int(_lib.tf_wait_limit_ns())
+
+
+def tf_segments_status(seg, stream=None):
+    """(status, bits): reads and clears the table's status word (synchronises
+    the stream); status is TF_OK or TF_ETIMEOUT, raised for other codes."""
+    bits = ctypes.c_uint32(0)
+    rc = _lib.tf_segments_status(_h(seg), _stream(stream), ctypes.byref(bits))
+    if rc not in (TF_OK, TF_ETIMEOUT):
+        raise TFError("tf_segments_status", rc)
+    return rc, int(bits.value)

@@ -51,6 +51,23 @@ def check_conv(y_gpu, y_ref, m):
     assert not bad.any(), f"conv: {bad.sum()} of {bad.size} outside tolerance, worst excess {np.max(err - bound):.3e}"
 
 
+def check_attn_magnitude(out_gpu, out_ref, mag, what="attention"):
+    """Attention over V of mixed magnitudes: per element
+    |out - ref| <= 2e-3 * max(1, mag), with mag the float64 attention of |V|
+    (the weighted mean of the magnitudes being averaged), and relative L2
+    <= 1e-3. For V of N(0, 1) scale mag stays below 1 and this is the stated
+    bar; where a few huge values enter the average, the absolute part grows
+    with them, as the fp32 accumulation's rounding does."""
+    g = out_gpu.astype(np.float64)
+    diff = np.abs(g - out_ref)
+    bound = 2e-3 * np.maximum(1.0, mag)
+    bad = diff > bound
+    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside, worst excess {np.max(diff - bound):.3e}"
+    rel_l2 = float(np.linalg.norm(g - out_ref) / max(np.linalg.norm(out_ref), 1e-300))
+    assert rel_l2 <= 1e-3, f"{what}: rel-L2 {rel_l2:.3e}"
+    return rel_l2
+
+
 def check_attn(out_gpu, out_ref, what="attention"):
     g = out_gpu.astype(np.float64)
     diff = g - out_ref

@@ -43,9 +43,26 @@ def test_header_constants_match_binding(T):
 
 
 def test_strerror(T):
-    for code in range(5):
+    for code in range(6):
         assert T.tf_strerror(code).startswith("TF_")
     assert "unknown" in T.tf_strerror(99)
+
+
+def test_wait_limit_and_status_refusals(T):
+    """The device wait limit: default 2 s, settable within [0, 60 s], refused
+    beyond; the status query refuses a NULL table (no GPU needed)."""
+    lib = T.lib()
+    assert T.tf_wait_limit_ns() == T.TF_WAIT_LIMIT_DEFAULT_NS == 2_000_000_000
+    try:
+        T.tf_set_wait_limit_ns(0)
+        assert T.tf_wait_limit_ns() == 0
+        T.tf_set_wait_limit_ns(T.TF_WAIT_LIMIT_MAX_NS)
+        assert T.tf_wait_limit_ns() == T.TF_WAIT_LIMIT_MAX_NS
+        assert lib.tf_set_wait_limit_ns(T.TF_WAIT_LIMIT_MAX_NS + 1) == T.TF_ERANGE
+        assert T.tf_wait_limit_ns() == T.TF_WAIT_LIMIT_MAX_NS      # unchanged by the refusal
+    finally:
+        T.tf_set_wait_limit_ns(T.TF_WAIT_LIMIT_DEFAULT_NS)
+    assert lib.tf_segments_status(None, None, None) == T.TF_EINVAL
 
 
 def _chunk(rows):
