@@ -12,11 +12,15 @@
 // keys [0, len + 1)): only the per-row key bounds change.
 //
 // Persistent (at most two CTAs per SM, each running (key chunk, KV head)
-// units back to back; see the kernel), 7 warps:
+// units back to back; see the kernel), 8 warps:
 //   warp 6, lane 0   TMA loads of K/V tiles (64 keys = 8 KB each, 128-byte
 //                    swizzle) into a 5-stage ring, refilling a stage as soon
 //                    as the P.V that read it completes;
-//   warp 4, lane 0   the MMAs;
+//   warp 4, lane 0   the q.K MMAs;
+//   warp 7, lane 0   the P.V MMAs (two issuing threads: a single thread
+//                    issuing both in tile order held each q.K behind the
+//                    P.V of two tiles earlier, and the softmax waited for
+//                    its scores);
 //   warp 5           converts each V tile bf16 -> fp16 in shared memory as
 //                    soon as it lands (exact within fp16's range);
 //   warps 0-3        softmax; query row qi sits on TMEM lane
@@ -57,7 +61,7 @@ constexpr int kTileB = kKT * TF_D * 2;      // 8 KB: one K or V tile
 constexpr int kStageB = 2 * kTileB;         // K then V
 constexpr int kQRows = 128;                 // MMA M
 constexpr int kQB = kQRows * TF_D * 2;      // 16 KB
-constexpr int kWarps = 7;
+constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
 constexpr uint32_t kCols = 256;             // tensor-memory columns per CTA
 constexpr int kSBuf = 3;                    // S/P buffers: tile j uses buffer j % 3
@@ -67,7 +71,7 @@ constexpr float kLog2e8 = 0.18033688011112042f;   // log2(e) / sqrt(64)
 constexpr float kTau = 8.f;
 
 constexpr int kUQ = 4;                      // queue of the CTA's next units
-constexpr int kUQConsumers = 6;             // MMA thread, V converter warp, 4 softmax warps
+constexpr int kUQConsumers = 7;             // the two MMA threads, V converter warp, 4 softmax warps
 
 struct Bars {
     uint64_t kv_full[kStages];
@@ -81,7 +85,8 @@ struct Bars {
     uint64_t uq_empty[kUQ];
     int32_t uq[kUQ];
     uint64_t grp;                // the four softmax warps meet here (last-CTA merges)
-    uint64_t drain;
+    uint64_t drain;              // the q.K thread's MMAs in flight (drained at the end)
+    uint64_t drain_pv;           // the P.V thread's
     uint32_t tmem_base;
     WaitCtl wc;                  // abort flag and wait limit of the CTA's bounded waits
     int32_t redo_m;              // the CTA's last unit (running index) queued for the exact recompute
@@ -366,6 +371,7 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
         }
         mbar_init(su32(&bars->grp), 128);
         mbar_init(su32(&bars->drain), 1);
+        mbar_init(su32(&bars->drain_pv), 1);
         bars->wc.flag = 0;
         bars->wc.limit_ns = t.wait_ns;
         bars->redo_m = -1;
@@ -392,7 +398,10 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == 4) {
-        // ------------------------------------------------------------ control
+        // ------------------------------------------------------------ q.K MMAs
+        // S(g) may be issued as soon as K tile g has landed and the P.V of tile
+        // g-3 has released its S buffer, independently of the P.V thread, so
+        // the scores stay ahead of the softmax
         if (lane == 0) {
             const uint64_t dq = sdesc(sQ, 16, 1024);
             bool ok = true;
@@ -402,43 +411,57 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                 ok = mbar_wait(su32(&bars->q_ready), n & 1, abortp);   // the unit's queries landed
                 if (!ok) break;
                 tc_fence_after();
-                for (int j = 0; j <= T && ok; ++j) {
-                    if (j < T) {
-                        const int g1 = gt + j, s = g1 % kStages, b = g1 % kSBuf;
-                        ok = mbar_wait(su32(&bars->kv_full[s]), (g1 / kStages) & 1, abortp);
+                for (int j = 0; j < T && ok; ++j) {
+                    const int g1 = gt + j, s = g1 % kStages, b = g1 % kSBuf;
+                    ok = mbar_wait(su32(&bars->kv_full[s]), (g1 / kStages) & 1, abortp);
+                    if (!ok) break;
+                    if (g1 >= kSBuf) {   // P.V(g1-3) has released S buffer b
+                        ok = mbar_wait(su32(&bars->o_done[b]), ((g1 - kSBuf) / kSBuf) & 1, abortp);
                         if (!ok) break;
-                        if (g1 >= kSBuf) {   // P.V(g1-3) has released S buffer b
-                            ok = mbar_wait(su32(&bars->o_done[b]), ((g1 - kSBuf) / kSBuf) & 1, abortp);
-                            if (!ok) break;
-                        }
-                        tc_fence_after();
-                        const uint64_t dk = sdesc(sStage + s * kStageB, 16, 1024);
-#pragma unroll
-                        for (int k = 0; k < TF_D / 16; ++k)   // K = 64: 4 steps of 16 (32 bytes)
-                            tc_mma_ss(tmem + kColS + 64 * b, dq + 2 * k, dk + 2 * k, kIdescQK, k > 0 ? 1u : 0u);
-                        tc_commit(su32(&bars->s_full[b]));
                     }
-                    if (j >= 1) {
-                        const int jj = j - 1, g2 = gt + jj, s = g2 % kStages, b = g2 % kSBuf;
-                        ok = mbar_wait(su32(&bars->p_full[b]), (g2 / kSBuf) & 1, abortp);
-                        if (!ok) break;
-                        ok = mbar_wait(su32(&bars->v_ready[s]), (g2 / kStages) & 1, abortp);
-                        if (!ok) break;
-                        tc_fence_after();
-                        const uint64_t dv = sdesc(sStage + s * kStageB + kTileB, kTileB, 1024);
+                    tc_fence_after();
+                    const uint64_t dk = sdesc(sStage + s * kStageB, 16, 1024);
 #pragma unroll
-                        for (int k = 0; k < kKT / 16; ++k)   // 64 keys: 4 steps of 16 (2 KB of V rows)
-                            tc_mma_ts(tmem + kColO, tmem + kColS + 64 * b + 8 * k, dv + 128 * k, kIdescPV,
-                                      (jj > 0 || k > 0) ? 1u : 0u);
-                        tc_commit(su32(&bars->o_done[b]));
-                        tc_commit(su32(&bars->kv_empty[s]));
-                    }
+                    for (int k = 0; k < TF_D / 16; ++k)   // K = 64: 4 steps of 16 (32 bytes)
+                        tc_mma_ss(tmem + kColS + 64 * b, dq + 2 * k, dk + 2 * k, kIdescQK, k > 0 ? 1u : 0u);
+                    tc_commit(su32(&bars->s_full[b]));
                 }
                 gt += T;
                 if (ok) u = next_unit_thread(bars, n, abortp);
             }
-            tc_commit(su32(&bars->drain));   // every MMA issued so far
+            tc_commit(su32(&bars->drain));   // every MMA this thread issued
             mbar_drain(su32(&bars->drain), 0);
+        }
+        __syncwarp();
+    } else if (warp == 7) {
+        // ------------------------------------------------------------ P.V MMAs
+        if (lane == 0) {
+            bool ok = true;
+            int gt = 0, n = 0;
+            for (int u = blockIdx.x; u >= 0 && ok; ++n) {
+                const int T = unit_of(t, layer, u).T;
+                for (int j = 0; j < T && ok; ++j) {
+                    const int g2 = gt + j, s = g2 % kStages, b = g2 % kSBuf;
+                    ok = mbar_wait(su32(&bars->p_full[b]), (g2 / kSBuf) & 1, abortp);
+                    if (!ok) break;
+                    ok = mbar_wait(su32(&bars->v_ready[s]), (g2 / kStages) & 1, abortp);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t dv = sdesc(sStage + s * kStageB + kTileB, kTileB, 1024);
+#pragma unroll
+                    for (int k = 0; k < kKT / 16; ++k)   // 64 keys: 4 steps of 16 (2 KB of V rows)
+                        tc_mma_ts(tmem + kColO, tmem + kColS + 64 * b + 8 * k, dv + 128 * k, kIdescPV,
+                                  (j > 0 || k > 0) ? 1u : 0u);
+                    // the stage's K was read by the q.K of this tile, which completed
+                    // before the softmax read S; V by this P.V
+                    tc_commit(su32(&bars->o_done[b]));
+                    tc_commit(su32(&bars->kv_empty[s]));
+                }
+                gt += T;
+                if (ok) u = next_unit_thread(bars, n, abortp);
+            }
+            tc_commit(su32(&bars->drain_pv));
+            mbar_drain(su32(&bars->drain_pv), 0);
         }
         __syncwarp();
     } else if (warp == 6) {
@@ -549,6 +572,7 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
             gt += U.T;
             // every q.K of this unit is done (the softmax read each S): the next
             // unit's queries may overwrite the buffer while this one finishes
+            // (loading them during the last tile instead measured slower)
             const int un = next_unit_warp(bars, m, abortp);
             if (un >= 0) load_q_async(sQ, q, unit_of(t, layer, un), tid);
             if (!abortp->flag) mbar_wait(su32(&bars->o_done[(gt - 1) % kSBuf]), ((gt - 1) / kSBuf) & 1, abortp);
