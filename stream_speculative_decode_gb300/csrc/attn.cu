@@ -215,6 +215,31 @@ int attn_prepare() {
 // attention layer with the partial records at `po` (o) and `pml` (m, l).
 int launch_attn_partials(const SegTable& t, int layer, const uint16_t* q, float* po, float2* pml,
                          cudaStream_t stream, float* out, int full) {
+    if (t.n_items_mma > 0 && t.n_items_mma < t.n_items && t.side) {
+        // both kinds of windows: the two launches run side by side (they write
+        // disjoint streams' records and outputs). The persistent tensor-core
+        // grid, sized to its share of the keys, stays on the caller's stream,
+        // where it launches early (programmatic dependent launch) and holds its
+        // SMs; the mma.sync launch, forked onto the table's side stream, fills
+        // the rest once the previous kernel is done. (The other way round the
+        // early mma.sync launch took every SM before the tensor-core one.)
+        cudaError_t e = cudaEventRecord(t.ev_fork, stream);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(t.side, t.ev_fork, 0);
+        if (e != cudaSuccess) return cuda_fail(e);
+        int rc = launch_attn_partials_tc(t, layer, q, po, pml, stream, out, full, t.tc_grid_mixed);
+        if (rc != TF_OK) return rc;
+        const dim3 grid(t.n_items_mma * TF_NKV);
+        if (t.mma_mt == 1)
+            rc = launch_pdl(attn_partials_kernel<1>, grid, dim3(kThreads), smem_bytes(1), t.side, t, layer, q, po, pml,
+                            out, full);
+        else
+            rc = launch_pdl(attn_partials_kernel<2>, grid, dim3(kThreads), smem_bytes(2), t.side, t, layer, q, po, pml,
+                            out, full);
+        if (rc != TF_OK) return rc;
+        e = cudaEventRecord(t.ev_join, t.side);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, t.ev_join, 0);
+        return e == cudaSuccess ? TF_OK : cuda_fail(e);
+    }
     if (t.n_items_mma > 0) {
         const dim3 grid(t.n_items_mma * TF_NKV);
         int rc;

@@ -707,12 +707,12 @@ int attn_tc_prepare() {
 }
 
 int launch_attn_partials_tc(const SegTable& t0, int layer, const uint16_t* q, float* po, float2* pml,
-                            cudaStream_t stream, float* out, int full) {
+                            cudaStream_t stream, float* out, int full, int grid_cap) {
     if (!t0.k_maps || !t0.v_maps) return TF_EINVAL;
     SegTable t = t0;
     t.wait_ns = wait_limit_ns();
     const int n_units = (t.n_items - t.n_items_mma) * TF_NKV;
-    const int slots = 2 * sm_count();   // two CTAs per SM, all resident
+    const int slots = grid_cap > 0 ? grid_cap : 2 * sm_count();   // two CTAs per SM, all resident
     const int grid = n_units < slots ? n_units : slots;
     return launch_pdl(attn_partials_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, t, layer, q, po, pml,
                       out, full, n_units);

@@ -317,6 +317,29 @@ int finish_build(tf_segments* seg, std::vector<tf::SegStream>& ss, std::vector<i
         t.status = reinterpret_cast<uint32_t*>(b + o_st);   // zero in the image
         rc = attn_prepare();
         if (rc == TF_OK) rc = attn_tc_prepare();
+        if (rc == TF_OK && n_items_mma > 0 && size_t(n_items_mma) < items.size()) {
+            // a round of both window kinds: the tensor-core launch runs on a side
+            // stream with a grid proportional to its share of the keys (the K/V
+            // bytes), the mma.sync launch takes the rest of the SMs
+            int64_t keys_tc = 0, keys_all = 0;
+            for (const SegStream& d : ss) {
+                keys_all += d.keys;
+                if (attn_path_of(d.rows) == kAttnTc) keys_tc += d.keys;
+            }
+            const int slots = 2 * sm_count();
+            int g = int((int64_t(slots) * keys_tc + keys_all - 1) / (keys_all > 0 ? keys_all : 1));
+            t.tc_grid_mixed = g < 1 ? 1 : (g > slots ? slots : g);
+            if (cudaStreamCreateWithFlags(&t.side, cudaStreamNonBlocking) != cudaSuccess ||
+                cudaEventCreateWithFlags(&t.ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&t.ev_join, cudaEventDisableTiming) != cudaSuccess) {
+                // fall back to the two launches one after the other on the caller's stream
+                if (t.ev_fork) cudaEventDestroy(t.ev_fork);
+                if (t.side) cudaStreamDestroy(t.side);
+                t.side = nullptr;
+                t.ev_fork = t.ev_join = nullptr;
+                cudaGetLastError();
+            }
+        }
         if (rc != TF_OK) {
             cudaFree(seg->blob);
             delete seg;
@@ -511,6 +534,9 @@ int tf_prompt_build(int32_t rows, int32_t keys, int32_t kv_capacity, const void*
 int tf_segments_free(tf_segments* seg) {
     if (!seg) return TF_OK;
     int rc = TF_OK;
+    if (seg->dev.ev_join) cudaEventDestroy(seg->dev.ev_join);
+    if (seg->dev.ev_fork) cudaEventDestroy(seg->dev.ev_fork);
+    if (seg->dev.side) cudaStreamDestroy(seg->dev.side);
     if (seg->blob) {
         cudaError_t e = cudaFree(seg->blob);
         if (e != cudaSuccess) rc = tf::cuda_fail(e);

@@ -81,6 +81,14 @@ struct SegTable {
     int32_t* tc_redo;                 // tensor-core attention: [0] units queued for the exact recompute, [1..] them
     uint32_t* status;                 // TF_STATUS_* bits: a kernel gave up a bounded wait (tf_segments_status)
     unsigned long long wait_ns;       // limit of a device wait, set per launch from tf_set_wait_limit_ns
+    // Host side only (no kernel reads them): a round holding both kinds of
+    // attention windows runs its tensor-core launch on `side`, forked from and
+    // joined back to the caller's stream, so that it runs alongside the
+    // mma.sync launch; tc_grid_mixed is its grid then (its share of the keys).
+    cudaStream_t side;
+    cudaEvent_t ev_fork, ev_join;
+    int32_t tc_grid_mixed;
+    int32_t pad3_;
 };
 
 constexpr int kAttnMma = 0;   // mma.sync flash-decode kernel (narrow windows)
@@ -178,7 +186,8 @@ int launch_attn_merge(const SegTable& t, const float* po, const float2* pml, flo
 
 // attn_tc.cu: the tensor-core partials kernel (same records as the mma.sync kernel).
 int launch_attn_partials_tc(const SegTable& t, int layer, const uint16_t* q, float* po, float2* pml,
-                            cudaStream_t stream, float* out, int full);   // items [n_items_mma, n_items)
+                            cudaStream_t stream, float* out, int full,
+                            int grid = 0);   // items [n_items_mma, n_items); grid 0: two CTAs per SM
 int attn_tc_prepare();
 
 }  // namespace tf
