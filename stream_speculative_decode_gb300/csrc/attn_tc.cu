@@ -24,9 +24,12 @@
 //   warp 5           converts each V tile bf16 -> fp16 in shared memory as
 //                    soon as it lands (exact within fp16's range);
 //   warps 0-3        softmax; query row qi sits on TMEM lane
-//                    32*(qi / per) + qi % per (per = ceil(4*rows / 4)), so the
-//                    rows spread over the four lane quadrants and all four
-//                    SM sub-partitions share the softmax.
+//                    32*(qi / per) + qi % per (per = 16 for windows of at
+//                    most 16 rows, 32 for wider ones), so the rows spread
+//                    over the four lane quadrants and all four SM
+//                    sub-partitions share the softmax.
+// The q.K thread also loads each unit's queries (TMA, 16 KB) as soon as the
+// previous unit's last q.K has read the query buffer.
 // Per key tile j (TMEM columns: S/P of tile j at 64*(j%3), O at 192):
 //   S = Q K^T      M = 128 lanes (4*rows real rows, the rest zero), N = 64
 //                  keys, K = 64: A = Q (bf16, smem), B = K tile (bf16, smem);
@@ -81,6 +84,7 @@ struct Bars {
     uint64_t p_full[kSBuf];      // per S buffer
     uint64_t o_done[kSBuf];      // P.V of a tile using S buffer b completed
     uint64_t q_ready;            // the unit's queries are in shared memory (one phase a unit)
+    uint64_t q_free;             // every q.K of the unit is done: its query buffer may be refilled
     uint64_t uq_full[kUQ];       // the CTA's next units (unit index, -1 when there are no more)
     uint64_t uq_empty[kUQ];
     int32_t uq[kUQ];
@@ -280,20 +284,30 @@ __device__ __forceinline__ bool group_sync(Bars* bars, int& ph, volatile WaitCtl
     return ok;
 }
 
-// The unit's queries into shared memory (cp.async, zero rows past 4*rows),
-// swizzled K-major: lane L holds query qi = per*(L/32) + L%32 when L%32 < per
-// (dual, per <= 16: qi = per*(L/32) + L%16 when L%16 < per).
-__device__ __forceinline__ void load_q_async(uint32_t sQ, const uint16_t* q, const Unit& U, int tid) {
-    const int nq = U.st.rows * 4, per = (nq + 3) / 4;
-    const int lmask = per <= 16 ? 15 : 31;
-    for (int idx = tid; idx < kQRows * 8; idx += 128) {
-        const int L = idx >> 3, ch = idx & 7;
-        const int qq = per * (L >> 5) + (L & lmask);
-        const bool valid = (L & lmask) < per && qq < nq;
-        const uint16_t* src = q + ((size_t(U.st.row_offset + (qq >> 2)) * TF_NQ + 4 * U.g + (qq & 3)) * TF_D + ch * 8);
-        cp_async16(sQ + L * 128 + ((ch ^ (L & 7)) << 4), valid ? src : q, valid);
+// Query rows of a unit per TMEM lane quadrant: 16 for windows of at most 16
+// rows (dual softmax: lanes L and L + 16 of a quadrant hold the same query),
+// 32 for the prompt's wider windows. Quadrant w holds the unit's queries
+// [per*w, per*w + per), i.e. window rows per/4*w .. +per/4 - 1 with their four
+// heads of the KV head.
+__device__ __forceinline__ int q_per(int rows) { return rows <= 16 ? 16 : 32; }
+
+// The unit's queries into shared memory by TMA (one thread), K-major with the
+// 128-byte swizzle, lane L of the Q tile holding query per*(L/32) + L%per
+// (dual: + L%16, written twice): 8 boxes of 16 query rows (4 window rows x 4
+// heads), completing `bar` with 16 KB. Rows past the window belong to no query
+// of the unit (other streams' rows, or zeros past the last row): their lanes
+// are not valid rows and their results are never written.
+__device__ __forceinline__ void issue_q(uint32_t sQ, const CUtensorMap* qmap, const Unit& U, uint32_t bar) {
+    mbar_expect_tx(bar, kQB);
+    const bool dual = U.st.rows <= 16;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int w = k >> 1, h = k & 1;
+        // dual: both halves of quadrant w hold window rows 4w..4w+3; else the
+        // halves hold rows 8w..8w+3 and 8w+4..8w+7
+        const int row = U.st.row_offset + (dual ? 4 * w : 8 * w + 4 * h);
+        tma_load_3d(sQ + uint32_t(32 * w + 16 * h) * 128u, qmap, 0, 4 * U.g, row, bar);
     }
-    cp_async_commit();
 }
 
 // The exact recompute of the units the launch queued (rare: V beyond fp16's
@@ -342,7 +356,8 @@ __device__ __noinline__ void recompute_exact(const SegTable& t, int layer, const
 // buffers and their mbarrier phases follow one running tile count.
 __global__ void __launch_bounds__(kThreads, 2)
 attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, float* __restrict__ part_o,
-                        float2* __restrict__ part_ml, float* __restrict__ out, int full, int n_units) {
+                        float2* __restrict__ part_ml, float* __restrict__ out, int full, int n_units,
+                        const __grid_constant__ CUtensorMap qmap) {
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = su32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;            // 128-byte swizzle atoms need 1 KB alignment
@@ -364,7 +379,8 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
             mbar_init(su32(&bars->p_full[b]), 4);   // the 4 softmax warps
             mbar_init(su32(&bars->o_done[b]), 1);
         }
-        mbar_init(su32(&bars->q_ready), 128);       // every softmax thread, after its copies
+        mbar_init(su32(&bars->q_ready), 1);         // the q.K thread's expect_tx, then the TMA bytes
+        mbar_init(su32(&bars->q_free), 1);          // the q.K thread's commit after a unit's last q.K
         for (int k = 0; k < kUQ; ++k) {
             mbar_init(su32(&bars->uq_full[k]), 1);
             mbar_init(su32(&bars->uq_empty[k]), kUQConsumers);
@@ -389,8 +405,6 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(su32(&bars->tmem_base)), "r"(kCols) : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    } else if (warp < 4 && int(blockIdx.x) < n_units) {
-        load_q_async(sQ, q, unit_of(t, layer, blockIdx.x), tid);   // the first unit's queries
     }
     tc_fence_before();
     __syncthreads();
@@ -405,7 +419,11 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
         if (lane == 0) {
             const uint64_t dq = sdesc(sQ, 16, 1024);
             bool ok = true;
-            int gt = 0, n = 0;
+            int gt = 0, n = 0, q_issued = 0;
+            if (int(blockIdx.x) < n_units) {
+                issue_q(sQ, &qmap, unit_of(t, layer, blockIdx.x), su32(&bars->q_ready));
+                q_issued = 1;
+            }
             for (int u = blockIdx.x; u >= 0 && ok; ++n) {
                 const int T = unit_of(t, layer, u).T;
                 ok = mbar_wait(su32(&bars->q_ready), n & 1, abortp);   // the unit's queries landed
@@ -427,10 +445,23 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                     tc_commit(su32(&bars->s_full[b]));
                 }
                 gt += T;
-                if (ok) u = next_unit_thread(bars, n, abortp);
+                if (!ok) break;
+                // the next unit's queries, as soon as this unit's q.K have read the
+                // buffer (long before the softmax finishes this unit)
+                tc_commit(su32(&bars->q_free));
+                u = next_unit_thread(bars, n, abortp);
+                if (u >= 0) {
+                    ok = mbar_wait(su32(&bars->q_free), n & 1, abortp);
+                    if (ok) {
+                        issue_q(sQ, &qmap, unit_of(t, layer, u), su32(&bars->q_ready));
+                        ++q_issued;
+                    }
+                }
             }
             tc_commit(su32(&bars->drain));   // every MMA this thread issued
             mbar_drain(su32(&bars->drain), 0);
+            if (q_issued > n)   // a query load not waited for (the CTA gave up): let it land
+                mbar_drain(su32(&bars->q_ready), (q_issued - 1) & 1);
         }
         __syncwarp();
     } else if (warp == 7) {
@@ -536,15 +567,11 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
         // ------------------------------------------------------------ softmax + records
         int gt = 0, gph = 0;
         const uint32_t trow = tmem + (uint32_t(warp * 32) << 16);
-        // the first unit's queries (copied by this thread) become visible to the tensor cores
-        asm volatile("cp.async.wait_all;" ::: "memory");
-        fence_async_smem();
-        mbar_arrive(su32(&bars->q_ready));
         for (int u = blockIdx.x, m = 0; u >= 0; ++m) {
             const Unit U = unit_of(t, layer, u);
             const SegStream& st = U.st;
-            const int nq = st.rows * 4, per = (nq + 3) / 4;
-            const bool dual = per <= 16;
+            const int nq = st.rows * 4, per = q_per(st.rows);
+            const bool dual = per == 16;
             const int ql = dual ? (lane & 15) : lane;   // the lane's query within the quadrant
             const int qi = per * warp + ql;
             const bool qvalid = ql < per && qi < nq;
@@ -570,11 +597,7 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
             else
                 softmax_tiles<kKT, false>(ss);
             gt += U.T;
-            // every q.K of this unit is done (the softmax read each S): the next
-            // unit's queries may overwrite the buffer while this one finishes
-            // (loading them during the last tile instead measured slower)
             const int un = next_unit_warp(bars, m, abortp);
-            if (un >= 0) load_q_async(sQ, q, unit_of(t, layer, un), tid);
             if (!abortp->flag) mbar_wait(su32(&bars->o_done[(gt - 1) % kSBuf]), ((gt - 1) / kSBuf) & 1, abortp);
             tc_fence_after();
             if (wact) {
@@ -642,11 +665,6 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
             // O is read: the next unit's first P.V (which overwrites it) waits for
             // this thread's next p_full arrival
             tc_fence_before();
-            if (un >= 0) {   // the next unit's queries, copied by this thread, are visible
-                asm volatile("cp.async.wait_all;" ::: "memory");
-                fence_async_smem();
-                mbar_arrive(su32(&bars->q_ready));
-            }
             if (mode == kMergeLastCta) {
                 // every CTA of (stream, KV head) counts its arrival after its records
                 // are visible; the last one merges and resets the counter
@@ -714,8 +732,10 @@ int launch_attn_partials_tc(const SegTable& t0, int layer, const uint16_t* q, fl
     const int n_units = (t.n_items - t.n_items_mma) * TF_NKV;
     const int slots = grid_cap > 0 ? grid_cap : 2 * sm_count();   // two CTAs per SM, all resident
     const int grid = n_units < slots ? n_units : slots;
+    CUtensorMap qmap;
+    if (!encode_q_map(&qmap, q, t.R)) return cuda_fail(cudaErrorInvalidValue);
     return launch_pdl(attn_partials_tc_kernel, dim3(grid), dim3(kThreads), kSmemBytes, stream, t, layer, q, po, pml,
-                      out, full, n_units);
+                      out, full, n_units, qmap);
 }
 
 }  // namespace tf

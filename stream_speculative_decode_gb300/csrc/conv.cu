@@ -112,9 +112,9 @@ conv_rows_kernel(SegTable t, int layer, const uint16_t* __restrict__ bcx,
         const int j = slot + k * kSlots;
         if (j < n) {
             const uint16_t* row = bcx + size_t(row_base + j) * TF_CIN + c;
-            B[k] = __ldcs(reinterpret_cast<const uint4*>(row));
-            C[k] = __ldcs(reinterpret_cast<const uint4*>(row + TF_H));
-            X[k] = __ldcs(reinterpret_cast<const uint4*>(row + 2 * TF_H));
+            B[k] = __ldg(reinterpret_cast<const uint4*>(row));
+            C[k] = __ldg(reinterpret_cast<const uint4*>(row + TF_H));
+            X[k] = __ldg(reinterpret_cast<const uint4*>(row + 2 * TF_H));
         }
     }
     uint4 wv[3];   // taps of channels c..c+7: 24 bf16, element (channel j, tap k) at 3*j+k

@@ -80,6 +80,21 @@ bool encode_kv_map(CUtensorMap* out, const void* base, int keys, int cap) {
 
 }  // namespace
 
+bool encode_q_map(CUtensorMap* out, const void* q, int rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    // (d, query head, row) of extents (64, 32, rows); a box is 4 heads of 4 rows
+    // (16 query rows of 128 bytes), 128-byte swizzle; rows past `rows` read as zeros
+    const cuuint64_t dims[3] = {cuuint64_t(TF_D), cuuint64_t(TF_NQ), cuuint64_t(rows)};
+    const cuuint64_t strides[2] = {cuuint64_t(TF_D) * 2, cuuint64_t(TF_NQ) * TF_D * 2};
+    const cuuint32_t box[3] = {cuuint32_t(TF_D), 4u, 4u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool encode_w2_map(CUtensorMap* out, const void* w2, int rows) {
     auto enc = tensor_map_encoder();
     if (!enc) return false;

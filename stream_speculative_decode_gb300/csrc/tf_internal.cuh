@@ -105,6 +105,10 @@ int attn_path_of(int rows);
 // boxes of 128 rows x 64 columns with 128-byte swizzle; rows past `rows` read
 // as zeros. False when the driver refuses it.
 bool encode_w2_map(CUtensorMap* out, const void* w2, int rows);
+// segments.cu: TMA map of the queries bf16 [rows][TF_NQ][TF_D] as (d, head, row),
+// boxes of 4 heads x 4 rows (16 query rows of one KV head's group), 128-byte
+// swizzle; rows past `rows` read as zeros. False when the driver refuses it.
+bool encode_q_map(CUtensorMap* out, const void* q, int rows);
 
 }  // namespace tf
 
