@@ -10,21 +10,23 @@
  *             per-stream attention partials; float64 attention and a host
  *             replay of the conv steps as the checks);
  *           - commit "a verify's greedy rows take the GPU's pick of their
- *             logits" (first largest logit, ties to the lower id, nonfinite
- *             rows flagged);
+ *             logits" (the largest logit, the lowest id among equal ones,
+ *             nonfinite rows flagged);
  *           - commit "the conv, qk, attention and merge kernels' bodies as
  *             inline functions" (qk, attention, merge);
  *           - section "Failures the tests catch" (a scratch too small for
  *             per-stream partials; a table reaching memory it did not declare).
  *   [DSP]   PR #1391 "lfm2: draft with LiquidAI's DSpark drafter (--drafter)":
- *           the lane core verifies every draft; the target's attention keeps
- *           its causal count; the drafter's block attention ("a FULL template
- *           flag, every block row seeing the keys [0, len + 1)"), its Markov
- *           head ("adds W2 W1[previous token] to each row's logits and takes
- *           the argmax, one row after the other"; the step as the argmax of
- *           bf16(base + bf16(W2 . W1[prev])), ties to the lowest token, a NaN
- *           score flagged) and the held path's copy of the drafter's picks
- *           into the verify's ids (a bad pick "sets a flag the verify reads").
+ *           every draft is verified by the target; the target's attention
+ *           stays causal; the drafter's block attention (the same kernels
+ *           with a FULL flag, under which every row of a block sees all of
+ *           its stream's keys), its Markov head (each draft row adds the
+ *           product of W2 with the W1 row of the previous pick to its logits
+ *           and takes the argmax, the rows in sequence; the step as the
+ *           argmax of bf16(base + bf16(W2 . W1[prev])), lowest token on a
+ *           tie, a NaN score flagged) and the held path's kernel that fills
+ *           the verify's ids from the drafter's picks (a bad pick raises a
+ *           flag for the verify instead of becoming a token).
  *
  * Conventions for every call:
  *   - All tensors are dense, row-major, in DEVICE memory owned by the caller,
@@ -73,8 +75,8 @@ typedef enum {
 struct CUstream_st;                       /* cudaStream_t is struct CUstream_st* */
 typedef struct CUstream_st* tf_cuda_stream;
 
-/* One stream of a shared round ([SRD] "a table of the streams' cache
- * addresses, row offsets and key counts").
+/* One stream of a shared round ([SRD]: the table lists each stream's cache
+ * addresses, row offset and key count).
  *   rows        window rows r_s = 1 + drafts, 1..TF_MAX_ROWS
  *   row_offset  first row of the stream in every [R][...] tensor; streams are
  *               packed in order: row_offset_0 = 0, row_offset_{s+1} =
@@ -95,7 +97,7 @@ typedef struct {
     int32_t n_streams;
     int32_t n_rows;           /* R = sum of rows */
     int32_t max_rows;
-    int32_t n_conv_tiles;     /* 8-row conv tiles ([SRD] "8-row tiles") */
+    int32_t n_conv_tiles;     /* conv tiles of at most 8 rows ([SRD]) */
     int32_t n_attn_items;     /* (stream, key chunk) work items per KV head */
     int32_t attn_kernels;     /* partial-kernel launches per attention layer (1 or 2) */
     int32_t attn_merge_launch;/* 1 if tf_attn also launches the merge kernel */
@@ -134,8 +136,8 @@ int tf_segments_plan(const tf_stream* streams, int n_streams, tf_plan* out);
  *                to a bf16 [TF_NKV][kv_capacity][TF_D] cache (head-major)
  * Refuses (TF_EINVAL) null or misaligned pointers and any two buffers of the
  * table that overlap (conv states and histories across every stream and
- * layer; K and V caches likewise) -- the bug class of [SRD]'s planted controls
- * "every stream reading or writing the first stream's conv state or kv cache".
+ * layer; K and V caches likewise) -- the bug class of [SRD]'s planted controls,
+ * in which every stream reads or writes stream 0's conv state or KV cache.
  * The table is copied to the device on `stream` before the call returns; the
  * host arrays may be freed at once. *out is owned by the caller and released
  * with tf_segments_free. */
@@ -152,13 +154,13 @@ int tf_segments_free(tf_segments* seg);
 int tf_segments_query(const tf_segments* seg, tf_plan* out);
 
 /* Bytes of partial scratch tf_attn_partials writes and tf_attn_merge reads
- * ([SRD] "the scratch's attention partials now hold each stream's apart").
+ * ([SRD]: each stream keeps its own partials in the scratch).
  * Layout: float o[n_partials][TF_D], then float2 ml[n_partials] (m, l).
  * 0 for a NULL table. */
 size_t tf_partials_bytes(const tf_segments* seg);
 
 /* a1. LFM2 gated short conv of one conv layer over every row of every stream
- * ([SRD]: "short conv (30 layers)", run once a layer over every row).
+ * ([SRD]: the 30 short-conv layers, each run once over every row).
  *   bcx  bf16 [R][TF_CIN], row = (B, C, x)
  *   w    bf16 [TF_H][TF_KW] depthwise taps; w[c][0] multiplies the oldest row
  *   y    float [R][TF_H] output, y = C * conv
@@ -172,16 +174,23 @@ int tf_conv_rows(const tf_segments* seg, int conv_layer, const void* bcx,
 
 /* a2. Causal GQA attention partials of one attention layer: for every stream,
  * KV head, key chunk, window row and query head, (m, l, o) over the chunk's
- * visible keys ([SRD] "qk, attention and merge (10 layers)"). Streams with
- * windows of 13 rows or more run on the tcgen05 tensor-core kernel, the others
+ * visible keys ([SRD]: the qk, attention and merge of the 10 attention
+ * layers). Streams with windows of 13 rows or more run on the tcgen05
+ * tensor-core kernel, the others
  * on the mma.sync kernel; the choice depends on the stream alone (so a
  * stream's bits do not depend on its round), and a round holding both kinds
  * makes one launch of each (tf_plan.attn_kernels). The environment variable
  * TF_ATTN_PATH=mma|tc, read by tf_segments_build, forces one kernel for every
  * window of at most 16 rows (a prompt table's wider windows always run on the
  * tensor cores); the mma.sync kernel takes a window as items of at most 8
- * rows. Values of V must lie within fp16's range (|v| < 65504): P.V runs in
- * fp16 with fp32 accumulation.
+ * rows. P.V runs with P and V in fp16 and fp32 accumulation; a piece of work
+ * whose fp16 result holds a partial sum that is not finite (a V of 65,536 or
+ * more has no fp16 value) or whose partial outputs |o|/l all lie below 2^-10
+ * is computed again with V in bf16 and P split into a bf16 high part and a
+ * bf16 remainder (the mma.sync kernel per item, the tensor-core kernel per
+ * unit of one chunk and KV head, in the launch's last CTA). So every finite
+ * V is supported; in an fp16 result only values of V below 2^-14 round, by
+ * at most 2^-25 each. Sums of P.V must stay within fp32's range.
  *   q         bf16 [R][TF_NQ][TF_D]
  *   partials  device scratch of tf_partials_bytes(seg) bytes. Record of
  *             stream s, chunk c, KV head g, row i, head 4g+hh:
@@ -199,8 +208,12 @@ int tf_attn_partials(const tf_segments* seg, int attn_layer, const void* q,
  * output directly and a stream with few partial records (4 * rows * chunks
  * <= 512) is merged by the last CTA to finish each of its KV heads (counted
  * by per-layer counters in the table that reset themselves); streams with
- * more records are merged by one merge launch. ([SRD]: "one launch a layer
- * over every row".) Same arguments as tf_attn_partials plus `out`
+ * more records are merged by one merge launch. ([SRD]: each layer runs once
+ * over every row.) A round holding both kinds of window runs the mma.sync
+ * launch on a stream of the table's own, forked from `stream` and joined
+ * back to it before the call returns, so that the two launches run side by
+ * side; work queued on `stream` after the call waits for both. Same
+ * arguments as tf_attn_partials plus `out`
  * (float [R][TF_NQ][TF_D]); `partials` is the scratch of tf_partials_bytes.
  * Calls on the same table and layer must not overlap on the GPU.
  * Errors: TF_EINVAL. */
@@ -208,8 +221,9 @@ int tf_attn(const tf_segments* seg, int attn_layer, const void* q, void* partial
             tf_cuda_stream stream);
 
 /* The drafter's non-causal block attention ([DSP] lfm2_attn_block: the
- * target's attention "with a FULL template flag, every block row seeing the
- * keys [0, len + 1)"). Reading: len + 1 is the stream's key count including
+ * target's attention kernels with a FULL flag, under which every row of a
+ * block sees the keys [0, len + 1)). Reading: len + 1 is the stream's key
+ * count including
  * the block's own rows, so every window row sees all `keys` keys of its
  * stream (what the last row sees under the causal count). Same arguments,
  * records, kernels, chunking and errors as tf_attn_partials / tf_attn; the
@@ -234,7 +248,10 @@ int tf_attn_merge(const tf_segments* seg, const void* partials, float* out,
  *   q    bf16 [R][TF_NQ][TF_D], out float [R][TF_NQ][TF_D], as above.
  * Every GPU that loads the library holds the array until the process exits.
  * The first call on a device looks the array's device address up (with that
- * device current); make that first call before any stream capture. Calls
+ * device current); make that first call before any stream capture. The
+ * address is kept for the life of the process: a cudaDeviceReset (or
+ * anything else that unloads the library's module from a device) leaves it
+ * stale, so do not call tf_attn_static after one. Calls
  * share the one array: calls whose launches overlap on the GPU (different
  * streams at once) race and give wrong results. Nothing in the array has to
  * start at zero; each call writes every record it reads.
@@ -245,8 +262,9 @@ int tf_attn_merge(const tf_segments* seg, const void* partials, float* out,
 int tf_attn_static(const tf_segments* seg, int attn_layer, const void* q, float* out,
                    tf_cuda_stream stream);
 
-/* a4. Greedy pick of each row of bf16 logits ([SRD] lfm2_argmax: "the first
- * largest logit ... ties to the lower id, nonfinite rows flagged").
+/* a4. Greedy pick of each row of bf16 logits ([SRD] lfm2_argmax: the largest
+ * logit, the lowest id among equal largest values, and a flag on any row
+ * holding a nonfinite value).
  *   logits      bf16, row r at logits + r*row_stride (elements), V per row
  *   pick        int32 [R]: lowest id holding the row's largest value (-0 and
  *               +0 are equal); -1 when the row is flagged
@@ -259,7 +277,7 @@ int tf_argmax_rows(const void* logits, int R, int V, int64_t row_stride,
                    int32_t* pick, uint8_t* flag, tf_cuda_stream stream);
 
 /* a5. Greedy verify of every stream: the accepted-draft prefix length
- * ([DSP] "the lane core verifies every draft"; [SRD] verifyFn takes the pick
+ * ([DSP]: the target verifies every draft; [SRD] verifyFn takes the pick
  * for greedy rows, flagged rows are drawn on the host).
  *   ids         int32 [R]: row 0 of a window is the pending token, rows 1..
  *               the drafts
@@ -285,8 +303,8 @@ int tf_accept(const tf_segments* seg, const int32_t* ids, const int32_t* pick,
  * its block rows are packed stream after stream at draft row o_s - s (o_s its
  * window's row offset), R - S rows in all. Block row j of stream s scores
  *   score[v] = bf16(base[v] + bf16(W2[v] . W1[tok]))     (v < vocab)
- * with tok = prev[s] for j = 0 and the pick of row j-1 after that ("one row
- * after the other"); the dot accumulates in fp32 on the tensor cores and is
+ * with tok = prev[s] for j = 0 and the pick of row j-1 after that (the rows in
+ * sequence); the dot accumulates in fp32 on the tensor cores and is
  * rounded to nearest even, as is the sum. The pick is the lowest token with
  * the largest score.
  *   W1, W2      bf16 [vocab][TF_MK]
@@ -328,8 +346,8 @@ int tf_draft_ids(const tf_segments* seg, const int32_t* prev, const int32_t* dra
                  const uint8_t* draft_flag, int vocab, int32_t* ids, uint8_t* dflag,
                  tf_cuda_stream stream);
 
-/* A prompt (prefill) call of one stream ([SRD]: "Prompt calls and one-stream
- * windows keep their launches"; the per-stream kernels run them in their own
+/* A prompt (prefill) call of one stream ([SRD]: prompt calls and windows of a
+ * single stream still take the per-stream launches; those kernels run them in their own
  * 16-row tiles, here 32-row windows, which fill a 128-lane tensor-core tile
  * with their 4 query heads per KV head):
  * `rows` new rows (row 0 first) whose K/V are already in the cache, so the
@@ -361,9 +379,9 @@ int tf_prompt_build(int32_t rows, int32_t keys, int32_t kv_capacity,
  * results it could not compute (attention records; Markov rows get pick -1
  * and flag bit 1), sets a bit in the table's status word and returns. Nothing
  * faults and the context stays usable; the launch itself still reports
- * success, so the failure is read with tf_segments_status. No library
- * counterpart on the pages' side: the pages' Metal kernels have no device
- * waits of this kind.
+ * success, so the failure is read with tf_segments_status (the review of
+ * the drafter's held path asks that a failure flag of asynchronous work
+ * reach the host: PR #1391, its review of the held path).
  *
  * tf_set_wait_limit_ns sets the limit (process-wide) for every later launch;
  * a launch captured in a CUDA graph keeps the limit it was captured with.

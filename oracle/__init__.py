@@ -10,11 +10,11 @@ Sources (web pages about the TensorFold project):
     take the GPU's pick of their logits" (the greedy pick), "a shared round runs
     each layer's conv and attention once over all its streams" (segment table,
     float64 attention, host replay of the conv steps, per-stream partials), and
-    "kernel contract: ... four planted controls".
-  * PR #1391 "lfm2: draft with LiquidAI's DSpark drafter (--drafter)": "The lane
-    core verifies every draft"; the target keeps its causal count.
+    the commit on the kernel contract and its planted controls.
+  * PR #1391 "lfm2: draft with LiquidAI's DSpark drafter (--drafter)": the
+    target checks every draft; its attention stays causal.
   * The same PR's drafter side (``oracle/draft.py``): the Markov head's pick
-    and the copy of the drafter's picks into the verify's ids.
+    and the kernel that fills the verify's ids from the drafter's picks.
   * Issue #1374 "LFM2.5-24B-A2B on Metal: drafts with LiquidAI's DSpark drafter
     (proposal and gate)", section "What": a drafted reply equals its plain one.
 

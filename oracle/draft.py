@@ -4,16 +4,17 @@ Only the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline and
 reference legs use this module; the product never imports it.
 
 Source: PR #1391 "lfm2: draft with LiquidAI's DSpark drafter (--drafter)".
-  * The drafter's Markov head "adds W2 W1[previous token] to each row's logits
-    and takes the argmax, one row after the other"; its kernels do "a Markov
-    step's W1 gather, W2 dot ..., bias add and argmax, ties to the lowest
-    token, a NaN score flagged"; the family test states the step as the argmax
-    of ``bf16(base + bf16(W2 . W1[prev]))``; a later commit keeps W2 in bf16
-    ("a bf16 scan"). -> ``markov_step``, ``markov_chain``, ``markov_all``.
-  * The held path: "a new kernel, lfm2_draft_ids, copies each window's drafts
-    from the drafter's picks into the verify's ids"; after review it no longer
-    maps an invalid id to 0 or ignores a nonfinite pick but "sets a flag the
-    verify reads". -> ``draft_ids_all``.
+  * The drafter's Markov head adds to each draft row's logits the product of
+    W2 with the W1 row of the previous pick and takes the argmax, the rows in
+    sequence; a Markov step's kernels gather the W1 row, take the W2 dot, add
+    the bias and take the argmax (lowest token on a tie, a NaN score
+    flagged); the family test states the step as the argmax of
+    ``bf16(base + bf16(W2 . W1[prev]))``; a later commit scans W2 in bf16.
+    -> ``markov_step``, ``markov_chain``, ``markov_all``.
+  * The held path: a kernel, lfm2_draft_ids, fills each verify window's ids
+    from the drafter's picks; after review an invalid id or a nonfinite pick
+    is no longer turned into token 0 or ignored but raises a flag that the
+    verify checks. -> ``draft_ids_all``.
 
 bf16 tensors are ``numpy.uint16`` bit patterns, as in ``oracle.step``.
 """
@@ -63,13 +64,13 @@ def markov_step(base, W1, W2, prev):
     ``score[v] = bf16(base[v] + bf16(W2[v] . W1[prev]))``: the dot of W2's row v
     with the previous token's W1 row, rounded once to bf16; added to the row's
     base logit and rounded once more. The pick is the first largest score
-    (ties to the lower token); a row with a nonfinite score is flagged and its
+    (the lowest token on a tie); a row with a nonfinite score is flagged and its
     pick is -1.
 
-    Readings: the "bias" the pages' kernel adds is the row's base logit (the
+    Readings: the bias the pages' kernel adds is the row's base logit (the
     family test's formula has no other term); the dot is exact (float64, whose
-    error is far below a bf16 rounding step) before its rounding; "a NaN score
-    flagged" covers every nonfinite score (NaN, +Inf, -Inf) as the verify's
+    error is far below a bf16 rounding step) before its rounding; the flag on
+    a NaN score covers every nonfinite score (NaN, +Inf, -Inf) as the verify's
     greedy pick does; a previous token outside [0, V) flags the row (no W1 row
     to gather).
 
@@ -90,7 +91,7 @@ def markov_step(base, W1, W2, prev):
 
 
 def markov_chain(base_rows, W1, W2, prev0):
-    """The Markov steps of one stream's block, one row after the other.
+    """The Markov steps of one stream's block, row by row in sequence.
 
     Row 0's previous token is the stream's pending token ``prev0``; row j's is
     row j-1's pick, so a flagged row (pick -1) flags every row after it.
@@ -148,8 +149,8 @@ def draft_ids_all(streams, prev, drafts, draft_flag, vocab):
     token or draft outside [0, vocab), or a draft whose pick is flagged
     (``draft_flag``, may be None), is written as -1 -- an id the verify never
     accepts -- and sets ``DFLAG_BAD_PENDING`` / ``DFLAG_BAD_DRAFT`` in the
-    stream's flag, which the verify's caller reads (the pages: the copy "sets a
-    flag the verify reads" instead of mapping a bad id to 0).
+    stream's flag, which the verify's caller reads (the pages: the copy raises
+    a flag for the verify instead of turning a bad id into token 0).
 
     Returns ids int32 [R], dflag uint8 [S].
     """

@@ -62,12 +62,12 @@ def f64_to_bf16_rne(x):
 # ------------------------------------------------------------ a1: short conv
 
 def short_conv_stream(bcx, w, state, want_history=True):
-    """LFM2 gated short conv of one stream's window, one row after the other.
+    """LFM2 gated short conv of one stream's window, row by row.
 
     Source: PR #1377 "LFM2: shared-round decode", commit "a shared round runs
     each layer's conv and attention once over all its streams": the short conv
-    of each stream's rows runs with the stream's own conv state, and is checked
-    against "a host replay of the conv steps" -- this function is that replay.
+    of each stream's rows runs with the stream's own conv state, and the host
+    checks it by replaying the conv steps -- this function is that replay.
 
     Readings (the pages give no formula):
       * ``bcx`` row = (B, C, x), consecutive H-wide slices in that order.
@@ -137,10 +137,10 @@ def _visible(keys, rows, i, full=False):
     (their K/V are appended before attention); row i sits at position
     ``keys - rows + i`` and attends causally to itself and every earlier key.
     Source: PR #1391 "lfm2: draft with LiquidAI's DSpark drafter": the target's
-    attention instantiations "keep their causal count".
+    attention stays causal.
 
     ``full``: the drafter's block attention (same PR: the attention and merge
-    kernels "with a FULL template flag", every block row seeing the keys
+    kernels under a FULL flag, with every row of a block seeing the keys
     ``[0, len + 1)``). Reading: ``len + 1`` is the key count including the
     block's own rows, so every row sees all ``keys`` keys -- what the block's
     last row sees under the causal count.
@@ -156,7 +156,7 @@ def attention_stream(q, K, V, keys, rows, full=False):
 
     Source: PR #1377 "LFM2: shared-round decode", commit "a shared round runs
     each layer's conv and attention once over all its streams": the stream
-    attention is checked against "float64 attention".
+    attention is checked against attention computed in float64.
 
     Reading: query head h reads KV head h // 4; the score is
     ``(q . k) * 0.125``; softmax over the visible keys (``_visible``).
@@ -189,8 +189,8 @@ def attention_partials_stream(q, K, V, keys, rows, chunk, full=False):
     ``m = -inf, l = 0, o = 0``.
 
     Source: PR #1377 "LFM2: shared-round decode", commit "a shared round runs
-    each layer's conv and attention once over all its streams" ("the scratch's
-    attention partials now hold each stream's apart") and the commit "the conv,
+    each layer's conv and attention once over all its streams" (each stream
+    keeps its own attention partials in the scratch) and the commit "the conv,
     qk, attention and merge kernels' bodies as inline functions" (qk,
     attention, then a merge). The chunk size is not on the pages; it is a
     parameter here and must not change the merged result.
@@ -260,9 +260,9 @@ def argmax_rows(logits):
     """Greedy pick of each row of bf16 logits.
 
     Source: PR #1377 "LFM2: shared-round decode", commit "a verify's greedy
-    rows take the GPU's pick of their logits": each row's FIRST largest logit
-    is picked ("ties to the lower id") and a row with a nonfinite logit is
-    flagged.
+    rows take the GPU's pick of their logits": each row's largest logit is
+    picked, the lowest id winning among equal values, and a row with a
+    nonfinite logit is flagged.
 
     Readings: nonfinite means NaN, +Inf or -Inf; -0 and +0 are equal (so a tie
     between them goes to the lower id); a flagged row's pick is set to -1 (the
@@ -295,9 +295,9 @@ def accept_stream(ids, pick, flag, rows, keys, vocab):
     """Greedy verify of one stream's window: accepted-draft prefix length.
 
     Sources: PR #1377 "LFM2: shared-round decode", commit "a verify's greedy
-    rows take the GPU's pick of their logits" (greedy rows take the pick;
-    flagged rows are drawn on the host); PR #1391 / issue #1374 ("the lane core
-    verifies every draft, so a drafted reply equals its plain reply").
+    rows take the GPU's pick of their logits" (a greedy row takes the pick; the
+    host samples a flagged row); PR #1391 / issue #1374 (the target checks
+    every draft, so a reply with drafts equals the reply without).
 
     Reading: row 0 of the window is the pending token, rows 1..r-1 the drafts.
     Row j's pick is the target's next token after row j's input, so draft j+1
@@ -363,7 +363,7 @@ def verify_step(inp, vocab=None, want_conv_history=True):
     Parity unpinned (no values on the pages to pin them to): whether the
     pages' conv rounds exactly the gate product as read in
     ``short_conv_stream``; the pages' own partial layout; what the pages do
-    with a flagged row beyond "draw on the host".
+    with a flagged row beyond sampling it on the host.
 
     Returns a dict with y (list per conv layer), states (after the window),
     states_rewound, out (list per attention layer), pick, flag, accept tuple.

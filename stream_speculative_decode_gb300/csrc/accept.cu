@@ -1,10 +1,10 @@
 // a5: greedy verify of every stream's window and the conv-state rewind.
 //
-// PR #1391 "lfm2: draft with LiquidAI's DSpark drafter (--drafter)": the lane
-// core verifies every draft, so a drafted reply equals the plain one. PR #1377
-// "LFM2: shared-round decode", commit "a verify's greedy rows take the GPU's
-// pick of their logits": greedy rows take the pick; flagged rows are drawn on
-// the host.
+// PR #1391 "lfm2: draft with LiquidAI's DSpark drafter (--drafter)": the
+// target checks every draft, so a reply with drafts is the same as one without.
+// PR #1377 "LFM2: shared-round decode", commit "a verify's greedy rows take the
+// GPU's pick of their logits": a greedy row takes the GPU's pick, and the host
+// samples a flagged row itself.
 //
 // Reading: draft j+1 is accepted while rows 0..j are accepted, row j is not
 // flagged and pick[j] == ids[j+1]; the token after the prefix is pick[a]

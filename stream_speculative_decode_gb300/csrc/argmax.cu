@@ -1,8 +1,9 @@
 // a4: greedy pick over each row of bf16 logits.
 //
 // PR #1377 "LFM2: shared-round decode", commit "a verify's greedy rows take
-// the GPU's pick of their logits": each row's first largest logit is picked
-// ("ties to the lower id") and a row holding a nonfinite logit is flagged; the
+// the GPU's pick of their logits": each row's largest logit is picked, the
+// lowest id winning among equal values, and a row holding a nonfinite logit
+// is flagged; the
 // host used to scan the 128,000 bf16 logits of every row with the GPU idle.
 //
 // Design: a row is split over a thread-block cluster of `cl` CTAs (cl = 1..8,

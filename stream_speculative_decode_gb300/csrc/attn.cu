@@ -24,11 +24,11 @@
 // HBM bound: 256 bytes of K+V per key per KV head; the window's queries ride
 // along. Arithmetic intensity 4*rows flops per byte for each of q.k and P.V.
 //
-// The same kernels serve the drafter's block attention (PR #1391: the target's
-// attention and merge "with a FULL template flag", every block row seeing the
-// keys [0, len + 1)): with `full` set every window row sees all of the
-// stream's keys instead of its causal count; nothing else changes, and the
-// merge is shared (it reads only the records).
+// The same kernels serve the drafter's block attention (PR #1391: the
+// target's attention and merge kernels under a FULL flag, with every row of a
+// block seeing the keys [0, len + 1)): with `full` set every window row sees
+// all of the stream's keys instead of its causal count; nothing else changes,
+// and the merge is shared (it reads only the records).
 #include "attn_item.cuh"
 
 namespace tf {

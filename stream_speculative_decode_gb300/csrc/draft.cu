@@ -3,9 +3,9 @@
 // verify).
 //
 // PR #1391 "lfm2: draft with LiquidAI's DSpark drafter (--drafter)", the held
-// path: a kernel "copies each window's drafts from the drafter's picks into
-// the verify's ids"; after review, a nonfinite pick or an id past the
-// vocabulary is no longer mapped to 0 but "sets a flag the verify reads".
+// path: a kernel fills each verify window's ids from the drafter's picks;
+// after review, a nonfinite pick or an id past the vocabulary is no longer
+// turned into token 0 but raises a flag that the verify checks.
 //
 // Layout (reading): window row 0 of stream s is its pending token prev[s];
 // window row j >= 1 is the draft at packed draft row o_s - s + j - 1 (each

@@ -6,11 +6,11 @@
 // launch a step (markov_step_kernel, described here).
 //
 // PR #1391 "lfm2: draft with LiquidAI's DSpark drafter (--drafter)": the head
-// "adds W2 W1[previous token] to each row's logits and takes the argmax, one
-// row after the other"; its kernels do the W1 gather, the W2 dot, the add and
-// an argmax with ties to the lowest token and a NaN score flagged; the family
-// test states the step as the argmax of bf16(base + bf16(W2 . W1[prev])); W2
-// stays bf16 ("a bf16 scan").
+// adds to each draft row's logits the product of W2 with the W1 row of the
+// previous pick and takes the argmax, row by row in sequence; its kernels do
+// the W1 gather, the W2 dot, the add and an argmax that takes the lowest token
+// on a tie and flags a NaN score; the family test states the step as the
+// argmax of bf16(base + bf16(W2 . W1[prev])); W2 is scanned in bf16.
 //
 // One step is a skinny GEMM followed by an argmax: D[s][v] = E[s] . W2[v] with
 // E[s] = W1[tok_s], for up to 128 streams (MMA M = 128 TMEM lanes, one lane per

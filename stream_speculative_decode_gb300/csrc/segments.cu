@@ -2,9 +2,9 @@
 //
 // PR #1377 "LFM2: shared-round decode", commit "a shared round runs each
 // layer's conv and attention once over all its streams": the kernels run once
-// a layer over every row "from a table of the streams' cache addresses, row
-// offsets and key counts"; a stream of more than 8 rows is folded into 8-row
-// tiles; the attention partials hold each stream's apart. The same commit's
+// a layer over every row, driven by a table that lists each stream's cache
+// addresses, row offset and key count; streams longer than 8 rows are cut into
+// tiles of 8; each stream keeps its own attention partials. The same commit's
 // residency concern (a table reaching buffers nobody declared) becomes here a
 // host check that the table's buffers are valid, aligned and never overlap.
 #include <algorithm>

@@ -6,8 +6,8 @@ graphs; every step of the path is a call into libtf.so.
 
 Layer order of the LFM2 stack modelled here: one attention layer after every
 third conv layer (30 conv + 10 attention layers, PR #1377 "LFM2: shared-round
-decode": "short conv (30 layers) and its qk, attention and merge (10
-layers)"); with other counts the attention layers are spread evenly.
+decode": a forward runs 30 short-conv layers and 10 layers of qk, attention and
+merge); with other counts the attention layers are spread evenly.
 """
 
 import numpy as np

@@ -12,8 +12,8 @@ Tolerances (stated once, used by every parity test):
   * Markov picks (the drafter's head): the tensor cores sum the 256 products
     of W2[v] . W1[tok] in fp32, the oracle exactly, so bf16(dot) may differ by
     one rounding step where the exact dot sits near a bf16 rounding boundary.
-    Rule (the pages check "the pick's score is below the row's best by more
-    than its bound"): with e = 2 * gamma_256 * sum_k |W2[v][k] W1[tok][k]|
+    Rule (the pages' own check compares the pick's score with the row's best
+    against an error bound): with e = 2 * gamma_256 * sum_k |W2[v][k] W1[tok][k]|
     (gamma_n = n u / (1 - n u), u = 2^-24, doubled for the tensor cores'
     accumulation), each token's score lies in [lo_v, hi_v] = the scores of the
     roundings of dot -+ e; the GPU's pick p must be a possible first argmax:

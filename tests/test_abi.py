@@ -89,7 +89,7 @@ def test_partial_count(T, total_rows):
     """The pages check the partial count at 1, 32 and 2,048 rows (PR #1377,
     commit "a shared round runs each layer's conv and attention once over
     all its streams"); the failure they guard is a count computed in a narrow
-    integer ("expected 262144, found 65536")."""
+    integer that wraps (their test reports a count four times too small)."""
     streams, off, s = [], 0, 0
     while off < total_rows:
         rows = min(1 + (s * 7) % 16, total_rows - off)
@@ -132,8 +132,8 @@ def _fake(base, i, span):
 
 
 def test_build_refuses_aliased_conv_state(T):
-    """The pages' planted control "every stream reading or writing the first
-    stream's conv state": the host refuses a table whose streams share one."""
+    """The pages' planted control of all streams reading or writing stream 0's
+    conv state: the host refuses a table whose streams share one."""
     streams = [(1, 0, 10, 16), (1, 1, 10, 16)]
     st = [0x10000, 0x10000]                      # both streams on one state
     kv = 1024 * 16
@@ -144,7 +144,7 @@ def test_build_refuses_aliased_conv_state(T):
 
 
 def test_build_refuses_aliased_kv(T):
-    """... and "every stream writing the first stream's kv cache"."""
+    """... and the control in which all streams write stream 0's KV cache."""
     streams = [(1, 0, 10, 16), (1, 1, 10, 16)]
     st = [0x10000, 0x10000 + 8192]
     k = [0x100000, 0x100000 + 4096]              # overlapping caches

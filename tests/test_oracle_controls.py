@@ -1,14 +1,14 @@
 """Planted controls: copies of the oracle with one mistake each must fail the
 pins. The pages' kernel contract plants four such controls (PR #1377 "LFM2:
-shared-round decode", commit "kernel contract: LFM2's shared-round launches
-carry recorded M1/M2 limits and four planted controls": a tie to the highest
-id, a nonfinite logit not flagged, every stream reading or writing the first
-stream's conv state or KV cache); the rest guard the readings the pins fix.
-The draft side's controls follow the pages' drafter contract (PR #1391 "lfm2:
-draft with LiquidAI's DSpark drafter", the commit that gives the Markov scan and
-pick, the draft ids and the block attention their planted controls: a NaN score
-not flagged, every stream reading the first stream's previous token, a pick
-past the vocabulary keeping its token, a block row missing the last key).
+shared-round decode", its kernel-contract commit): a pick that takes the
+highest id on a tie, a row with a nonfinite logit left unflagged, and all
+streams sharing stream 0's conv state or KV cache (for reads or writes); the
+rest guard the readings the pins fix. The draft side's controls follow the
+pages' drafter contract (PR #1391 "lfm2: draft with LiquidAI's DSpark
+drafter", the commit adding controls for the Markov head, the draft ids and
+the block attention): a NaN score left unflagged, all streams taking stream
+0's previous token, a pick beyond the vocabulary kept as a token, a block row
+that misses the last key.
 The mistakes are planted in the oracle's source, on the CPU.
 """
 

@@ -6,9 +6,10 @@ an allocator or pool it does not own, or a runtime that hands the library only
 the tensors it reads and writes. For them tf_attn_static runs one attention
 layer (partials, then merge) with the partial scratch in a fixed array
 compiled into the library. These tests call it through the C ABI and compare
-it with the usual tf_attn_partials + tf_attn_merge pair, within the attention
-tolerance of the parity tests, on calls in a row (each later call finds the
-earlier call's records in the shared array).
+it with the usual tf_attn_partials + tf_attn_merge pair and with the float64
+oracle, within the attention tolerance of the parity tests, on calls in a row
+(each later call finds the earlier call's records in the shared array), and
+check that a call leaves the device's free memory unchanged.
 """
 
 import numpy as np
@@ -65,6 +66,35 @@ def test_static_scratch_matches_partials_and_merge(mods):
     for _ in range(2):
         check_attn(_static(mods, d2, 0), want2.astype(np.float64), "static scratch, second table")
     d2.free()
+
+
+def test_static_scratch_matches_float64_and_allocates_nothing(mods):
+    """On a round holding both kinds of window (so both attention kernels and
+    the merge launch run), the static call's output meets the float64 oracle at
+    the parity tolerance, and after a first call the device's free memory
+    (cudaMemGetInfo) is the same before and after each further call: the call
+    allocates nothing."""
+    from oracle import step as O
+    tf, inputs, step, torch = mods
+    w = inputs.Workload("no-alloc-3", [16, 5, 1, 13], [80000, 2600, 90, 700], 0, 1, vocab=1000,
+                        drafts="random", seed=23)
+    inp = inputs.make_inputs(w, backend="numpy")
+    d = step.DeviceStep(inp)
+    assert d.seg.plan["attn_kernels"] == 2 and d.seg.plan["attn_merge_launch"] == 1
+    ref = O.attention_layer(inp.streams, inp.q[0], inp.K[0], inp.V[0])
+    out = torch.full_like(d.out[0], float("nan"))
+    tf.tf_attn_static(d.seg, 0, d.q[0], out)       # first call: looks the array's address up
+    torch.cuda.synchronize()
+    for _ in range(2):
+        out.fill_(float("nan"))
+        torch.cuda.synchronize()
+        free0, _total = torch.cuda.mem_get_info()
+        tf.tf_attn_static(d.seg, 0, d.q[0], out)
+        torch.cuda.synchronize()
+        free1, _total = torch.cuda.mem_get_info()
+        assert free1 == free0, (free0, free1)
+        check_attn(out.cpu().numpy(), ref, "static scratch against float64")
+    d.free()
 
 
 def test_static_scratch_refuses_oversized_table(mods):
