@@ -155,9 +155,11 @@ struct SoftState {
     float l;             // sum of 2^(s*log2e/8 - mref) over the keys so far
 };
 
-// DUAL: this thread owns half of each tile's keys (the other half of its
-// lane's row is written as P = 0, so P.V sums over its half only); the row's
-// max is shared with the partner lane (lane ^ 16) so both use one reference.
+// DUAL (windows of at most 16 rows: the query rows sit on lanes 0-15 of each
+// quadrant): threads L and L + 16 of a warp share TMEM lane L (the 16x32bx2
+// load and store shape), thread L owning keys 0-31 of each tile and columns
+// 0-31 of O, thread L + 16 keys 32-63 and columns 32-63; the row's max and sum
+// are shared through one shuffle. Otherwise a thread owns its lane's row.
 template <int KC, bool DUAL>
 __device__ __forceinline__ void softmax_tiles(SoftState& st) {
     const int lane = threadIdx.x & 31;
@@ -174,11 +176,14 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
             const int k0 = j * kKT + half * NV;      // chunk-local key of v[0]
             float v[NV];
             {
-                uint32_t r[KC];
-                tc_ld_n<KC>(st.trow + colS, r);
+                uint32_t r[NV];
+                if constexpr (DUAL)
+                    tc_ld16x2_32<KC / 2>(st.trow + colS, r);   // this half's 32 scores of lane L
+                else
+                    tc_ld_n<KC>(st.trow + colS, r);
                 tc_wait_ld();
 #pragma unroll
-                for (int c = 0; c < NV; ++c) v[c] = __uint_as_float(half ? r[NV + c] : r[c]);
+                for (int c = 0; c < NV; ++c) v[c] = __uint_as_float(r[c]);
             }
             if (j * kKT + kKT > st.lim_all) {   // the causal edge or the chunk's end lies in this tile
 #pragma unroll
@@ -209,19 +214,31 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
                     st.l *= alpha;
                 }
                 if (j >= 1) {
+                    if constexpr (DUAL) {   // this thread's 32 columns of O
 #pragma unroll 1
-                    for (int h = 0; h < 4; ++h) {   // O (64 columns)
-                        uint32_t o16[16];
-                        tc_ld16(st.trow + kColO + 16 * h, o16);
-                        tc_wait_ld();
-                        uint32_t a8[8], b8[8];
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t o16[16];
+                            tc_ld16x2_16<32>(st.trow + kColO + 16 * h, o16);
+                            tc_wait_ld();
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            a8[c] = __float_as_uint(__uint_as_float(o16[c]) * alpha);
-                            b8[c] = __float_as_uint(__uint_as_float(o16[8 + c]) * alpha);
+                            for (int c = 0; c < 16; ++c) o16[c] = __float_as_uint(__uint_as_float(o16[c]) * alpha);
+                            tc_st16x2_16<32>(st.trow + kColO + 16 * h, o16);
                         }
-                        tc_st8(st.trow + kColO + 16 * h, a8);
-                        tc_st8(st.trow + kColO + 16 * h + 8, b8);
+                    } else {
+#pragma unroll 1
+                        for (int h = 0; h < 4; ++h) {   // O (64 columns)
+                            uint32_t o16[16];
+                            tc_ld16(st.trow + kColO + 16 * h, o16);
+                            tc_wait_ld();
+                            uint32_t a8[8], b8[8];
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                a8[c] = __float_as_uint(__uint_as_float(o16[c]) * alpha);
+                                b8[c] = __float_as_uint(__uint_as_float(o16[8 + c]) * alpha);
+                            }
+                            tc_st8(st.trow + kColO + 16 * h, a8);
+                            tc_st8(st.trow + kColO + 16 * h + 8, b8);
+                        }
                     }
                     tc_wait_st();
                 }
@@ -236,14 +253,8 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
                 s4[c & 3] += p0 + p1;
                 own[c] = pack_h2(p0, p1);
             }
-            if constexpr (DUAL) {   // this half's P and zeros for the partner's half
-                uint32_t w[KC / 2];
-#pragma unroll
-                for (int c = 0; c < NV / 2; ++c) {
-                    w[c] = half ? 0u : own[c];
-                    w[NV / 2 + c] = half ? own[c] : 0u;
-                }
-                tc_st_n<KC / 2>(st.trow + colS, w);   // P (fp16 pairs) over the first KC/2 columns of S
+            if constexpr (DUAL) {   // P (fp16 pairs) of lane L: keys 0-31 at columns 0-15, 32-63 at 16-31
+                tc_st16x2_16<KC / 4>(st.trow + colS, own);
             } else {
                 tc_st_n<KC / 2>(st.trow + colS, own);
             }
@@ -293,18 +304,20 @@ __device__ __forceinline__ int q_per(int rows) { return rows <= 16 ? 16 : 32; }
 
 // The unit's queries into shared memory by TMA (one thread), K-major with the
 // 128-byte swizzle, lane L of the Q tile holding query per*(L/32) + L%per
-// (dual: + L%16, written twice): 8 boxes of 16 query rows (4 window rows x 4
+// (dual: lanes L%32 < 16 only): boxes of 16 query rows (4 window rows x 4
 // heads), completing `bar` with 16 KB. Rows past the window belong to no query
 // of the unit (other streams' rows, or zeros past the last row): their lanes
 // are not valid rows and their results are never written.
 __device__ __forceinline__ void issue_q(uint32_t sQ, const CUtensorMap* qmap, const Unit& U, uint32_t bar) {
-    mbar_expect_tx(bar, kQB);
     const bool dual = U.st.rows <= 16;
+    mbar_expect_tx(bar, dual ? kQB / 2 : kQB);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const int w = k >> 1, h = k & 1;
-        // dual: both halves of quadrant w hold window rows 4w..4w+3; else the
-        // halves hold rows 8w..8w+3 and 8w+4..8w+7
+        // dual: lanes 0-15 of quadrant w hold window rows 4w..4w+3 (lanes 16-31
+        // hold no query: their S rows are never read); else the halves hold
+        // rows 8w..8w+3 and 8w+4..8w+7
+        if (dual && h) continue;
         const int row = U.st.row_offset + (dual ? 4 * w : 8 * w + 4 * h);
         tma_load_3d(sQ + uint32_t(32 * w + 16 * h) * 128u, qmap, 0, 4 * U.g, row, bar);
     }
@@ -575,7 +588,6 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
             const int ql = dual ? (lane & 15) : lane;   // the lane's query within the quadrant
             const int qi = per * warp + ql;
             const bool qvalid = ql < per && qi < nq;
-            const bool owner = qvalid && (!dual || lane < 16);   // writes the row's record
             const bool wact = per * warp < nq;      // the warp holds at least one real row
             const int mode = out ? st.merge_mode : kMergeKernel;   // records only in the two-call form
             SoftState ss;
@@ -605,61 +617,71 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                 const bool aborted = abortp->flag != 0;
                 float f = 1.f;
                 if (ss.mtrue > ss.mref && ss.mref != -INFINITY) f = ex2(ss.mref - ss.mtrue);
-                uint32_t ro[64];
-                tc_ld64(trow + kColO, ro);
-                tc_wait_ld();
-                float lsum = ss.l;
-                if (dual) {   // the row's two halves (lanes L and L + 16)
+                // this thread's columns of O: all 64 of its lane, or (dual) its
+                // half [d0, d0 + 32) of lane L's row
+                auto finish = [&](auto& ro) {
+                    constexpr int ND = int(sizeof(ro) / sizeof(ro[0]));
+                    const int d0 = ND == 32 ? 32 * (lane >> 4) : 0;
+                    float lsum = ss.l;
+                    if (ND == 32) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 16);   // the row's two key halves
+                    // P.V ran with V in fp16. A row whose O is not finite (a V of
+                    // 65,536 or more has no fp16 value), or a warp whose rows'
+                    // outputs |o| / l all lie below 2^-10 (fp16's subnormal steps
+                    // of 2^-24 would cost relative precision), sends the unit to
+                    // the exact recompute at the end of the launch; its records
+                    // are rewritten there and its merge waits for them.
+                    bool nonfinite = false, big = false;
+                    if (qvalid && lsum > 0.f) {
+                        nonfinite = !isfinite(lsum);
 #pragma unroll
-                    for (int c = 0; c < 64; ++c)
-                        ro[c] = __float_as_uint(__uint_as_float(ro[c]) +
-                                                __uint_as_float(__shfl_xor_sync(0xFFFFFFFFu, ro[c], 16)));
-                    lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, 16);
-                }
-                // P.V ran with V in fp16. A row whose O is not finite (a V of
-                // 65,536 or more has no fp16 value), or a warp whose rows'
-                // outputs |o| / l all lie below 2^-10 (fp16's subnormal steps
-                // of 2^-24 would cost relative precision), sends the unit to
-                // the exact recompute at the end of the launch; its records
-                // are rewritten there and its merge waits for them.
-                bool nonfinite = false, big = false;
-                if (qvalid && lsum > 0.f) {
-                    nonfinite = !isfinite(lsum);
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) {
-                        const float v = __uint_as_float(ro[c]);
-                        nonfinite |= !isfinite(v);
-                        big |= fabsf(v) >= 0x1p-10f * lsum;
+                        for (int c = 0; c < ND; ++c) {
+                            const float v = __uint_as_float(ro[c]);
+                            nonfinite |= !isfinite(v);
+                            big |= fabsf(v) >= 0x1p-10f * lsum;
+                        }
                     }
-                }
-                const bool seen = __any_sync(0xFFFFFFFFu, qvalid && lsum > 0.f);
-                const bool redo = !aborted && (__any_sync(0xFFFFFFFFu, nonfinite) ||
-                                               (seen && !__any_sync(0xFFFFFFFFu, big)));
-                if (redo && lane == 0 && atomicMax(&bars->redo_m, m) < m)
-                    t.tc_redo[1 + atomicAdd(t.tc_redo, 1)] = u;
-                if (owner && mode == kMergeDirect) {   // the stream's only chunk: the output itself
-                    const float inv = aborted ? NAN : 1.f / lsum;   // a row always sees key 0 of its stream
-                    float4* dst = reinterpret_cast<float4*>(out_row(out, st, U.g, qi));
+                    const bool seen = __any_sync(0xFFFFFFFFu, qvalid && lsum > 0.f);
+                    const bool redo = !aborted && (__any_sync(0xFFFFFFFFu, nonfinite) ||
+                                                   (seen && !__any_sync(0xFFFFFFFFu, big)));
+                    if (redo && lane == 0 && atomicMax(&bars->redo_m, m) < m)
+                        t.tc_redo[1 + atomicAdd(t.tc_redo, 1)] = u;
+                    if (qvalid && mode == kMergeDirect) {   // the stream's only chunk: the output itself
+                        const float inv = aborted ? NAN : 1.f / lsum;   // a row always sees key 0 of its stream
+                        float4* dst = reinterpret_cast<float4*>(out_row(out, st, U.g, qi) + d0);
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        dst[c] = make_float4(__uint_as_float(ro[4 * c]) * inv, __uint_as_float(ro[4 * c + 1]) * inv,
-                                             __uint_as_float(ro[4 * c + 2]) * inv,
-                                             __uint_as_float(ro[4 * c + 3]) * inv);
-                } else if (owner) {
-                    const int64_t rec = st.pbase + (int64_t(U.chunk) * TF_NKV + U.g) * nq + qi;
-                    const bool empty = ss.mtrue == -INFINITY;
-                    float4* dst = reinterpret_cast<float4*>(part_o + rec * TF_D);
+                        for (int c = 0; c < ND / 4; ++c)
+                            dst[c] = make_float4(__uint_as_float(ro[4 * c]) * inv,
+                                                 __uint_as_float(ro[4 * c + 1]) * inv,
+                                                 __uint_as_float(ro[4 * c + 2]) * inv,
+                                                 __uint_as_float(ro[4 * c + 3]) * inv);
+                    } else if (qvalid) {
+                        const int64_t rec = st.pbase + (int64_t(U.chunk) * TF_NKV + U.g) * nq + qi;
+                        const bool empty = ss.mtrue == -INFINITY;
+                        float4* dst = reinterpret_cast<float4*>(part_o + rec * TF_D + d0);
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        float4 v = make_float4(__uint_as_float(ro[4 * c]) * f, __uint_as_float(ro[4 * c + 1]) * f,
-                                               __uint_as_float(ro[4 * c + 2]) * f,
-                                               __uint_as_float(ro[4 * c + 3]) * f);
-                        if (aborted) v = make_float4(NAN, NAN, NAN, NAN);
-                        else if (empty) v = make_float4(0.f, 0.f, 0.f, 0.f);
-                        dst[c] = v;
+                        for (int c = 0; c < ND / 4; ++c) {
+                            float4 v = make_float4(__uint_as_float(ro[4 * c]) * f, __uint_as_float(ro[4 * c + 1]) * f,
+                                                   __uint_as_float(ro[4 * c + 2]) * f,
+                                                   __uint_as_float(ro[4 * c + 3]) * f);
+                            if (aborted) v = make_float4(NAN, NAN, NAN, NAN);
+                            else if (empty) v = make_float4(0.f, 0.f, 0.f, 0.f);
+                            dst[c] = v;
+                        }
+                        if (d0 == 0)
+                            part_ml[rec] = aborted ? make_float2(NAN, INFINITY)
+                                                   : make_float2(ss.mtrue, empty ? 0.f : lsum * f);
                     }
-                    part_ml[rec] = aborted ? make_float2(NAN, INFINITY)
-                                           : make_float2(ss.mtrue, empty ? 0.f : lsum * f);
+                };
+                if (dual) {
+                    uint32_t r32[32];
+                    tc_ld16x2_32<32>(trow + kColO, r32);
+                    tc_wait_ld();
+                    finish(r32);
+                } else {
+                    uint32_t r64[64];
+                    tc_ld64(trow + kColO, r64);
+                    tc_wait_ld();
+                    finish(r64);
                 }
             }
             // O is read: the next unit's first P.V (which overwrites it) waits for
