@@ -90,13 +90,15 @@ __device__ __forceinline__ uint32_t ord_bf16(float best) {
     return (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
 }
 
-// The 128 base logits of one tile of the lane's row (bf16 pairs); zeros past
-// the vocabulary. The branch depends on the tile alone (uniform in the warp).
-__device__ __forceinline__ void load_base_tile(const uint16_t* brow, int v0, int vocab, uint32_t (&dst)[64]) {
-    if (v0 + kTileV <= vocab) {
+// The base logits of columns [v0, v0 + 2*NW) of a row as NW bf16 pairs, zeros
+// past the vocabulary (v0 a multiple of 8). The branch depends on the tile
+// alone (uniform across the threads that share it).
+template <int NW>
+__device__ __forceinline__ void load_base(const uint16_t* brow, int v0, int vocab, uint32_t (&dst)[NW]) {
+    if (v0 + 2 * NW <= vocab) {
         const uint4* bp = reinterpret_cast<const uint4*>(brow + v0);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
+        for (int k = 0; k < NW / 4; ++k) {
             const uint4 x = __ldcs(bp + k);   // read once: evict first
             dst[4 * k] = x.x;
             dst[4 * k + 1] = x.y;
@@ -105,13 +107,17 @@ __device__ __forceinline__ void load_base_tile(const uint16_t* brow, int v0, int
         }
     } else {
 #pragma unroll
-        for (int k = 0; k < 64; ++k) {
+        for (int k = 0; k < NW; ++k) {
             const int i0 = v0 + 2 * k;
             const uint32_t lo = i0 < vocab ? brow[i0] : 0u;
             const uint32_t hi = i0 + 1 < vocab ? brow[i0 + 1] : 0u;
             dst[k] = lo | (hi << 16);
         }
     }
+}
+// The 128 base logits of one tile of the lane's row.
+__device__ __forceinline__ void load_base_tile(const uint16_t* brow, int v0, int vocab, uint32_t (&dst)[64]) {
+    load_base<64>(brow, v0, vocab, dst);
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -135,20 +141,46 @@ __device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
     return d;
 }
 
-// 32 columns (ids v .. v+31, `n` of them inside the vocabulary): scores,
-// nonfinite bits and the running first largest.
-__device__ __forceinline__ void score_piece(const uint32_t (&r)[32], const uint32_t* base16, int v, int n,
-                                            float& best, int& bid, uint32_t& nf) {
-    uint32_t sc[16];
+// 32 scores as 16 bf16 pairs, by value, for the out-of-line paths below.
+struct Pairs16 {
+    uint32_t w[16];
+};
+// Columns [n, 32) lie past the vocabulary: the most negative finite value
+// there (never first, never flagged). Out of line: only the vocabulary's last
+// tile takes it, and the hot loops stay small enough for the instruction cache.
+__device__ __noinline__ Pairs16 mask_past_vocab(Pairs16 sc, int n) {
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-        sc[k] = add_bf16x2(cvt_bf16x2(__uint_as_float(r[2 * k + 1]), __uint_as_float(r[2 * k])), base16[k]);
-        if (n < 32) {   // past the vocabulary: the most negative finite value (never first, never flagged)
-            if (2 * k >= n) sc[k] = (sc[k] & 0xFFFF0000u) | 0xFF7Fu;
-            if (2 * k + 1 >= n) sc[k] = (sc[k] & 0x0000FFFFu) | 0xFF7F0000u;
-        }
-        nf |= (sc[k] & 0x7F807F80u) + 0x00800080u;   // bit 15 / 31: exponent all ones
+        if (2 * k >= n) sc.w[k] = (sc.w[k] & 0xFFFF0000u) | 0xFF7Fu;
+        if (2 * k + 1 >= n) sc.w[k] = (sc.w[k] & 0x0000FFFFu) | 0xFF7F0000u;
     }
+    return sc;
+}
+// The first of the 32 columns holding mv (out of line: taken only when the
+// running best improves, a few times a step).
+__device__ __noinline__ int first_column(Pairs16 sc, float mv) {
+    int c = 31;
+#pragma unroll
+    for (int k = 15; k >= 0; --k) {
+        if (bf_hi(sc.w[k]) == mv) c = 2 * k + 1;
+        if (bf_lo(sc.w[k]) == mv) c = 2 * k;
+    }
+    return c;
+}
+
+// The scores of 32 columns as 16 bf16 pairs (ids v .. v+31, `n` of them
+// inside the vocabulary): nonfinite bits and the running first largest.
+__device__ __forceinline__ void score_sums(uint32_t (&sc)[16], int v, int n, float& best, int& bid, uint32_t& nf) {
+    if (n < 32) {
+        Pairs16 p;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) p.w[k] = sc[k];
+        p = mask_past_vocab(p, n);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) sc[k] = p.w[k];
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) nf |= (sc[k] & 0x7F807F80u) + 0x00800080u;   // bit 15 / 31: exponent all ones
     uint32_t m8[8], m4[4];
 #pragma unroll
     for (int k = 0; k < 8; ++k) m8[k] = max_bf16x2(sc[2 * k], sc[2 * k + 1]);
@@ -157,15 +189,21 @@ __device__ __forceinline__ void score_piece(const uint32_t (&r)[32], const uint3
     const uint32_t m = max_bf16x2(max_bf16x2(m4[0], m4[1]), max_bf16x2(m4[2], m4[3]));
     const float mv = fmaxf(bf_lo(m), bf_hi(m));
     if (mv > best) {   // rare after the first tiles: find the first column holding mv
-        int c = 31;
+        Pairs16 p;
 #pragma unroll
-        for (int k = 15; k >= 0; --k) {
-            if (bf_hi(sc[k]) == mv) c = 2 * k + 1;
-            if (bf_lo(sc[k]) == mv) c = 2 * k;
-        }
+        for (int k = 0; k < 16; ++k) p.w[k] = sc[k];
+        bid = v + first_column(p, mv);
         best = mv;
-        bid = v + c;
     }
+}
+// 32 columns from their fp32 dot products: each rounded to bf16, plus the base.
+__device__ __forceinline__ void score_piece(const uint32_t (&r)[32], const uint32_t* base16, int v, int n,
+                                            float& best, int& bid, uint32_t& nf) {
+    uint32_t sc[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k)
+        sc[k] = add_bf16x2(cvt_bf16x2(__uint_as_float(r[2 * k + 1]), __uint_as_float(r[2 * k])), base16[k]);
+    score_sums(sc, v, n, best, bid, nf);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -707,6 +745,552 @@ markov_chain_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, int 
     }
 }
 
+
+// ---- the whole chain with W2 held on chip (tables of at most 64 streams) --
+//
+// Streaming W2 (65.5 MB at a 128,000-token vocabulary) through every step
+// makes a step cost one pass over it at the rate L2 delivers it to the SMs,
+// which measured no better than HBM's. Most of W2 fits on chip across the
+// 152 SMs instead: with at most 64 streams the step is computed transposed,
+// D[v][s] = W2[v] . E[s] (MMA M = 128 vocabulary rows, N = 32 or 64 streams,
+// K = 256), so that W2 is the A operand, which tcgen05 can read from tensor
+// memory. Each CTA (one per SM) keeps the first three of its W2 tiles in
+// tensor memory (128 columns each, written once at the start), the fourth in
+// shared memory (loaded once), and streams the rest through a ring of 16 KB
+// k-blocks every step; the ring refills while the CTAs meet between steps, so
+// one step reads a fraction of W2 from L2.
+//
+// Transposed, the accumulator holds one vocabulary row per TMEM lane and one
+// stream per column, while the argmax runs along the vocabulary. The epilogue
+// therefore passes each tile through shared memory: phase A (thread = TMEM
+// lane) rounds the lane's dot products to bf16 and stores them as
+// [stream][vocabulary] rows (16-byte chunks XOR-swizzled by the stream), then
+// phase B (thread = a stream and 128/N consecutive columns of it) reads its
+// columns back as bf16 pairs, adds the base logits (loaded two tiles ahead)
+// with one rounding, tests for nonfinite scores and keeps the first largest,
+// as the per-step kernel does. Two staging buffers, one barrier a tile.
+//
+// Between steps the CTAs meet through the table's scratch, three generations
+// deep: each CTA folds its 2 or 4 partial results per stream, atomicMax-es
+// them into one of eight keys per stream (CTA c into key c % 8, which keeps
+// same-address atomics few), counts its arrival, and once the count shows
+// every CTA every CTA reads the eight keys and the flags and takes the picks
+// itself, so no CTA has to publish them before the next step; CTA 0 writes the
+// outputs and clears the generation two steps ahead. Waits are bounded as in
+// the other kernels; a CTA that gives up raises the launch's abort word, and
+// CTA 0 marks the rows of the steps not done (flag bit 1).
+
+constexpr int kTmTiles = 3;       // W2 tiles a CTA holds in tensor memory
+constexpr int kSmTiles = 1;       // W2 tiles a CTA holds in shared memory
+constexpr int kKeyGroups = 8;     // per-stream keys CTAs meet in (CTA c in key c % 8)
+constexpr int kMaxDynSmem = 232448;
+constexpr int kRingMax = 12;
+constexpr uint32_t kHoldCols = 512;
+constexpr int kHoldEpi = 256;                     // epilogue threads: two groups of four warps
+constexpr int kHoldMmaWarp = 8, kHoldTmaWarp = 9;
+constexpr int kHoldThreads = kHoldEpi + 64;
+
+struct HoldBars {
+    uint64_t full[kRingMax];
+    uint64_t empty[kRingMax];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t e_ready;       // E holds the step's W1 rows (the 128 epilogue threads)
+    uint64_t tm_ready;      // the tensor-memory tiles are written (the 128 epilogue threads)
+    uint64_t res_full;      // the shared-memory tile has landed
+    uint64_t drain;
+    uint32_t tmem_base;
+    int32_t stop;           // epilogue thread 0's snapshot of the abort flag, read after a barrier
+    WaitCtl wc;
+    int32_t tok[64];        // the step's previous token of stream s, -1 if none or invalid
+    int32_t row[64];        // the step's draft row of stream s, -1 if it has none
+};
+
+template <int kN>
+struct Hold {
+    static constexpr int kEB = kKB * kN * 128;            // E: kN rows x 256, four k-blocks of kN x 128 B
+    static constexpr int kStgB = kN * kTileV * 2;         // one staging buffer: [stream][128 columns] bf16
+    static constexpr int kResB = kSmTiles * kKB * kSlabB;
+    static constexpr int kFixed = 1024 + kEB + kResB + 2 * kStgB + int(sizeof(HoldBars));
+    static constexpr int kRingFit = (kMaxDynSmem - kFixed) / kSlabB;
+    static constexpr int kRing = kRingFit < kRingMax ? kRingFit : kRingMax;
+    static constexpr int kSmem = kFixed + kRing * kSlabB;
+    static constexpr int kParts = kTileV / kN;            // phase-B threads per stream
+    static constexpr uint32_t kAcc = kTmTiles * 128;      // tensor-memory column of accumulator 0
+    // kind::f16, fp32 accumulate, A and B bf16 K-major, N = kN, M = 128
+    static constexpr uint32_t kIdesc =
+        (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kN >> 3) << 17) | (uint32_t(128 >> 4) << 24);
+    static_assert(kRing >= 4, "the ring holds at least one tile");
+    static_assert(kAcc + 2 * kN <= kHoldCols, "tiles and accumulators fit tensor memory");
+    static_assert(kParts * kN == kTileV && kN % 32 == 0, "phase-B split");
+};
+
+// tcgen05.mma with the accumulate flag as an immediate (0: overwrite D)
+template <int ACC>
+__device__ __forceinline__ void tc_mma_ss_acc(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+                 ::"r"(d), "l"(a), "l"(b), "r"(idesc), "n"(ACC) : "memory");
+}
+template <int ACC>
+__device__ __forceinline__ void tc_mma_ts_acc(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc) {
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+                 ::"r"(d), "r"(a), "l"(b), "r"(idesc), "n"(ACC) : "memory");
+}
+__device__ __forceinline__ void sts16(uint32_t a, uint32_t v) {
+    asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(static_cast<unsigned short>(v)) : "memory");
+}
+
+template <int kN>
+__global__ void __launch_bounds__(kHoldThreads, 1)
+markov_hold_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, const uint16_t* __restrict__ W2,
+                   int vocab, const uint16_t* __restrict__ base, int64_t base_stride,
+                   const int32_t* __restrict__ prev, int32_t* __restrict__ pick, uint8_t* __restrict__ flag,
+                   const __grid_constant__ CUtensorMap w2map) {
+    using C = Hold<kN>;
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = su32(smem_raw);
+    const uint32_t sbase = (raw + 1023u) & ~1023u;
+    unsigned char* gbase = smem_raw + (sbase - raw);
+    const uint32_t sE = sbase;
+    const uint32_t sRes = sE + C::kEB;
+    const uint32_t sRing = sRes + C::kResB;
+    const uint32_t sStg = sRing + C::kRing * kSlabB;
+    unsigned char* gStg = gbase + (sStg - sbase);
+    HoldBars* bars = reinterpret_cast<HoldBars*>(gStg + 2 * C::kStgB);
+    volatile WaitCtl* abortp = &bars->wc;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nt = (vocab + kTileV - 1) / kTileV;
+    const int t_begin = int((int64_t(blockIdx.x) * nt) / gridDim.x);
+    const int t_end = int((int64_t(blockIdx.x + 1) * nt) / gridDim.x);
+    const int ntl = t_end - t_begin;
+    const int nT = ntl < kTmTiles ? ntl : kTmTiles;                      // tiles [0, nT) in tensor memory
+    const int nR = ntl < kTmTiles + kSmTiles ? ntl : kTmTiles + kSmTiles;   // [nT, nR) in shared memory
+    const int ns = ntl - nR;                                             // [nR, ntl) streamed every step
+    // the i-th tile of a step: the first streamed tile (already in the ring
+    // when the step starts), the held tiles, then the other streamed ones
+    auto order = [&](int i) { return ns == 0 ? i : (i == 0 ? nR : (i <= nR ? i - 1 : i)); };
+    uint32_t* sync = t.mk_sync;                                          // [0] arrivals, [2] abort
+    uint32_t* gflags = sync + 64;                                        // [3][64]
+    unsigned long long* gkeys = reinterpret_cast<unsigned long long*>(sync + 256);   // [3][kKeyGroups][64]
+
+    if (tid == 0) {
+        for (int s = 0; s < C::kRing; ++s) {
+            mbar_init(su32(&bars->full[s]), 1);
+            mbar_init(su32(&bars->empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(su32(&bars->acc_full[b]), 1);
+            mbar_init(su32(&bars->acc_empty[b]), 4);   // the four warps of the accumulator's group
+        }
+        mbar_init(su32(&bars->e_ready), kHoldEpi);
+        mbar_init(su32(&bars->tm_ready), kHoldEpi);
+        mbar_init(su32(&bars->res_full), 1);
+        mbar_init(su32(&bars->drain), 1);
+        bars->wc.flag = 0;
+        bars->wc.limit_ns = t.wait_ns;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    pdl_wait();
+    if (warp == kHoldMmaWarp) tc_alloc(su32(&bars->tmem_base), kHoldCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == kHoldTmaWarp) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t keep = l2_evict_last();
+            {   // the tensor-memory tiles' rows (contiguous in W2) into L2 for the epilogue's loads
+                const int64_t r0 = int64_t(t_begin) * kTileV;
+                const int64_t r1 = min(int64_t(t_begin + nT) * kTileV, int64_t(vocab));
+                if (r1 > r0) l2_prefetch_bulk(W2 + r0 * TF_MK, uint32_t((r1 - r0) * TF_MK * 2));
+            }
+            bool res_issued = false;
+            if (nR > nT) {
+                mbar_expect_tx(su32(&bars->res_full), uint32_t(C::kResB));
+                for (int kb = 0; kb < kKB; ++kb)
+                    tma_load_2d_hint(sRes + kb * kSlabB, &w2map, kb * 64, (t_begin + nT) * kTileV,
+                                     su32(&bars->res_full), keep);
+                res_issued = true;
+            }
+            const int per_step = ns * kKB;
+            const int total = steps * per_step;
+            int issued = 0;
+            for (int i = 0; i < total; ++i) {
+                const int s = i % C::kRing;
+                if (i >= C::kRing && !mbar_wait(su32(&bars->empty[s]), ((i / C::kRing) - 1) & 1, abortp)) break;
+                const int il = i % per_step;
+                const uint32_t bar = su32(&bars->full[s]);
+                mbar_expect_tx(bar, kSlabB);
+                tma_load_2d_hint(sRing + s * kSlabB, &w2map, (il % kKB) * 64, (t_begin + nR + il / kKB) * kTileV,
+                                 bar, keep);
+                ++issued;
+            }
+            if (abortp->flag) {   // let the copies in flight land before the CTA exits
+                for (int i = issued > C::kRing ? issued - C::kRing : 0; i < issued; ++i)
+                    mbar_drain(su32(&bars->full[i % C::kRing]), (i / C::kRing) & 1);
+                if (res_issued) mbar_drain(su32(&bars->res_full), 0);
+            }
+        }
+        __syncwarp();
+    } else if (warp == kHoldMmaWarp) {
+        // ------------------------------------------------------------ MMA
+        // One thread issues every MMA, so the issue path is kept short:
+        // descriptors are formed once and advanced by constants (a shared-memory
+        // descriptor's address field counts 16-byte units), every K loop is
+        // unrolled, and the accumulate flag is an immediate.
+        if (lane == 0) {
+            const uint64_t dE0 = sdesc(sE, 16, 1024);
+            const uint64_t dRes0 = sdesc(sRes, 16, 1024);
+            const uint64_t dRing0 = sdesc(sRing, 16, 1024);
+            constexpr uint32_t kEkb = uint32_t(kN * 128) >> 4;   // E's k-block stride, 16-byte units
+            constexpr uint32_t kSlab16 = uint32_t(kSlabB) >> 4;
+            bool ok = true, tm_seen = false, res_seen = false;
+            int si = 0;   // streamed k-blocks consumed
+            for (int j = 0; j < steps && ok; ++j) {
+                ok = mbar_wait(su32(&bars->e_ready), j & 1, abortp);
+                if (!ok) break;
+                tc_fence_after();
+                for (int i = 0; i < ntl && ok; ++i) {
+                    const int gt = j * ntl + i, b = gt & 1;
+                    if (gt >= 2) {
+                        ok = mbar_wait(su32(&bars->acc_empty[b]), ((gt >> 1) - 1) & 1, abortp);
+                        if (!ok) break;
+                    }
+                    tc_fence_after();
+                    const int lt = order(i);
+                    const uint32_t d = tmem + C::kAcc + uint32_t(b * kN);
+                    if (lt < nT) {
+                        if (!tm_seen) {
+                            ok = mbar_wait(su32(&bars->tm_ready), 0, abortp);
+                            tm_seen = true;
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        const uint32_t a = tmem + uint32_t(lt * 128);   // A: 8 tensor-memory columns per 16 of K
+#pragma unroll
+                        for (int k = 0; k < TF_MK / 16; ++k) {
+                            const uint64_t db = dE0 + uint64_t((k >> 2) * kEkb + 2 * (k & 3));
+                            if (k == 0)
+                                tc_mma_ts_acc<0>(d, a, db, C::kIdesc);
+                            else
+                                tc_mma_ts_acc<1>(d, a + uint32_t(8 * k), db, C::kIdesc);
+                        }
+                    } else if (lt < nR) {
+                        if (!res_seen) {
+                            ok = mbar_wait(su32(&bars->res_full), 0, abortp);
+                            res_seen = true;
+                            if (!ok) break;
+                            tc_fence_after();
+                        }
+                        const uint64_t da0 = dRes0 + uint64_t(uint32_t(lt - nT) * kKB * kSlab16);
+#pragma unroll
+                        for (int k = 0; k < TF_MK / 16; ++k) {
+                            const uint64_t da = da0 + uint64_t((k >> 2) * kSlab16 + 2 * (k & 3));
+                            const uint64_t db = dE0 + uint64_t((k >> 2) * kEkb + 2 * (k & 3));
+                            if (k == 0)
+                                tc_mma_ss_acc<0>(d, da, db, C::kIdesc);
+                            else
+                                tc_mma_ss_acc<1>(d, da, db, C::kIdesc);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kb = 0; kb < kKB; ++kb) {
+                            const int s = si % C::kRing;
+                            if (!ok || !mbar_wait(su32(&bars->full[s]), (si / C::kRing) & 1, abortp)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint64_t da0 = dRing0 + uint64_t(uint32_t(s) * kSlab16);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                const uint64_t db = dE0 + uint64_t(kb * kEkb + 2 * k);
+                                if (kb == 0 && k == 0)
+                                    tc_mma_ss_acc<0>(d, da0, db, C::kIdesc);
+                                else
+                                    tc_mma_ss_acc<1>(d, da0 + uint64_t(2 * k), db, C::kIdesc);
+                            }
+                            tc_commit(su32(&bars->empty[s]));
+                            ++si;
+                        }
+                    }
+                    if (ok) tc_commit(su32(&bars->acc_full[b]));
+                }
+            }
+            tc_commit(su32(&bars->drain));
+            mbar_drain(su32(&bars->drain), 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue: two groups of 128 threads
+        // group wg takes the step-ordered tiles g with g % 2 == wg, accumulator wg and staging buffer wg
+        const int wg = tid >> 7, et = tid & 127;   // et: the TMEM lane (tile row) of phase A
+        const uint32_t tlane = tmem + (uint32_t((warp & 3) * 32) << 16);
+        const int ps = et % kN, ph = et / kN;   // phase B: stream ps, columns [ph*kN, ph*kN + kN) of a tile
+        const uint32_t stg = sStg + uint32_t(wg * C::kStgB);
+        auto wg_sync = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(1 + wg) : "memory"); };
+        auto all_sync = [&]() { asm volatile("bar.sync 3, 256;" ::: "memory"); };
+        int ps_rows = 0, ps_off = 0;
+        if (ps < t.S) {
+            const SegStream st = t.streams[ps];
+            ps_rows = st.rows;
+            ps_off = st.row_offset - ps;   // the stream's draft row of step j: ps_off + j
+        }
+        auto prefetch_base = [&](int jj) {   // this CTA's slice of stream tid's base row of step jj into L2
+            if (tid < t.S && jj < steps) {
+                const SegStream st = t.streams[tid];
+                if (st.rows - 1 > jj) {
+                    const int v_begin = t_begin * kTileV;
+                    const int v_end = min(t_end * kTileV, vocab);
+                    const uint32_t bytes = uint32_t(v_end - v_begin) * 2u & ~15u;
+                    if (bytes)
+                        l2_prefetch_bulk(base + int64_t(st.row_offset - tid + jj) * base_stride + v_begin, bytes);
+                }
+            }
+        };
+        // base logits of the step-ordered tile g (over all steps) for phase B
+        uint32_t bcur[kN / 2];
+        auto load_b = [&](int g) {
+            const int j = g / ntl, i = g - (g / ntl) * ntl;
+            if (j < steps && ps_rows - 1 > j)
+                load_base<kN / 2>(base + int64_t(ps_off + j) * base_stride, (t_begin + order(i)) * kTileV + ph * kN,
+                                  vocab, bcur);
+        };
+        if (tid < 64) {
+            int tok = -1, row = -1;
+            if (tid < t.S) {
+                const SegStream st = t.streams[tid];
+                if (st.rows > 1) {
+                    row = st.row_offset - tid;
+                    tok = prev[tid];
+                    if (tok < 0 || tok >= vocab) tok = -1;
+                }
+            }
+            bars->tok[tid] = tok;
+            bars->row[tid] = row;
+        }
+        prefetch_base(0);
+        load_b(wg);
+        all_sync();
+        int done_steps = 0;
+        for (int j = 0; j < steps; ++j) {
+            // E = the step's W1 rows (zero rows for streams without a token)
+            for (int idx = tid; idx < kN * (TF_MK / 8); idx += kHoldEpi) {
+                const int m = idx >> 5, c = idx & 31;
+                const int tok = bars->tok[m];
+                const uint16_t* src = tok >= 0 ? W1 + size_t(tok) * TF_MK + c * 8 : W1;
+                cp_async16(sE + (c >> 3) * (kN * 128) + m * 128 + (((c & 7) ^ (m & 7)) << 4), src, tok >= 0);
+            }
+            asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
+            fence_async_smem();
+            mbar_arrive(su32(&bars->e_ready));
+            if (j == 0) {
+                // the held tensor-memory tiles, group wg taking tiles wg, wg + 2, ...: lane et takes
+                // W2 row (tile start + et), 512 bytes, 64 columns at a time (zeros past the vocabulary)
+                for (int r = wg; r < nT; r += 2) {
+                    const int64_t vrow = int64_t(t_begin + r) * kTileV + et;
+                    const bool in = vrow < vocab;
+                    const uint4* src = reinterpret_cast<const uint4*>(W2 + (in ? vrow : 0) * TF_MK);
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        uint32_t w0[32], w1[32];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            const uint4 x = in ? __ldg(src + 16 * q + u) : make_uint4(0, 0, 0, 0);
+                            const uint4 y = in ? __ldg(src + 16 * q + 8 + u) : make_uint4(0, 0, 0, 0);
+                            w0[4 * u] = x.x; w0[4 * u + 1] = x.y; w0[4 * u + 2] = x.z; w0[4 * u + 3] = x.w;
+                            w1[4 * u] = y.x; w1[4 * u + 1] = y.y; w1[4 * u + 2] = y.z; w1[4 * u + 3] = y.w;
+                        }
+                        tc_st_n<32>(tlane + uint32_t(r * 128 + 64 * q), w0);
+                        tc_st_n<32>(tlane + uint32_t(r * 128 + 64 * q + 32), w1);
+                    }
+                }
+                tc_wait_st();
+                tc_fence_before();
+                mbar_arrive(su32(&bars->tm_ready));
+            }
+            prefetch_base(j + 1);
+
+            const bool valid = bars->tok[ps] >= 0;
+            float best = -INFINITY;
+            int bid = 0x7FFFFFFF;
+            uint32_t nf = 0;
+            bool ok = true;
+            for (int i = wg ^ ((j * ntl) & 1); i < ntl; i += 2) {   // this group's tiles of the step
+                const int gt = j * ntl + i;
+                // phase A: this lane's row of the tile, rounded to bf16, into the staging rows
+                // (a warp that gave up still meets every barrier of the step, doing no work)
+                if (ok && mbar_wait_warp(su32(&bars->acc_full[wg]), (gt >> 1) & 1, abortp)) {
+                    tc_fence_after();
+                    // the accumulator into registers and back to the MMA at once, then staged
+                    uint32_t a0[32], a1[32];
+                    tc_ld_n<32>(tlane + C::kAcc + uint32_t(wg * kN), a0);
+                    if constexpr (kN == 64) tc_ld_n<32>(tlane + C::kAcc + uint32_t(wg * kN + 32), a1);
+                    tc_wait_ld();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(su32(&bars->acc_empty[wg]));
+                    const uint32_t vo = uint32_t((et & 7) << 1), vc = uint32_t(et >> 3);
+                    auto stage = [&](const uint32_t (&a)[32], int s0) {
+#pragma unroll
+                        for (int k = 0; k < 32; k += 2) {
+                            const int s = s0 + k;
+                            const uint32_t p = cvt_bf16x2(__uint_as_float(a[k + 1]), __uint_as_float(a[k]));
+                            sts16(stg + uint32_t(s * 256) + (((vc ^ uint32_t(s & 7)) << 4) | vo), p);
+                            sts16(stg + uint32_t((s + 1) * 256) + (((vc ^ uint32_t((s + 1) & 7)) << 4) | vo),
+                                  p >> 16);
+                        }
+                    };
+                    stage(a0, 0);
+                    if constexpr (kN == 64) stage(a1, 32);
+                } else {
+                    ok = false;
+                }
+                wg_sync();
+                // phase B: stream ps, its kN columns of the tile, with their base logits
+                if (ok && valid) {
+                    const int v0 = (t_begin + order(i)) * kTileV;
+                    uint32_t r16[kN / 2];
+#pragma unroll
+                    for (int q = 0; q < kN / 8; ++q) {
+                        const uint32_t c = uint32_t(ph * (kN / 8) + q) ^ uint32_t(ps & 7);
+                        const uint4 x = lds128(stg + uint32_t(ps * 256) + (c << 4));
+                        r16[4 * q] = x.x;
+                        r16[4 * q + 1] = x.y;
+                        r16[4 * q + 2] = x.z;
+                        r16[4 * q + 3] = x.w;
+                    }
+#pragma unroll
+                    for (int p = 0; p < kN / 32; ++p) {
+                        const int v = v0 + ph * kN + 32 * p;
+                        if (v < vocab) {
+                            uint32_t sc[16];
+#pragma unroll
+                            for (int k = 0; k < 16; ++k) sc[k] = add_bf16x2(r16[16 * p + k], bcur[16 * p + k]);
+                            score_sums(sc, v, vocab - v < 32 ? vocab - v : 32, best, bid, nf);
+                        }
+                    }
+                }
+                load_b(gt + 2);
+                wg_sync();   // the staging buffer is read; the group's next tile may overwrite it
+            }
+            // ---- the CTAs meet: fold this CTA's parts of each stream, then its key per stream
+            unsigned long long* red = reinterpret_cast<unsigned long long*>(gStg);   // both buffers are free now
+            uint32_t* nfl = reinterpret_cast<uint32_t*>(red + kHoldEpi);
+            all_sync();
+            red[tid] = (valid && bid != 0x7FFFFFFF)
+                           ? (static_cast<unsigned long long>(ord_bf16(best)) << 32) |
+                                 static_cast<unsigned long long>(0xFFFFFFFFu - uint32_t(bid))
+                           : 0ull;
+            nfl[tid] = (nf & 0x80008000u) ? 1u : 0u;
+            all_sync();
+            const int b3 = j % 3;
+            if (tid < kN && bars->tok[tid] >= 0) {
+                unsigned long long k = 0;
+                uint32_t f = 0;
+#pragma unroll
+                for (int h = 0; h < 2 * C::kParts; ++h) {   // both groups' parts of stream tid
+                    const int e = (h / C::kParts) * 128 + (h % C::kParts) * kN + tid;
+                    k = max(k, red[e]);
+                    f |= nfl[e];
+                }
+                // (a thread whose wait gave up has raised the abort flag: this CTA then
+                // does not arrive, and the launch ends without these keys being read)
+                if (f)
+                    atomicOr(&gflags[b3 * 64 + tid], 1u);
+                else if (k)
+                    atomicMax(&gkeys[(b3 * kKeyGroups + int(blockIdx.x) % kKeyGroups) * 64 + tid], k);
+            }
+            if (blockIdx.x == 0) {   // clear the generation two steps ahead (read by every CTA before this step)
+                const int bn = (j + 1) % 3;
+                for (int idx = tid; idx < kKeyGroups * 64; idx += kHoldEpi) gkeys[bn * kKeyGroups * 64 + idx] = 0ull;
+                if (tid < 64) gflags[bn * 64 + tid] = 0u;
+            }
+            __threadfence();
+            all_sync();
+            if (tid == 0) {
+                if (!abortp->flag) {   // every wait of this CTA's step succeeded
+                    atomicAdd(sync, 1u);
+                    // every CTA has arrived (bounded: gives up on the wait limit or another CTA's abort)
+                    const uint32_t target = uint32_t(j + 1) * gridDim.x;
+                    const unsigned long long t0 = gtime(), limit = abortp->limit_ns;
+                    for (;;) {
+                        uint32_t g;
+                        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(g) : "l"(sync) : "memory");
+                        if (g >= target) break;
+                        if (abortp->flag || *reinterpret_cast<const volatile uint32_t*>(sync + 2) ||
+                            gtime() - t0 > limit) {
+                            abortp->flag = 1;
+                            break;
+                        }
+                        __nanosleep(32);
+                    }
+                }
+                bars->stop = abortp->flag ? 1 : 0;
+            }
+            all_sync();
+            if (bars->stop) break;
+            // the step's picks, taken by every CTA; CTA 0 writes them out
+            if (tid < 64) {
+                const int row = bars->row[tid], tok = bars->tok[tid];
+                int p = -1;
+                uint8_t f = 1;
+                if (row >= 0 && tok >= 0) {
+                    const uint32_t fl = __ldcg(&gflags[b3 * 64 + tid]);
+                    if (fl) {
+                        f = uint8_t(fl);
+                    } else {
+                        unsigned long long k = 0;
+#pragma unroll
+                        for (int g = 0; g < kKeyGroups; ++g)
+                            k = max(k, __ldcg(&gkeys[(b3 * kKeyGroups + g) * 64 + tid]));
+                        p = int(0xFFFFFFFFu - uint32_t(k & 0xFFFFFFFFull));
+                        f = 0;
+                    }
+                }
+                if (blockIdx.x == 0 && row >= 0) {
+                    pick[row] = p;
+                    flag[row] = f;
+                }
+                int ntok = -1, nrow = -1;
+                if (tid < t.S) {
+                    const SegStream st = t.streams[tid];
+                    if (st.rows - 1 > j + 1) {
+                        nrow = st.row_offset - tid + j + 1;
+                        ntok = (p >= 0 && p < vocab) ? p : -1;
+                    }
+                }
+                bars->tok[tid] = ntok;
+                bars->row[tid] = nrow;
+            }
+            done_steps = j + 1;
+            all_sync();
+        }
+        if (abortp->flag || done_steps < steps) {
+            abortp->flag = 1;
+            atomicExch(sync + 2, 1u);   // the other CTAs stop waiting
+            if (blockIdx.x == 0 && tid < t.S) {   // the rows of the steps not done
+                const SegStream st = t.streams[tid];
+                for (int j = done_steps; j + 1 < st.rows; ++j) {
+                    pick[st.row_offset - tid + j] = -1;
+                    flag[st.row_offset - tid + j] = 2;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    pdl_trigger();
+    if (tid == 0 && abortp->flag) atomicOr(t.status, uint32_t(TF_STATUS_MARKOV_TIMEOUT));
+    if (warp == kHoldMmaWarp) {
+        tc_fence_after();
+        tc_dealloc(tmem, kHoldCols);
+    }
+}
+
 }  // namespace
 }  // namespace tf
 
@@ -733,6 +1317,30 @@ extern "C" int tf_markov_chain(const tf_segments* seg, const void* W1, const voi
     const uint16_t* b = static_cast<const uint16_t*>(base);
     const char* path = std::getenv("TF_MARKOV_PATH");
     const bool per_step = (path && std::strcmp(path, "step") == 0) || t.S > kLanes;
+    const bool streamed = path && std::strcmp(path, "chain") == 0;
+    if (!per_step && !streamed && t.S <= 64) {
+        // W2 held on chip, the whole chain in one cooperative launch
+        auto* kern = t.S <= 32 ? markov_hold_kernel<32> : markov_hold_kernel<64>;
+        const int smem = t.S <= 32 ? Hold<32>::kSmem : Hold<64>::kSmem;
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return cuda_fail(e);
+        e = cudaMemsetAsync(t.mk_sync, 0, kMkSyncBytes, stream);   // arrivals, abort word, keys and flags
+        if (e != cudaSuccess) return cuda_fail(e);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(gx);
+        cfg.blockDim = dim3(kHoldThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, t, t.max_rows - 1, w1, static_cast<const uint16_t*>(W2), vocab, b,
+                               base_stride, prev, pick, flag, map);
+        if (e != cudaSuccess) return cuda_fail(e);
+        return launch_status();
+    }
     if (!per_step) {
         // the whole chain in one cooperative launch (every CTA resident: one per SM)
         e = cudaFuncSetAttribute(markov_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kChainSmemBytes);

@@ -248,7 +248,7 @@ int finish_build(tf_segments* seg, std::vector<tf::SegStream>& ss, std::vector<i
     const size_t o_mkf = off;      off = align_up(off + sizeof(uint32_t) * S, 256);
     const size_t o_mkc = off;      off = align_up(off + sizeof(uint32_t) * n_groups, 256);
     const size_t o_tcw = off;      off = align_up(off + sizeof(int32_t) * 2 * size_t(n_attn), 256);
-    const size_t o_mks = off;      off = align_up(off + sizeof(uint32_t) * 4, 256);
+    const size_t o_mks = off;      off = align_up(off + kMkSyncBytes, 256);
     const size_t n_tc_units = (items.size() - size_t(n_items_mma)) * TF_NKV;
     const size_t o_redo = off;     off = align_up(off + sizeof(int32_t) * (1 + n_tc_units), 256);
     const size_t o_st = off;       off = align_up(off + sizeof(uint32_t), 256);

@@ -77,7 +77,8 @@ struct SegTable {
     uint32_t* mk_flags;               // [S] Markov step: nonfinite / gave-up bits per stream, self-resetting
     uint32_t* mk_ctr;                 // [ceil(S/128)] Markov step: CTA arrivals per stream group
     int32_t* tc_work;                 // [n_attn][2] tensor-core attention: units handed out, CTAs done (self-resetting)
-    uint32_t* mk_sync;                // [4] Markov chain in one launch: arrivals, generation, abort (zeroed per launch)
+    uint32_t* mk_sync;                // Markov chain in one launch (kMkSyncBytes, zeroed per launch): [0] arrivals,
+                                      // [1] generation, [2] abort; from word 64 the per-step flags and keys
     int32_t* tc_redo;                 // tensor-core attention: [0] units queued for the exact recompute, [1..] them
     uint32_t* status;                 // TF_STATUS_* bits: a kernel gave up a bounded wait (tf_segments_status)
     unsigned long long wait_ns;       // limit of a device wait, set per launch from tf_set_wait_limit_ns
@@ -90,6 +91,10 @@ struct SegTable {
     int32_t tc_grid_mixed;
     int32_t pad3_;
 };
+
+// The Markov chain's scratch: 64 words of barrier state, then three
+// generations of 64 flag words (from word 64) and of 8 x 64 keys (from byte 1024).
+constexpr int kMkSyncBytes = 1024 + 3 * 8 * 64 * 8;
 
 constexpr int kAttnMma = 0;   // mma.sync flash-decode kernel (narrow windows)
 constexpr int kAttnTc = 1;    // tcgen05 + TMA kernel (windows of 13 rows or more)

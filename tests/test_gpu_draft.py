@@ -189,16 +189,18 @@ def test_markov_golden_cases(mods):
     assert n >= 9
 
 
-@pytest.mark.parametrize("path", [None, "step"])
+@pytest.mark.parametrize("path", [None, "chain", "step"])
 @pytest.mark.parametrize("vocab,rows", [
     (1000, [3, 1, 5, 2, 16, 4]),     # 8 W2 tiles of 128, one per CTA
     (1003, [2, 7, 1, 3]),            # a ragged last tile
     (20000, [4, 4, 9]),              # several tiles per CTA
 ])
 def test_markov_random(mods, vocab, rows, path, monkeypatch):
-    """The whole chain in one launch (tables of up to 128 streams) and one
-    launch per step (TF_MARKOV_PATH=step); each twice on the same table (the
-    scratch and the step barrier reset themselves)."""
+    """The whole chain in one launch with W2 held on chip (tables of up to 64
+    streams), the same with W2 streamed every step (TF_MARKOV_PATH=chain, the
+    form tables of 65-128 streams take) and one launch per step
+    (TF_MARKOV_PATH=step); each twice on the same table (the scratch and the
+    step barrier reset themselves)."""
     tf, inputs, _, _ = mods
     if path:
         monkeypatch.setenv("TF_MARKOV_PATH", path)
@@ -283,6 +285,44 @@ def test_markov_full_vocab_sampled(mods):
     assert n_exact >= n_rows - 1
     (_kind, r_inf, _i), = d.planted["nonfinite"]
     assert flag[r_inf] == 1 and pick[r_inf] == -1
+    seg.free()
+
+
+@pytest.mark.parametrize("path", [None, "chain"])
+@pytest.mark.parametrize("n_streams", [64, 40])
+def test_markov_held_w2_full_vocab_sampled(mods, monkeypatch, path, n_streams):
+    """Tables of 33-64 streams at a 127,997-token vocabulary (a ragged last
+    tile), where every CTA holds three W2 tiles in tensor memory and one in
+    shared memory and streams its other two or three every step: the chains
+    of eight streams (the longest among them) checked row by row against the
+    oracle from the GPU's own previous tokens, a planted NaN row flagged with
+    the rest of its chain, every row written; the same table through the
+    kernel that streams all of W2 (TF_MARKOV_PATH=chain) for comparison."""
+    tf, inputs, _, torch = mods
+    if path:
+        monkeypatch.setenv("TF_MARKOV_PATH", path)
+    vocab = 127_997
+    rng = np.random.default_rng(60 + n_streams)
+    rows = [int(r) for r in rng.integers(1, 17, size=n_streams)]
+    rows[int(rng.integers(n_streams))] = 16
+    w = inputs.Workload("markov-held", rows, list(rows), 0, 0, vocab=vocab, seed=61 + n_streams)
+    d = inputs.make_draft_inputs(w, nan_rows=1)
+    seg = _rows_table(tf, rows)
+    pick, flag = _markov_gpu(mods, seg, d.W1, d.W2, d.base, d.prev, vocab)
+    assert np.all((flag == 0) | (flag == 1)) and np.all(pick[flag == 0] >= 0)
+    chosen = sorted(set([int(np.argmax(rows))] + [int(x) for x in rng.choice(n_streams, size=7, replace=False)]))
+    n_rows = n_exact = 0
+    for s in chosen:
+        r, o, _k = d.streams[s]
+        tok = int(d.prev[s])
+        for j in range(r - 1):
+            k = o - s + j
+            n_exact += check_markov_row(pick[k], flag[k], d.base[k], d.W1, d.W2, tok, f"stream {s} row {j}")
+            n_rows += 1
+            tok = int(pick[k])
+    assert n_rows > 0 and n_exact >= n_rows - 1
+    (_kind, r_nan, _i), = d.planted["nonfinite"]
+    assert flag[r_nan] == 1 and pick[r_nan] == -1
     seg.free()
 
 

@@ -109,9 +109,10 @@ def _rows_table(tf, rows):
     return tf.tf_segments_build(streams, [], None, [], [], 0, 0)
 
 
-@pytest.mark.parametrize("path", [None, "step"])
+@pytest.mark.parametrize("path", [None, "chain", "step"])
 def test_markov_wait_runs_out_then_recovers(mods, wait_limit, path, monkeypatch):
-    """The Markov chain (one cooperative launch, or one launch per step with
+    """The Markov chain (one cooperative launch holding W2 on chip, the one
+    streaming it with TF_MARKOV_PATH=chain, or one launch per step with
     TF_MARKOV_PATH=step) with the wait limit at 0: rows it gave up on carry
     flag bit 1 and pick -1 (or were computed before the give-up), the status
     reports it; with the default limit the same table's chain matches the
