@@ -757,34 +757,39 @@ markov_chain_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, int 
 // memory. Each CTA (one per SM) keeps the first three of its W2 tiles in
 // tensor memory (128 columns each, written once at the start), the fourth in
 // shared memory (loaded once), and streams the rest through a ring of 16 KB
-// k-blocks every step; the ring refills while the CTAs meet between steps, so
-// one step reads a fraction of W2 from L2.
+// k-blocks every step; the streamed tiles come last in a step, so the ring
+// refills while the CTAs meet between steps and while the held tiles run.
 //
-// Transposed, the accumulator holds one vocabulary row per TMEM lane and one
-// stream per column, while the argmax runs along the vocabulary. The epilogue
-// therefore passes each tile through shared memory: phase A (thread = TMEM
-// lane) rounds the lane's dot products to bf16 and stores them as
-// [stream][vocabulary] rows (16-byte chunks XOR-swizzled by the stream), then
-// phase B (thread = a stream and 128/N consecutive columns of it) reads its
-// columns back as bf16 pairs, adds the base logits (loaded two tiles ahead)
-// with one rounding, tests for nonfinite scores and keeps the first largest,
-// as the per-step kernel does. Two staging buffers, one barrier a tile.
+// Transposed, each TMEM lane holds one vocabulary row and each column one
+// stream. The epilogue works lane-major: thread = lane = vocabulary row, and
+// two groups of four warps split the streams (group g takes streams
+// [g*N/2, (g+1)*N/2)). Per tile a thread rounds its dot products to bf16 two
+// streams at a time, adds the base logits (staged per tile in shared memory
+// by bulk copies: stream s's 128 logits as one 256-byte row), and keeps per
+// stream the largest score with its tile (packed bf16 compare and max; tiles
+// are visited in vocabulary order, so a strict compare keeps the first) and
+// a nonfinite bit. The argmax along the vocabulary is then taken once a
+// step: a shuffle reduction over the warp's lanes of (ordered score, lowest
+// row) keys, then over the four warps.
 //
 // Between steps the CTAs meet through the table's scratch, three generations
-// deep: each CTA folds its 2 or 4 partial results per stream, atomicMax-es
-// them into one of eight keys per stream (CTA c into key c % 8, which keeps
-// same-address atomics few), counts its arrival, and once the count shows
-// every CTA every CTA reads the eight keys and the flags and takes the picks
-// itself, so no CTA has to publish them before the next step; CTA 0 writes the
-// outputs and clears the generation two steps ahead. Waits are bounded as in
-// the other kernels; a CTA that gives up raises the launch's abort word, and
-// CTA 0 marks the rows of the steps not done (flag bit 1).
+// deep: each CTA atomicMax-es its key per stream into one of eight keys per
+// stream (CTA c into key c % 8, which keeps same-address atomics few), counts
+// its arrival, and once the count shows every CTA, every CTA reads the eight
+// keys and the flags and takes the picks itself, so no CTA has to publish
+// them before the next step; CTA 0 writes the outputs and clears the
+// generation two steps ahead. Before it arrives, a CTA asks L2 for the W1
+// rows of its own best tokens, one of which is each stream's next token.
+// Waits are bounded as in the other kernels; a CTA that gives up raises the
+// launch's abort word, and CTA 0 marks the rows of the steps not done (flag
+// bit 1).
 
 constexpr int kTmTiles = 3;       // W2 tiles a CTA holds in tensor memory
 constexpr int kSmTiles = 1;       // W2 tiles a CTA holds in shared memory
 constexpr int kKeyGroups = 8;     // per-stream keys CTAs meet in (CTA c in key c % 8)
 constexpr int kMaxDynSmem = 232448;
 constexpr int kRingMax = 12;
+constexpr int kBaseBufs = 3;      // tiles of base logits staged ahead
 constexpr uint32_t kHoldCols = 512;
 constexpr int kHoldEpi = 256;                     // epilogue threads: two groups of four warps
 constexpr int kHoldMmaWarp = 8, kHoldTmaWarp = 9;
@@ -793,36 +798,39 @@ constexpr int kHoldThreads = kHoldEpi + 64;
 struct HoldBars {
     uint64_t full[kRingMax];
     uint64_t empty[kRingMax];
+    uint64_t bfull[kBaseBufs];   // a tile's base logits have landed (each producer lane's copies)
+    uint64_t bempty[kBaseBufs];  // the 8 epilogue warps have read them
     uint64_t acc_full[2];
-    uint64_t acc_empty[2];
-    uint64_t e_ready;       // E holds the step's W1 rows (the 128 epilogue threads)
-    uint64_t tm_ready;      // the tensor-memory tiles are written (the 128 epilogue threads)
-    uint64_t res_full;      // the shared-memory tile has landed
+    uint64_t acc_empty[2];       // the 8 epilogue warps have read the accumulator
+    uint64_t e_ready;            // E holds the step's W1 rows (the 256 epilogue threads)
+    uint64_t tm_ready;           // the tensor-memory tiles are written (the 256 epilogue threads)
+    uint64_t res_full;           // the shared-memory tile has landed
     uint64_t drain;
     uint32_t tmem_base;
-    int32_t stop;           // epilogue thread 0's snapshot of the abort flag, read after a barrier
+    int32_t stop;                // epilogue thread 0's snapshot of the abort flag, read after a barrier
     WaitCtl wc;
-    int32_t tok[64];        // the step's previous token of stream s, -1 if none or invalid
-    int32_t row[64];        // the step's draft row of stream s, -1 if it has none
+    int32_t tok[64];             // the step's previous token of stream s, -1 if none or invalid
+    int32_t row[64];             // the step's draft row of stream s, -1 if it has none
+    uint32_t wkey[8][32];        // step end: each warp's best key per stream of its group (all ones: nonfinite)
 };
 
 template <int kN>
 struct Hold {
+    static constexpr int kS = kN / 2;                     // streams per epilogue group
     static constexpr int kEB = kKB * kN * 128;            // E: kN rows x 256, four k-blocks of kN x 128 B
-    static constexpr int kStgB = kN * kTileV * 2;         // one staging buffer: [stream][128 columns] bf16
+    static constexpr int kBaseB = kN * kTileV * 2;        // one tile of base logits: [stream][128] bf16
     static constexpr int kResB = kSmTiles * kKB * kSlabB;
-    static constexpr int kFixed = 1024 + kEB + kResB + 2 * kStgB + int(sizeof(HoldBars));
+    static constexpr int kFixed = 1024 + kEB + kResB + kBaseBufs * kBaseB + int(sizeof(HoldBars));
     static constexpr int kRingFit = (kMaxDynSmem - kFixed) / kSlabB;
     static constexpr int kRing = kRingFit < kRingMax ? kRingFit : kRingMax;
     static constexpr int kSmem = kFixed + kRing * kSlabB;
-    static constexpr int kParts = kTileV / kN;            // phase-B threads per stream
     static constexpr uint32_t kAcc = kTmTiles * 128;      // tensor-memory column of accumulator 0
     // kind::f16, fp32 accumulate, A and B bf16 K-major, N = kN, M = 128
     static constexpr uint32_t kIdesc =
         (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kN >> 3) << 17) | (uint32_t(128 >> 4) << 24);
     static_assert(kRing >= 4, "the ring holds at least one tile");
     static_assert(kAcc + 2 * kN <= kHoldCols, "tiles and accumulators fit tensor memory");
-    static_assert(kParts * kN == kTileV && kN % 32 == 0, "phase-B split");
+    static_assert(kS == 16 || kS == 32, "streams per group");
 };
 
 // tcgen05.mma with the accumulate flag as an immediate (0: overwrite D)
@@ -836,8 +844,16 @@ __device__ __forceinline__ void tc_mma_ts_acc(uint32_t d, uint32_t a, uint64_t b
     asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
                  ::"r"(d), "r"(a), "l"(b), "r"(idesc), "n"(ACC) : "memory");
 }
-__device__ __forceinline__ void sts16(uint32_t a, uint32_t v) {
-    asm volatile("st.shared.b16 [%0], %1;" ::"r"(a), "h"(static_cast<unsigned short>(v)) : "memory");
+__device__ __forceinline__ uint32_t lds16(uint32_t a) {
+    unsigned short v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+// packed bf16 pair compare: each 16-bit half all ones where a > b (ordered; 0 for NaN)
+__device__ __forceinline__ uint32_t gt_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("set.gt.u32.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
 }
 
 template <int kN>
@@ -847,27 +863,28 @@ markov_hold_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, const
                    const int32_t* __restrict__ prev, int32_t* __restrict__ pick, uint8_t* __restrict__ flag,
                    const __grid_constant__ CUtensorMap w2map) {
     using C = Hold<kN>;
+    constexpr int kS = C::kS;
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = su32(smem_raw);
     const uint32_t sbase = (raw + 1023u) & ~1023u;
     unsigned char* gbase = smem_raw + (sbase - raw);
     const uint32_t sE = sbase;
     const uint32_t sRes = sE + C::kEB;
-    const uint32_t sRing = sRes + C::kResB;
-    const uint32_t sStg = sRing + C::kRing * kSlabB;
-    unsigned char* gStg = gbase + (sStg - sbase);
-    HoldBars* bars = reinterpret_cast<HoldBars*>(gStg + 2 * C::kStgB);
+    const uint32_t sBase = sRes + C::kResB;
+    const uint32_t sRing = sBase + kBaseBufs * C::kBaseB;
+    HoldBars* bars = reinterpret_cast<HoldBars*>(gbase + (sRing - sbase) + C::kRing * kSlabB);
     volatile WaitCtl* abortp = &bars->wc;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nt = (vocab + kTileV - 1) / kTileV;
     const int t_begin = int((int64_t(blockIdx.x) * nt) / gridDim.x);
     const int t_end = int((int64_t(blockIdx.x + 1) * nt) / gridDim.x);
-    const int ntl = t_end - t_begin;
-    const int nT = ntl < kTmTiles ? ntl : kTmTiles;                      // tiles [0, nT) in tensor memory
+    const int ntl = t_end - t_begin;                                     // tiles, visited in vocabulary order
+    const int nT = ntl < kTmTiles ? ntl : kTmTiles;                      // [0, nT) in tensor memory
     const int nR = ntl < kTmTiles + kSmTiles ? ntl : kTmTiles + kSmTiles;   // [nT, nR) in shared memory
     const int ns = ntl - nR;                                             // [nR, ntl) streamed every step
-    // the i-th tile of a step: the first streamed tile (already in the ring
-    // when the step starts), the held tiles, then the other streamed ones
+    // the i-th tile of a step: the first streamed tile (its k-blocks already in
+    // the ring when the step starts), the held tiles, then the other streamed ones,
+    // so that the ring refills while the held tiles run
     auto order = [&](int i) { return ns == 0 ? i : (i == 0 ? nR : (i <= nR ? i - 1 : i)); };
     uint32_t* sync = t.mk_sync;                                          // [0] arrivals, [2] abort
     uint32_t* gflags = sync + 64;                                        // [3][64]
@@ -878,9 +895,13 @@ markov_hold_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, const
             mbar_init(su32(&bars->full[s]), 1);
             mbar_init(su32(&bars->empty[s]), 1);
         }
+        for (int q = 0; q < kBaseBufs; ++q) {
+            mbar_init(su32(&bars->bfull[q]), 32);   // the producer's 32 lanes, as their copies land
+            mbar_init(su32(&bars->bempty[q]), 8);
+        }
         for (int b = 0; b < 2; ++b) {
             mbar_init(su32(&bars->acc_full[b]), 1);
-            mbar_init(su32(&bars->acc_empty[b]), 4);   // the four warps of the accumulator's group
+            mbar_init(su32(&bars->acc_empty[b]), 8);
         }
         mbar_init(su32(&bars->e_ready), kHoldEpi);
         mbar_init(su32(&bars->tm_ready), kHoldEpi);
@@ -898,40 +919,120 @@ markov_hold_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, const
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == kHoldTmaWarp) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ producer warp
+        // lane 0: W2 (the shared-memory tile once, the streamed tiles' k-blocks
+        // through the ring every step); all lanes: each tile's base logits,
+        // lane l copying streams l and l + 32
+        const uint64_t keep = l2_evict_last();
         if (lane == 0) {
-            const uint64_t keep = l2_evict_last();
             {   // the tensor-memory tiles' rows (contiguous in W2) into L2 for the epilogue's loads
                 const int64_t r0 = int64_t(t_begin) * kTileV;
                 const int64_t r1 = min(int64_t(t_begin + nT) * kTileV, int64_t(vocab));
                 if (r1 > r0) l2_prefetch_bulk(W2 + r0 * TF_MK, uint32_t((r1 - r0) * TF_MK * 2));
             }
-            bool res_issued = false;
             if (nR > nT) {
                 mbar_expect_tx(su32(&bars->res_full), uint32_t(C::kResB));
                 for (int kb = 0; kb < kKB; ++kb)
                     tma_load_2d_hint(sRes + kb * kSlabB, &w2map, kb * 64, (t_begin + nT) * kTileV,
                                      su32(&bars->res_full), keep);
-                res_issued = true;
             }
-            const int per_step = ns * kKB;
-            const int total = steps * per_step;
-            int issued = 0;
-            for (int i = 0; i < total; ++i) {
-                const int s = i % C::kRing;
-                if (i >= C::kRing && !mbar_wait(su32(&bars->empty[s]), ((i / C::kRing) - 1) & 1, abortp)) break;
-                const int il = i % per_step;
-                const uint32_t bar = su32(&bars->full[s]);
-                mbar_expect_tx(bar, kSlabB);
-                tma_load_2d_hint(sRing + s * kSlabB, &w2map, (il % kKB) * 64, (t_begin + nR + il / kKB) * kTileV,
-                                 bar, keep);
-                ++issued;
+        }
+        int rows_s[2] = {0, 0}, off_s[2] = {0, 0};   // streams lane and lane + 32
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int s = lane + 32 * h;
+            if (s < kN && s < t.S) {
+                const SegStream st = t.streams[s];
+                rows_s[h] = st.rows;
+                off_s[h] = st.row_offset - s;
             }
-            if (abortp->flag) {   // let the copies in flight land before the CTA exits
-                for (int i = issued > C::kRing ? issued - C::kRing : 0; i < issued; ++i)
-                    mbar_drain(su32(&bars->full[i % C::kRing]), (i / C::kRing) & 1);
-                if (res_issued) mbar_drain(su32(&bars->res_full), 0);
+        }
+        // Two queues served as their slots free up, so that neither waits
+        // behind the other: base tiles (gb, in step order; a buffer frees when
+        // the epilogue has read it) and ring k-blocks (gr; a slot frees when the
+        // MMAs reading it complete). The ring thus refills across step
+        // boundaries while the epilogue still holds base buffers. Bounded: no
+        // progress for the wait limit (or another thread's give-up) ends it.
+        const int total_b = steps * ntl, per_step_r = ns * kKB, total_r = steps * per_step_r;
+        int gb = 0, gr = 0;
+        bool ok = true;
+        unsigned long long idle0 = gtime();
+        while (ok && (gb < total_b || gr < total_r)) {
+            bool moved = false;
+            if (gb < total_b) {
+                const int q = gb % kBaseBufs;
+                bool free_q = gb < kBaseBufs;
+                if (!free_q && lane == 0) free_q = mbar_test(su32(&bars->bempty[q]), ((gb / kBaseBufs) - 1) & 1);
+                if (__shfl_sync(0xFFFFFFFFu, free_q ? 1 : 0, 0)) {
+                    // 16-byte asynchronous copies through the load path (many small bulk
+                    // copies would queue on the SM's one TMA unit, ahead of W2): lane l
+                    // copies the rows of streams l and l + 32, through L1 so that the two
+                    // halves of each 32-byte sector are fetched from L2 once
+                    const int j = gb / ntl, i = gb - j * ntl;
+                    const int v0 = (t_begin + order(i)) * kTileV;
+                    // 128 logits, or the vocabulary's tail rounded up to 16 bytes (within
+                    // the row: the stride is a multiple of 8 elements and at least the vocabulary)
+                    const int nv = vocab - v0 < kTileV ? vocab - v0 : kTileV;
+                    const int nchunk = (nv + 7) >> 3;
+                    const uint32_t dst = sBase + uint32_t(q * C::kBaseB);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        if (rows_s[h] - 1 > j) {
+                            const uint16_t* src = base + int64_t(off_s[h] + j) * base_stride + v0;
+                            const uint32_t d = dst + uint32_t((lane + 32 * h) * 256);
+#pragma unroll
+                            for (int c = 0; c < 16; ++c)
+                                if (c < nchunk)
+                                    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(d + c * 16),
+                                                 "l"(src + c * 8) : "memory");
+                        }
+                    }
+                    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(su32(&bars->bfull[q]))
+                                 : "memory");
+                    ++gb;
+                    moved = true;
+                }
             }
+            if (gr < total_r) {
+                const int s = gr % C::kRing;
+                bool free_s = gr < C::kRing;
+                if (lane == 0) {
+                    if (!free_s) free_s = mbar_test(su32(&bars->empty[s]), ((gr / C::kRing) - 1) & 1);
+                    if (free_s) {
+                        const int il = gr % per_step_r;
+                        const uint32_t bar = su32(&bars->full[s]);
+                        mbar_expect_tx(bar, kSlabB);
+                        tma_load_2d_hint(sRing + s * kSlabB, &w2map, (il % kKB) * 64,
+                                         (t_begin + nR + il / kKB) * kTileV, bar, keep);
+                    }
+                }
+                if (__shfl_sync(0xFFFFFFFFu, free_s ? 1 : 0, 0)) {
+                    ++gr;
+                    moved = true;
+                }
+            }
+            if (moved) {
+                idle0 = gtime();
+            } else {
+                bool give_up = false;
+                if (lane == 0) {
+                    if (abortp->flag) {
+                        give_up = true;
+                    } else if (gtime() - idle0 > abortp->limit_ns) {
+                        abortp->flag = 1;
+                        give_up = true;
+                    }
+                }
+                ok = !__shfl_sync(0xFFFFFFFFu, give_up ? 1 : 0, 0);
+                __nanosleep(20);
+            }
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");   // every lane's base copies have landed
+        if (!ok && lane == 0) {
+            // let the copies in flight land before the CTA exits (bounded waits)
+            for (int i = gr > C::kRing ? gr - C::kRing : 0; i < gr; ++i)
+                mbar_drain(su32(&bars->full[i % C::kRing]), (i / C::kRing) & 1);
+            if (nR > nT) mbar_drain(su32(&bars->res_full), 0);
         }
         __syncwarp();
     } else if (warp == kHoldMmaWarp) {
@@ -1025,19 +1126,10 @@ markov_hold_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, const
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue: two groups of 128 threads
-        // group wg takes the step-ordered tiles g with g % 2 == wg, accumulator wg and staging buffer wg
-        const int wg = tid >> 7, et = tid & 127;   // et: the TMEM lane (tile row) of phase A
+        // thread et = TMEM lane = row et of every tile; group wg takes streams [wg*kS, wg*kS + kS)
+        const int wg = tid >> 7, et = tid & 127;
         const uint32_t tlane = tmem + (uint32_t((warp & 3) * 32) << 16);
-        const int ps = et % kN, ph = et / kN;   // phase B: stream ps, columns [ph*kN, ph*kN + kN) of a tile
-        const uint32_t stg = sStg + uint32_t(wg * C::kStgB);
-        auto wg_sync = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(1 + wg) : "memory"); };
-        auto all_sync = [&]() { asm volatile("bar.sync 3, 256;" ::: "memory"); };
-        int ps_rows = 0, ps_off = 0;
-        if (ps < t.S) {
-            const SegStream st = t.streams[ps];
-            ps_rows = st.rows;
-            ps_off = st.row_offset - ps;   // the stream's draft row of step j: ps_off + j
-        }
+        auto all_sync = [&]() { asm volatile("bar.sync 1, 256;" ::: "memory"); };
         auto prefetch_base = [&](int jj) {   // this CTA's slice of stream tid's base row of step jj into L2
             if (tid < t.S && jj < steps) {
                 const SegStream st = t.streams[tid];
@@ -1049,14 +1141,6 @@ markov_hold_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, const
                         l2_prefetch_bulk(base + int64_t(st.row_offset - tid + jj) * base_stride + v_begin, bytes);
                 }
             }
-        };
-        // base logits of the step-ordered tile g (over all steps) for phase B
-        uint32_t bcur[kN / 2];
-        auto load_b = [&](int g) {
-            const int j = g / ntl, i = g - (g / ntl) * ntl;
-            if (j < steps && ps_rows - 1 > j)
-                load_base<kN / 2>(base + int64_t(ps_off + j) * base_stride, (t_begin + order(i)) * kTileV + ph * kN,
-                                  vocab, bcur);
         };
         if (tid < 64) {
             int tok = -1, row = -1;
@@ -1072,7 +1156,6 @@ markov_hold_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, const
             bars->row[tid] = row;
         }
         prefetch_base(0);
-        load_b(wg);
         all_sync();
         int done_steps = 0;
         for (int j = 0; j < steps; ++j) {
@@ -1113,95 +1196,120 @@ markov_hold_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, const
             }
             prefetch_base(j + 1);
 
-            const bool valid = bars->tok[ps] >= 0;
-            float best = -INFINITY;
-            int bid = 0x7FFFFFFF;
-            uint32_t nf = 0;
+            // per stream pair of the group: the largest score so far (bf16 pair), the
+            // tile holding each, and nonfinite bits (bit 15 / 31)
+            // (the first streamed tile, visited first, is held aside as scores and
+            // merged after the held tiles, so that the running maximum sees the tiles
+            // in vocabulary order)
+            // btile: the tile of each best, two 16-bit halves like the scores
+            uint32_t best[kS / 2], nfa[kS / 2], early[kS / 2], btile[kS / 2];
+#pragma unroll
+            for (int p = 0; p < kS / 2; ++p) {
+                best[p] = 0xFF80FF80u;   // -inf, -inf
+                early[p] = 0xFF80FF80u;
+                nfa[p] = 0u;
+                btile[p] = 0u;
+            }
             bool ok = true;
-            for (int i = wg ^ ((j * ntl) & 1); i < ntl; i += 2) {   // this group's tiles of the step
-                const int gt = j * ntl + i;
-                // phase A: this lane's row of the tile, rounded to bf16, into the staging rows
+            for (int i = 0; i < ntl; ++i) {
+                const int gt = j * ntl + i, b = gt & 1, q = gt % kBaseBufs;
                 // (a warp that gave up still meets every barrier of the step, doing no work)
-                if (ok && mbar_wait_warp(su32(&bars->acc_full[wg]), (gt >> 1) & 1, abortp)) {
+                if (ok && mbar_wait_warp(su32(&bars->acc_full[b]), (gt >> 1) & 1, abortp)) {
                     tc_fence_after();
-                    // the accumulator into registers and back to the MMA at once, then staged
-                    uint32_t a0[32], a1[32];
-                    tc_ld_n<32>(tlane + C::kAcc + uint32_t(wg * kN), a0);
-                    if constexpr (kN == 64) tc_ld_n<32>(tlane + C::kAcc + uint32_t(wg * kN + 32), a1);
+                    uint32_t a[kS];
+                    tc_ld_n<kS>(tlane + C::kAcc + uint32_t(b * kN + wg * kS), a);
                     tc_wait_ld();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(su32(&bars->acc_empty[wg]));
-                    const uint32_t vo = uint32_t((et & 7) << 1), vc = uint32_t(et >> 3);
-                    auto stage = [&](const uint32_t (&a)[32], int s0) {
+                    if (lane == 0) mbar_arrive(su32(&bars->acc_empty[b]));
+                    if (mbar_wait_warp(su32(&bars->bfull[q]), (gt / kBaseBufs) & 1, abortp)) {
+                        const int lt = order(i);
+                        const uint32_t bb = sBase + uint32_t(q * C::kBaseB + wg * kS * 256 + et * 2);
+                        if ((t_begin + lt) * kTileV + et < vocab) {
+                            const bool hold = ns > 0 && i == 0;
+                            const uint32_t ltp = uint32_t(lt) * 0x00010001u;
 #pragma unroll
-                        for (int k = 0; k < 32; k += 2) {
-                            const int s = s0 + k;
-                            const uint32_t p = cvt_bf16x2(__uint_as_float(a[k + 1]), __uint_as_float(a[k]));
-                            sts16(stg + uint32_t(s * 256) + (((vc ^ uint32_t(s & 7)) << 4) | vo), p);
-                            sts16(stg + uint32_t((s + 1) * 256) + (((vc ^ uint32_t((s + 1) & 7)) << 4) | vo),
-                                  p >> 16);
+                            for (int p = 0; p < kS / 2; ++p) {
+                                const uint32_t lo = lds16(bb + uint32_t((2 * p) * 256));
+                                const uint32_t hi = lds16(bb + uint32_t((2 * p + 1) * 256));
+                                const uint32_t sc = add_bf16x2(
+                                    cvt_bf16x2(__uint_as_float(a[2 * p + 1]), __uint_as_float(a[2 * p])), lo | (hi << 16));
+                                nfa[p] |= (sc & 0x7F807F80u) + 0x00800080u;
+                                if (hold) {
+                                    early[p] = sc;
+                                } else {
+                                    const uint32_t g = gt_bf16x2(sc, best[p]);
+                                    best[p] = max_bf16x2(best[p], sc);
+                                    btile[p] = (btile[p] & ~g) | (ltp & g);
+                                }
+                            }
                         }
-                    };
-                    stage(a0, 0);
-                    if constexpr (kN == 64) stage(a1, 32);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(su32(&bars->bempty[q]));
+                    } else {
+                        ok = false;
+                    }
                 } else {
                     ok = false;
                 }
-                wg_sync();
-                // phase B: stream ps, its kN columns of the tile, with their base logits
-                if (ok && valid) {
-                    const int v0 = (t_begin + order(i)) * kTileV;
-                    uint32_t r16[kN / 2];
+                if (ns > 0 && i == nR) {   // the held tiles are in: the first streamed tile (tile nR) next
 #pragma unroll
-                    for (int q = 0; q < kN / 8; ++q) {
-                        const uint32_t c = uint32_t(ph * (kN / 8) + q) ^ uint32_t(ps & 7);
-                        const uint4 x = lds128(stg + uint32_t(ps * 256) + (c << 4));
-                        r16[4 * q] = x.x;
-                        r16[4 * q + 1] = x.y;
-                        r16[4 * q + 2] = x.z;
-                        r16[4 * q + 3] = x.w;
-                    }
-#pragma unroll
-                    for (int p = 0; p < kN / 32; ++p) {
-                        const int v = v0 + ph * kN + 32 * p;
-                        if (v < vocab) {
-                            uint32_t sc[16];
-#pragma unroll
-                            for (int k = 0; k < 16; ++k) sc[k] = add_bf16x2(r16[16 * p + k], bcur[16 * p + k]);
-                            score_sums(sc, v, vocab - v < 32 ? vocab - v : 32, best, bid, nf);
-                        }
+                    for (int p = 0; p < kS / 2; ++p) {
+                        const uint32_t g = gt_bf16x2(early[p], best[p]);
+                        best[p] = max_bf16x2(best[p], early[p]);
+                        btile[p] = (btile[p] & ~g) | ((uint32_t(nR) * 0x00010001u) & g);
                     }
                 }
-                load_b(gt + 2);
-                wg_sync();   // the staging buffer is read; the group's next tile may overwrite it
             }
-            // ---- the CTAs meet: fold this CTA's parts of each stream, then its key per stream
-            unsigned long long* red = reinterpret_cast<unsigned long long*>(gStg);   // both buffers are free now
-            uint32_t* nfl = reinterpret_cast<uint32_t*>(red + kHoldEpi);
-            all_sync();
-            red[tid] = (valid && bid != 0x7FFFFFFF)
-                           ? (static_cast<unsigned long long>(ord_bf16(best)) << 32) |
-                                 static_cast<unsigned long long>(0xFFFFFFFFu - uint32_t(bid))
-                           : 0ull;
-            nfl[tid] = (nf & 0x80008000u) ? 1u : 0u;
+            // ---- the argmax along the vocabulary: warp, then the group's four warps
+            // key = (ordered score << 16) | (0xFFFF - row within this CTA's range): the
+            // largest key is the largest score at the lowest row; a nonfinite score
+            // anywhere makes the stream's key all ones (above every score's)
+            uint32_t key[kS];
+#pragma unroll
+            for (int p = 0; p < kS / 2; ++p) {
+                const float lo = bf_lo(best[p]), hi = bf_hi(best[p]);
+                key[2 * p] = (nfa[p] & 0x8000u)
+                                 ? 0xFFFFFFFFu
+                                 : (ord_bf16(lo) << 16) | (0xFFFFu - ((btile[p] & 0xFFFFu) * kTileV + uint32_t(et)));
+                key[2 * p + 1] = (nfa[p] & 0x80000000u)
+                                     ? 0xFFFFFFFFu
+                                     : (ord_bf16(hi) << 16) | (0xFFFFu - ((btile[p] >> 16) * kTileV + uint32_t(et)));
+            }
+            // rows past the vocabulary never scored: their best stays -inf (key below any score's)
+            // reduce-scatter: after the pass with offset o, lane l keeps the streams whose bit o is l's
+#pragma unroll
+            for (int o = kS / 2; o >= 1; o >>= 1) {
+                const bool upper = (lane & o) != 0;
+#pragma unroll
+                for (int s = 0; s < o; ++s) {
+                    const uint32_t send = upper ? key[s] : key[s + o];
+                    const uint32_t keep = upper ? key[s + o] : key[s];
+                    key[s] = max(keep, __shfl_xor_sync(0xFFFFFFFFu, send, o));
+                }
+            }
+            if constexpr (kS == 16)   // lanes l and l ^ 16 hold the same stream: fold them
+                key[0] = max(key[0], __shfl_xor_sync(0xFFFFFFFFu, key[0], 16));
+            // lane l now holds stream l % kS of the group
+            if (lane < kS) bars->wkey[warp][lane] = key[0];
             all_sync();
             const int b3 = j % 3;
             if (tid < kN && bars->tok[tid] >= 0) {
-                unsigned long long k = 0;
-                uint32_t f = 0;
+                const int g = tid / kS, sl = tid % kS;
+                uint32_t k = 0;
 #pragma unroll
-                for (int h = 0; h < 2 * C::kParts; ++h) {   // both groups' parts of stream tid
-                    const int e = (h / C::kParts) * 128 + (h % C::kParts) * kN + tid;
-                    k = max(k, red[e]);
-                    f |= nfl[e];
-                }
+                for (int w = 0; w < 4; ++w) k = max(k, bars->wkey[4 * g + w][sl]);
                 // (a thread whose wait gave up has raised the abort flag: this CTA then
                 // does not arrive, and the launch ends without these keys being read)
-                if (f)
+                if (k == 0xFFFFFFFFu) {
                     atomicOr(&gflags[b3 * 64 + tid], 1u);
-                else if (k)
-                    atomicMax(&gkeys[(b3 * kKeyGroups + int(blockIdx.x) % kKeyGroups) * 64 + tid], k);
+                } else if (k >> 16) {
+                    const uint32_t bidv = uint32_t(t_begin * kTileV) + (0xFFFFu - (k & 0xFFFFu));
+                    const unsigned long long key64 =
+                        (static_cast<unsigned long long>(k >> 16) << 32) | static_cast<unsigned long long>(0xFFFFFFFFu - bidv);
+                    atomicMax(&gkeys[(b3 * kKeyGroups + int(blockIdx.x) % kKeyGroups) * 64 + tid], key64);
+                    l2_prefetch_bulk(W1 + size_t(bidv) * TF_MK, TF_MK * 2);   // a candidate next token's W1 row
+                }
             }
             if (blockIdx.x == 0) {   // clear the generation two steps ahead (read by every CTA before this step)
                 const int bn = (j + 1) % 3;
@@ -1318,7 +1426,8 @@ extern "C" int tf_markov_chain(const tf_segments* seg, const void* W1, const voi
     const char* path = std::getenv("TF_MARKOV_PATH");
     const bool per_step = (path && std::strcmp(path, "step") == 0) || t.S > kLanes;
     const bool streamed = path && std::strcmp(path, "chain") == 0;
-    if (!per_step && !streamed && t.S <= 64) {
+    // the held form keys a row within a CTA's range in 16 bits: at most 511 tiles a CTA
+    if (!per_step && !streamed && t.S <= 64 && (nt + gx - 1) / gx <= 511) {
         // W2 held on chip, the whole chain in one cooperative launch
         auto* kern = t.S <= 32 ? markov_hold_kernel<32> : markov_hold_kernel<64>;
         const int smem = t.S <= 32 ? Hold<32>::kSmem : Hold<64>::kSmem;
