@@ -757,18 +757,19 @@ markov_chain_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, int 
 // memory. Each CTA (one per SM) keeps the first three of its W2 tiles in
 // tensor memory (128 columns each, written once at the start), the fourth in
 // shared memory (loaded once), and streams the rest through a ring of 16 KB
-// k-blocks every step; the streamed tiles come last in a step, so the ring
-// refills while the CTAs meet between steps and while the held tiles run.
+// k-blocks every step. A step visits the first streamed tile first (its
+// k-blocks arrive while the CTAs meet between steps), then the held tiles
+// (while the ring refills), then the other streamed ones.
 //
 // Transposed, each TMEM lane holds one vocabulary row and each column one
 // stream. The epilogue works lane-major: thread = lane = vocabulary row, and
 // two groups of four warps split the streams (group g takes streams
 // [g*N/2, (g+1)*N/2)). Per tile a thread rounds its dot products to bf16 two
 // streams at a time, adds the base logits (staged per tile in shared memory
-// by bulk copies: stream s's 128 logits as one 256-byte row), and keeps per
-// stream the largest score with its tile (packed bf16 compare and max; tiles
-// are visited in vocabulary order, so a strict compare keeps the first) and
-// a nonfinite bit. The argmax along the vocabulary is then taken once a
+// by the producer warp's 16-byte asynchronous copies: stream s's 128 logits
+// as one 256-byte row), and keeps per stream the largest score with its tile
+// (packed bf16 compare and max, the tiles merged in vocabulary order, so a
+// strict compare keeps the first) and a nonfinite bit. The argmax along the vocabulary is then taken once a
 // step: a shuffle reduction over the warp's lanes of (ordered score, lowest
 // row) keys, then over the four warps.
 //
@@ -878,7 +879,7 @@ markov_hold_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, const
     const int nt = (vocab + kTileV - 1) / kTileV;
     const int t_begin = int((int64_t(blockIdx.x) * nt) / gridDim.x);
     const int t_end = int((int64_t(blockIdx.x + 1) * nt) / gridDim.x);
-    const int ntl = t_end - t_begin;                                     // tiles, visited in vocabulary order
+    const int ntl = t_end - t_begin;
     const int nT = ntl < kTmTiles ? ntl : kTmTiles;                      // [0, nT) in tensor memory
     const int nR = ntl < kTmTiles + kSmTiles ? ntl : kTmTiles + kSmTiles;   // [nT, nR) in shared memory
     const int ns = ntl - nR;                                             // [nR, ntl) streamed every step
