@@ -786,7 +786,15 @@ def run_row(args, rank, world):
         # compulsory bytes: W2 once (steps after the first may find it in L2), every base row,
         # the gathered W1 rows, picks and flags
         alg = w.vocab * I.MK * 2 + n * w.vocab * 2 + n * I.MK * 2 + n * 5
-        kname = "markov_step_kernel (tcgen05 W2 . W1[tok] + argmax), whole chain"
+        path = os.environ.get("TF_MARKOV_PATH", "")
+        S = len(w.rows)
+        if path == "step" or S > 128:
+            kname = "markov_step_kernel (tcgen05 W2 . W1[tok] + argmax), one launch a step"
+        elif path == "chain" or S > 64:
+            kname = "markov_chain_kernel (tcgen05, W2 streamed every step), whole chain in one launch"
+        else:
+            kname = (f"markov_hold_kernel<{32 if S <= 32 else 64}> (tcgen05, W2 held in tensor and shared "
+                     "memory), whole chain in one launch")
         launches = steps_per_call
         extra = {"markov_steps": steps_per_call, "w2_bytes": w.vocab * I.MK * 2,
                  "w2_reads_if_no_l2_reuse": steps_per_call * w.vocab * I.MK * 2}
