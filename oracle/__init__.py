@@ -9,7 +9,8 @@ Sources (web pages about the TensorFold project):
   * PR #1377 "LFM2: shared-round decode": the commits "a verify's greedy rows
     take the GPU's pick of their logits" (the greedy pick), "a shared round runs
     each layer's conv and attention once over all its streams" (segment table,
-    float64 attention, host replay of the conv steps, per-stream partials), and
+    per-stream partials, and checks against float64 attention and against
+    the conv's steps replayed on the host), and
     the commit on the kernel contract and its planted controls.
   * PR #1391 "lfm2: draft with LiquidAI's DSpark drafter (--drafter)": the
     target checks every draft; its attention stays causal.

@@ -8,8 +8,8 @@
 // contractions (4*rows flops per byte of K/V each) and this kernel measured
 // faster than the mma.sync one (which would take such a window as two 8-row
 // items reading the chunk twice). With `full` set it is the
-// drafter's non-causal block attention (PR #1391: every block row sees the
-// keys [0, len + 1)): only the per-row key bounds change.
+// drafter's non-causal block attention (PR #1391: all rows of a block share
+// one key range, the stream's whole cache): only the per-row key bounds change.
 //
 // Persistent (at most two CTAs per SM, each running (key chunk, KV head)
 // units back to back; see the kernel), 8 warps:

@@ -66,7 +66,7 @@ def workload(index, n_conv=None, n_attn=None, vocab=None):
        (rounded, raised to the window), drafts accepted with geometric length
        (p = 0.7 per draft).
     6: the other reading of workload 5 (labelled as such): the same key draw,
-       rows U{1..16} per stream, not rescaled to 1,024 (R about 544).
+       rows U{1..16} per stream, not rescaled to 1,024 (R = 564).
     """
     rng = np.random.Generator(np.random.PCG64(index))
     if index == 1:
