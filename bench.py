@@ -262,7 +262,7 @@ def kernel_source_hash():
     change of the code itself makes it stale)."""
     import re
     h = hashlib.sha256()
-    for name in ("attn.cu", "attn_tc.cu", "tf_internal.cuh"):
+    for name in ("attn.cu", "attn_tc.cu", "attn_item.cuh", "tc_ptx.cuh", "tf_internal.cuh"):
         with open(os.path.join(ROOT, "stream_speculative_decode_gb300", "csrc", name)) as f:
             src = f.read()
         src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
