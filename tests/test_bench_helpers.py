@@ -36,7 +36,7 @@ def test_clocks_bad(bench):
 def _tree(tmp_path):
     csrc = tmp_path / "stream_speculative_decode_gb300" / "csrc"
     csrc.mkdir(parents=True)
-    for name in ("attn.cu", "attn_tc.cu", "tf_internal.cuh"):
+    for name in ("attn.cu", "attn_tc.cu", "attn_item.cuh", "tc_ptx.cuh", "tf_internal.cuh"):
         shutil.copy(os.path.join(ROOT, "stream_speculative_decode_gb300", "csrc", name), csrc / name)
     return csrc
 
