@@ -139,6 +139,32 @@ __device__ __forceinline__ Unit unit_of(const SegTable& t, int layer, int u) {
     return U;
 }
 
+// Blackwell's three-input max and paired fp32 FMA / add: each of these does
+// the work of two instructions with the same per-element rounding.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 // State of one softmax thread for one unit: query row qi = per*(lane quadrant)
 // + lane sits on TMEM lane quadrant*32 + lane (lanes past `per` hold zero
 // rows). Windows of at most 16 rows (per <= 16) run dual: lanes L and L + 16
@@ -190,15 +216,14 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
                 for (int c = 0; c < NV; ++c)
                     if (k0 + c >= st.lim) v[c] = -INFINITY;
             }
-            float m8[8];
+            float m4[4];   // four independent chains of three-input maxima
 #pragma unroll
-            for (int a = 0; a < 8; ++a) {
-                m8[a] = v[a];
+            for (int a = 0; a < 4; ++a) {
+                m4[a] = v[a];
 #pragma unroll
-                for (int c = a + 8; c < NV; c += 8) m8[a] = fmaxf(m8[a], v[c]);
+                for (int c = a + 4; c < NV; c += 8) m4[a] = max3f(m4[a], v[c], c + 4 < NV ? v[c + 4] : v[c]);
             }
-            float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                             fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            float mx = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3]));
             if (DUAL) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));   // the row's two halves
             const float mxs = mx * kLog2e8;
             st.mtrue = fmaxf(st.mtrue, mxs);
@@ -245,14 +270,20 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
             }
             const float mu = (st.mref == -INFINITY) ? 0.f : st.mref;
             uint32_t own[NV / 2];
-            float s4[4] = {0.f, 0.f, 0.f, 0.f};   // four independent sums
+            // p = 2^(s*log2e/8 - mu), two at a time; two independent pair sums
+            const uint64_t k2 = f2pack(kLog2e8, kLog2e8), nmu2 = f2pack(-mu, -mu);
+            uint64_t sum2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
 #pragma unroll
             for (int c = 0; c < NV / 2; ++c) {
-                const float p0 = ex2(fmaf(v[2 * c], kLog2e8, -mu));
-                const float p1 = ex2(fmaf(v[2 * c + 1], kLog2e8, -mu));
-                s4[c & 3] += p0 + p1;
+                float x0, x1;
+                f2unpack(ffma2(f2pack(v[2 * c], v[2 * c + 1]), k2, nmu2), x0, x1);
+                const float p0 = ex2(x0), p1 = ex2(x1);
+                sum2[c & 1] = fadd2(sum2[c & 1], f2pack(p0, p1));
                 own[c] = pack_h2(p0, p1);
             }
+            float s4[4];
+            f2unpack(sum2[0], s4[0], s4[1]);
+            f2unpack(sum2[1], s4[2], s4[3]);
             if constexpr (DUAL) {   // P (fp16 pairs) of lane L: keys 0-31 at columns 0-15, 32-63 at 16-31
                 tc_st16x2_16<KC / 4>(st.trow + colS, own);
             } else {
