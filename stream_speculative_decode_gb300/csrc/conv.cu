@@ -103,6 +103,21 @@ conv_rows_kernel(SegTable t, int layer, const uint16_t* __restrict__ bcx,
     const int n = tile.nrows;
     const int row_base = st.row_offset + tile.row0;
     const bool first = tile.row0 == 0;
+    if (RPT == 2) {
+        // large tables: this thread's input rows into L2 while the previous kernel
+        // finishes (a non-binding hint: L2 is the point of coherence, so a line the
+        // previous kernel still writes is read after the wait as written)
+#pragma unroll
+        for (int k = 0; k < RPT; ++k) {
+            const int j = slot + k * kSlots;
+            if (j < n) {
+                const uint16_t* row = bcx + size_t(row_base + j) * TF_CIN + c;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(row));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(row + TF_H));
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(row + 2 * TF_H));
+            }
+        }
+    }
     pdl_wait();   // the table above; the data below may come from the previous kernel
 
     // this thread's rows slot, slot + kSlots, ... (loads issued before any arithmetic)
