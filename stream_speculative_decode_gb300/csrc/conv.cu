@@ -103,8 +103,8 @@ conv_rows_kernel(SegTable t, int layer, const uint16_t* __restrict__ bcx,
     const int n = tile.nrows;
     const int row_base = st.row_offset + tile.row0;
     const bool first = tile.row0 == 0;
-    if (RPT == 2) {
-        // large tables: this thread's input rows into L2 while the previous kernel
+    {
+        // this thread's input rows into L2 while the previous kernel
         // finishes (a non-binding hint: L2 is the point of coherence, so a line the
         // previous kernel still writes is read after the wait as written)
 #pragma unroll
