@@ -588,16 +588,20 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                     ok = false;
                     break;
                 }
-                const uint32_t vs = sStage + s * kStageB + kTileB;
+                const uint32_t vs = sStage + s * kStageB + kTileB + uint32_t(lane) * 16u;
+                // all 16 loads first: one shared-memory round trip a tile, not
+                // one per 16 bytes (the volatile loads and stores keep their order)
+                constexpr int NC = kTileB / 16 / 32;
+                uint4 v[NC];
 #pragma unroll
-                for (int c = 0; c < kTileB / 16 / 32; ++c) {
-                    const uint32_t a = vs + uint32_t(lane + 32 * c) * 16u;
-                    uint4 v = lds128(a);
-                    v.x = bf2_to_h2(v.x);
-                    v.y = bf2_to_h2(v.y);
-                    v.z = bf2_to_h2(v.z);
-                    v.w = bf2_to_h2(v.w);
-                    sts128(a, v);
+                for (int c = 0; c < NC; ++c) v[c] = lds128(vs + uint32_t(32 * c) * 16u);
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    v[c].x = bf2_to_h2(v[c].x);
+                    v[c].y = bf2_to_h2(v[c].y);
+                    v[c].z = bf2_to_h2(v[c].z);
+                    v[c].w = bf2_to_h2(v[c].w);
+                    sts128(vs + uint32_t(32 * c) * 16u, v[c]);
                 }
                 fence_async_smem();
                 __syncwarp();
