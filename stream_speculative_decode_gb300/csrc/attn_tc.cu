@@ -734,7 +734,7 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                                          ? 0 : (atomicAdd(ctr, 1) == st.n_chunks - 1);
                     if (group_sync(bars, gph, abortp) && bars->last) {
                         __threadfence();
-                        merge_stream_head<4>(st, U.g, part_o, part_ml, out, tid, 128);
+                        merge_stream_head<2, 4>(st, U.g, part_o, part_ml, out, tid, 128);
                         if (tid == 0) atomicExch(ctr, 0);
                     }
                 }

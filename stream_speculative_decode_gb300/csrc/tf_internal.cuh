@@ -233,58 +233,81 @@ __device__ __forceinline__ float* out_row(float* out, const SegStream& st, int g
 
 // Log-sum-exp merge of the chunk records of one (stream, KV head) into the
 // output, by the threads [tid, nthreads) of one CTA, one pass over the chunks
-// eight at a time (their loads in flight together) with a running max. The
-// records were written by other CTAs: they are read through L2 (ld.global.cg).
-template <int kB>   // records in flight per thread
+// kB at a time with a running max. A thread takes kU of its (query row, 4
+// dimensions) items at once and issues all their loads before using any
+// (kU = 1: one item at a time). The records were written by other CTAs: they
+// are read through L2 (ld.global.cg).
+template <int kB, int kU = 1>   // records in flight per item, items per thread at once
 __device__ __forceinline__ void merge_stream_head(const SegStream& st, int g, const float* part_o,
                                                   const float2* part_ml, float* out, int tid, int nthreads) {
     const int nq = st.rows * 4;
+    const int n_items = nq * (TF_D / 4);
     const int64_t stride = int64_t(TF_NKV) * nq;
     const int64_t base = st.pbase + int64_t(g) * nq;
-    for (int idx = tid; idx < nq * (TF_D / 4); idx += nthreads) {
-        const int qi = idx >> 4, d4 = (idx & 15) * 4;
-        float M = -INFINITY, L = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c0 = 0; c0 < st.n_chunks; c0 += kB) {
-            float2 ml[kB];
-            float4 v[kB];
+    for (int i0 = tid; i0 < n_items; i0 += nthreads * kU) {
+        float M[kU], L[kU];
+        float4 acc[kU];
 #pragma unroll
-            for (int k = 0; k < kB; ++k) {
-                ml[k] = make_float2(-INFINITY, 0.f);
-                v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (c0 + k < st.n_chunks) {
-                    const int64_t rec = base + (c0 + k) * stride + qi;
-                    ml[k] = __ldcg(part_ml + rec);
-                    v[k] = __ldcg(reinterpret_cast<const float4*>(part_o + rec * TF_D + d4));
+        for (int u = 0; u < kU; ++u) {
+            M[u] = -INFINITY;
+            L[u] = 0.f;
+            acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        for (int c0 = 0; c0 < st.n_chunks; c0 += kB) {
+            float2 ml[kU][kB];
+            float4 v[kU][kB];
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                const int idx = i0 + u * nthreads;
+                const int qi = idx >> 4, d4 = (idx & 15) * 4;
+#pragma unroll
+                for (int k = 0; k < kB; ++k) {
+                    ml[u][k] = make_float2(-INFINITY, 0.f);
+                    v[u][k] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (idx < n_items && c0 + k < st.n_chunks) {
+                        const int64_t rec = base + (c0 + k) * stride + qi;
+                        ml[u][k] = __ldcg(part_ml + rec);
+                        v[u][k] = __ldcg(reinterpret_cast<const float4*>(part_o + rec * TF_D + d4));
+                    }
                 }
             }
-            float Mb = M;
 #pragma unroll
-            for (int k = 0; k < kB; ++k)
-                if (ml[k].y > 0.f) Mb = fmaxf(Mb, ml[k].x);
-            if (Mb == -INFINITY) continue;
-            const float sc = (M == -INFINITY) ? 0.f : ex2_approx(M - Mb);
-            L *= sc;
-            acc.x *= sc;
-            acc.y *= sc;
-            acc.z *= sc;
-            acc.w *= sc;
-            M = Mb;
+            for (int u = 0; u < kU; ++u) {
+                float Mb = M[u];
 #pragma unroll
-            for (int k = 0; k < kB; ++k) {
-                if (ml[k].y > 0.f) {
-                    const float w = ex2_approx(ml[k].x - M);
-                    L += w * ml[k].y;
-                    acc.x += w * v[k].x;
-                    acc.y += w * v[k].y;
-                    acc.z += w * v[k].z;
-                    acc.w += w * v[k].w;
+                for (int k = 0; k < kB; ++k)
+                    if (ml[u][k].y > 0.f) Mb = fmaxf(Mb, ml[u][k].x);
+                if (Mb == -INFINITY) continue;
+                const float sc = (M[u] == -INFINITY) ? 0.f : ex2_approx(M[u] - Mb);
+                L[u] *= sc;
+                acc[u].x *= sc;
+                acc[u].y *= sc;
+                acc[u].z *= sc;
+                acc[u].w *= sc;
+                M[u] = Mb;
+#pragma unroll
+                for (int k = 0; k < kB; ++k) {
+                    if (ml[u][k].y > 0.f) {
+                        const float w = ex2_approx(ml[u][k].x - Mb);
+                        L[u] += w * ml[u][k].y;
+                        acc[u].x += w * v[u][k].x;
+                        acc[u].y += w * v[u][k].y;
+                        acc[u].z += w * v[u][k].z;
+                        acc[u].w += w * v[u][k].w;
+                    }
                 }
             }
         }
-        const float inv = 1.f / L;
-        *reinterpret_cast<float4*>(out_row(out, st, g, qi) + d4) =
-            make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+            const int idx = i0 + u * nthreads;
+            if (idx < n_items) {
+                const int qi = idx >> 4, d4 = (idx & 15) * 4;
+                const float inv = 1.f / L[u];
+                *reinterpret_cast<float4*>(out_row(out, st, g, qi) + d4) =
+                    make_float4(acc[u].x * inv, acc[u].y * inv, acc[u].z * inv, acc[u].w * inv);
+            }
+        }
     }
 }
 
