@@ -58,6 +58,11 @@
 namespace tf {
 namespace {
 
+// Launches per SM so far, by SM id: the second of two CTAs on an SM puts its
+// V converter on another SM sub-partition than the first's (a load balance
+// only: any outcome is correct).
+__device__ unsigned int g_tc_sm_launches[1024];
+
 constexpr int kKT = 64;                     // keys per tile
 constexpr int kStages = 5;
 constexpr int kTileB = kKT * TF_D * 2;      // 8 KB: one K or V tile
@@ -96,6 +101,7 @@ struct Bars {
     int32_t redo_m;              // the CTA's last unit (running index) queued for the exact recompute
     int32_t is_last;             // this CTA finished last (it runs the exact recomputes)
     int32_t last;
+    int32_t alt;                 // this CTA swaps the producer and V-converter warps
 };
 constexpr int kSmemBytes = 1024 + kQB + kStages * kStageB + int(sizeof(Bars));
 
@@ -435,6 +441,9 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
         bars->wc.flag = 0;
         bars->wc.limit_ns = t.wait_ns;
         bars->redo_m = -1;
+        uint32_t smid;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+        bars->alt = int32_t(atomicAdd(&g_tc_sm_launches[smid & 1023u], 1u) & 1u);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (tid == 0 && int(blockIdx.x) < n_units) {   // the first unit's first tiles into L2 meanwhile
@@ -454,6 +463,9 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    // warp 5 converts V and warp 6 issues the TMA loads, or the other way round
+    // (the two CTAs of an SM keep their converters on different sub-partitions)
+    const int w_conv = bars->alt ? 6 : 5, w_prod = bars->alt ? 5 : 6;
 
     if (warp == 4) {
         // ------------------------------------------------------------ q.K MMAs
@@ -539,7 +551,7 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
             mbar_drain(su32(&bars->drain_pv), 0);
         }
         __syncwarp();
-    } else if (warp == 6) {
+    } else if (warp == w_prod) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
             // K/V are read once: ask L2 to evict them first (measured 4% faster
@@ -576,7 +588,7 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                     mbar_drain(su32(&bars->kv_full[k % kStages]), (k / kStages) & 1);
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == w_conv) {
         // ------------------------------------------------------------ V tiles bf16 -> fp16
         int gt = 0;
         bool ok = true;
