@@ -22,7 +22,11 @@
 //                    P.V of two tiles earlier, and the softmax waited for
 //                    its scores);
 //   warp 5           converts each V tile bf16 -> fp16 in shared memory as
-//                    soon as it lands (exact within fp16's range);
+//                    soon as it lands (exact within fp16's range); the
+//                    second CTA on an SM swaps warps 5 and 6, so the two
+//                    converters load different SM sub-partitions (the four
+//                    softmax warps move in lockstep: the sub-partition with
+//                    both converters set their pace);
 //   warps 0-3        softmax; query row qi sits on TMEM lane
 //                    32*(qi / per) + qi % per (per = 16 for windows of at
 //                    most 16 rows, 32 for wider ones), so the rows spread
