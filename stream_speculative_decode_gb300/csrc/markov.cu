@@ -1347,14 +1347,17 @@ markov_hold_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, const
                 int p = -1;
                 uint8_t f = 1;
                 if (row >= 0 && tok >= 0) {
+                    // the flag word and the eight key groups in one round trip
                     const uint32_t fl = __ldcg(&gflags[b3 * 64 + tid]);
+                    unsigned long long kg[kKeyGroups];
+#pragma unroll
+                    for (int g = 0; g < kKeyGroups; ++g) kg[g] = __ldcg(&gkeys[(b3 * kKeyGroups + g) * 64 + tid]);
                     if (fl) {
                         f = uint8_t(fl);
                     } else {
                         unsigned long long k = 0;
 #pragma unroll
-                        for (int g = 0; g < kKeyGroups; ++g)
-                            k = max(k, __ldcg(&gkeys[(b3 * kKeyGroups + g) * 64 + tid]));
+                        for (int g = 0; g < kKeyGroups; ++g) k = max(k, kg[g]);
                         p = int(0xFFFFFFFFu - uint32_t(k & 0xFFFFFFFFull));
                         f = 0;
                     }
