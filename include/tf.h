@@ -111,7 +111,7 @@ typedef struct tf_segments tf_segments;
 
 /* Split-K chunk of a stream: keys [c*chunk, (c+1)*chunk). The chunk length is
  * 256 * max(rows, 4) keys (partial records stay near 1/64 of the K/V bytes),
- * and 512 * rows for windows of 13 to 16 rows (the tensor-core kernel: fewer,
+ * and 512 * rows for windows of 9 to 16 rows (the tensor-core kernel: fewer,
  * longer units measured faster there); it depends on the stream alone, so a
  * stream's results do not depend on which other streams share the round. */
 int32_t tf_chunk_keys(int32_t rows);
@@ -175,7 +175,7 @@ int tf_conv_rows(const tf_segments* seg, int conv_layer, const void* bcx,
 /* a2. Causal GQA attention partials of one attention layer: for every stream,
  * KV head, key chunk, window row and query head, (m, l, o) over the chunk's
  * visible keys ([SRD]: the qk, attention and merge of the 10 attention
- * layers). Streams with windows of 13 rows or more run on the tcgen05
+ * layers). Streams with windows of 9 rows or more run on the tcgen05
  * tensor-core kernel, the others
  * on the mma.sync kernel; the choice depends on the stream alone (so a
  * stream's bits do not depend on its round), and a round holding both kinds
@@ -371,7 +371,7 @@ int tf_prompt_build(int32_t rows, int32_t keys, int32_t kv_capacity,
                     tf_cuda_stream stream, tf_segments** out);
 
 /* ---- failures on the device ------------------------------------------------
- * The tensor-core attention kernel (tf_attn*, streams of 13 rows or more and
+ * The tensor-core attention kernel (tf_attn*, streams of 9 rows or more and
  * prompt windows) and the Markov chain (tf_markov_chain) wait on barriers
  * that other warps or CTAs of the same launch complete. Every such wait is
  * bounded by the wait limit below. A CTA whose wait runs out gives up: it

@@ -4,10 +4,10 @@
 // Same work items, chunking and partial records as the mma.sync kernel in
 // attn.cu (PR #1377 "LFM2: shared-round decode": one launch a layer over every
 // row from the segment table, per-stream partials; PR #1391: causal count),
-// used when a window holds 13 rows or more, where q.K and P.V are real
+// used when a window holds 9 rows or more, where q.K and P.V are real
 // contractions (4*rows flops per byte of K/V each) and this kernel measured
-// faster than the mma.sync one (which would take such a window as two 8-row
-// items reading the chunk twice). With `full` set it is the
+// faster than the mma.sync one (which would take such a window as two items
+// of at most 8 rows reading the chunk twice). With `full` set it is the
 // drafter's non-causal block attention (PR #1391: all rows of a block share
 // one key range, the stream's whole cache): only the per-row key bounds change.
 //

@@ -370,7 +370,7 @@ int finish_build(tf_segments* seg, std::vector<tf::SegStream>& ss, std::vector<i
 extern "C" {
 
 int32_t tf_chunk_keys(int32_t rows) {
-    if (rows >= 13 && rows <= TF_MAX_ROWS) return 512 * rows;   // verify windows on the tensor-core kernel
+    if (rows >= tf::kTcMinRows && rows <= TF_MAX_ROWS) return 512 * rows;   // verify windows on the tensor-core kernel
     return 256 * (rows < 4 ? 4 : rows);
 }
 

@@ -97,11 +97,12 @@ struct SegTable {
 constexpr int kMkSyncBytes = 1024 + 3 * 8 * 64 * 8;
 
 constexpr int kAttnMma = 0;   // mma.sync flash-decode kernel (narrow windows)
-constexpr int kAttnTc = 1;    // tcgen05 + TMA kernel (windows of 13 rows or more)
-// Measured on GB300: the mma.sync kernel streams faster up to 12-row windows
-// (as one or two items of at most 8 rows); from 13 rows the
-// tensor-core kernel wins clearly.
-constexpr int kTcMinRows = 13;
+constexpr int kAttnTc = 1;    // tcgen05 + TMA kernel (windows of 9 rows or more)
+// Measured on GB300: the mma.sync kernel streams faster up to 8-row windows
+// (one item); from 9 rows, where mma.sync takes a window as two items of at
+// most 8 rows that read the chunk twice, the tensor-core kernel wins (one unit
+// reads it once: 64 streams of U{1..16} rows 1,403 -> 1,280 us a step).
+constexpr int kTcMinRows = 9;
 
 // Kernel of a stream: by its window rows, unless TF_ATTN_PATH forces one.
 int attn_path_of(int rows);

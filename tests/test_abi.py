@@ -67,7 +67,7 @@ def test_wait_limit_and_status_refusals(T):
 
 def _chunk(rows):
     """The documented chunk rule."""
-    return 512 * rows if 13 <= rows <= 16 else 256 * max(rows, 4)
+    return 512 * rows if 9 <= rows <= 16 else 256 * max(rows, 4)
 
 
 def test_chunk_rule(T):
@@ -233,10 +233,11 @@ def test_argmax_refusals(T):
     assert lib.tf_argmax_rows(0x1000, 2, (1 << 30) + 1, (1 << 30) + 1, 0x1000, 0x2000, None) == T.TF_ERANGE
 
 
-@pytest.mark.parametrize("rows,kernels", [([1], 1), ([1, 2], 1), ([3], 1), ([12, 4], 1), ([13], 1), ([16, 13], 1),
-                                          ([1, 13], 2), ([2, 16, 1], 2), ([12, 16], 2)])
+@pytest.mark.parametrize("rows,kernels", [([1], 1), ([1, 2], 1), ([3], 1), ([8, 4], 1), ([9], 1), ([12], 1),
+                                          ([16, 13], 1), ([12, 16], 1), ([1, 13], 2), ([2, 16, 1], 2),
+                                          ([8, 9], 2), ([12, 4], 2)])
 def test_attention_kernel_count(T, rows, kernels, monkeypatch):
-    """Windows of 13 rows or more go to the tensor-core kernel, narrower ones to
+    """Windows of 9 rows or more go to the tensor-core kernel, narrower ones to
     the mma.sync kernel; a round holding both makes one launch of each."""
     monkeypatch.delenv("TF_ATTN_PATH", raising=False)
     streams, off = [], 0

@@ -169,10 +169,10 @@ def test_step_merge_modes(mods, fused):
 
 def test_step_chunk_edges(mods):
     """Key counts at, just below and just above split-K chunk multiples
-    (256*max(r, 4) keys; 512*r for the 13-16-row windows of the tensor-core
+    (256*max(r, 4) keys; 512*r for the 9-16-row windows of the tensor-core
     kernel)."""
-    rows = [1, 1, 1, 2, 2, 4, 4, 8, 6, 16, 16, 13, 13]
-    keys = [1024, 1023, 1025, 2048, 2049, 1024, 1023, 2049, 1537, 8192, 8193, 6656, 6657]
+    rows = [1, 1, 1, 2, 2, 4, 4, 8, 6, 16, 16, 13, 13, 9, 9]
+    keys = [1024, 1023, 1025, 2048, 2049, 1024, 1023, 2049, 1537, 8192, 8193, 6656, 6657, 4608, 4609]
     run_and_check(mods, small_work(mods, rows, keys, n_conv=1, n_attn=1, seed=6))
 
 

@@ -41,7 +41,7 @@ def _check_prompt(inp, res):
 def test_prompt_small(mods, rows, cached):
     """Ragged last windows (1, 16, 17, 13 of 45, 9 of 41, 12 of 300 rows), a
     prompt that starts the cache (no cached keys), windows on both kernels
-    (13 rows and up: tensor cores; shorter: mma.sync), windows of two key
+    (9 rows and up: tensor cores; shorter: mma.sync), windows of two key
     chunks (64 rows after 8,200 keys: 8,192-key chunks)."""
     tf, inputs, step, torch = mods
     w = inputs.prompt_workload(rows, cached, n_conv=2, n_attn=2, seed=rows + cached)

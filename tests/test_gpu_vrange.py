@@ -74,7 +74,7 @@ def test_scaled_v_matches_float64(mods, monkeypatch, path, k):
     largest (65,504), 2^100 near the top of bf16's range, 2^-20 and 2^-60 far
     below fp16's normal range; 2^-8 puts partial outputs around the 2^-10
     threshold, so recomputed and fp16 pieces meet in one output. Each kernel
-    forced in turn (TF_ATTN_PATH), and the natural split (windows of 13 rows
+    forced in turn (TF_ATTN_PATH), and the natural split (windows of 9 rows
     or more on the tensor cores)."""
     tf, inputs, step, torch = mods
     if path:

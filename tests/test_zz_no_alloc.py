@@ -101,7 +101,7 @@ def test_static_scratch_refuses_oversized_table(mods):
     """A table whose partials exceed the fixed array is refused with TF_ERANGE
     before anything is launched."""
     tf, inputs, step, torch = mods
-    rows, keys = 12, 520_000  # one 12-row stream: 170 chunks of 3,072 keys -> 17.2 MB of partials
+    rows, keys = 8, 520_000  # one 8-row stream: 254 chunks of 2,048 keys -> 17.2 MB of partials
     cap = inputs.kv_capacity(keys)
     K = torch.zeros((8, cap, 64), dtype=torch.bfloat16, device="cuda")
     V = torch.zeros((8, cap, 64), dtype=torch.bfloat16, device="cuda")
