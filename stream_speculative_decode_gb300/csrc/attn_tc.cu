@@ -39,9 +39,11 @@
 //                  keys, K = 64: A = Q (bf16, smem), B = K tile (bf16, smem);
 //                  issued while the softmax still works on tile j-1;
 //   softmax        thread = query row: the 64 scores in registers (one TMEM
-//                  load), row max, lazy rescale of O (only when the max rises
-//                  more than 2^8), p = 2^(s*log2e/8 - m) packed to fp16 in
-//                  place of S; windows of at most 16 rows run it dual (two
+//                  load), p = 2^(s*log2e/8 - m) against the row's reference
+//                  m, packed to fp16 in place of S; the tile's max only when
+//                  the tile's sum of p passes 2^8 (it bounds every p) or the
+//                  row has no reference yet, then a lazy rescale of O to the
+//                  new reference; windows of at most 16 rows run it dual (two
 //                  lanes per query row, 32 keys each, the row's two O
 //                  halves added at the end);
 //   O += P V       A = P (fp16, tensor memory), B = V tile (fp16, smem,
@@ -80,7 +82,7 @@ constexpr int kSBuf = 3;                    // S/P buffers: tile j uses buffer j
 constexpr uint32_t kColS = 0;               // + 64 * (tile % 3)
 constexpr uint32_t kColO = 192;             // O: 64 columns
 constexpr float kLog2e8 = 0.18033688011112042f;   // log2(e) / sqrt(64)
-constexpr float kTau = 8.f;
+constexpr float kSumMax = 256.f;            // 2^8: a tile whose p sum within it keeps its reference
 
 constexpr int kUQ = 4;                      // queue of the CTA's next units
 constexpr int kUQConsumers = 7;             // the two MMA threads, V converter warp, 4 softmax warps
@@ -175,6 +177,28 @@ __device__ __forceinline__ uint64_t fadd2(uint64_t a, uint64_t b) {
     return d;
 }
 
+// p = 2^(s*log2e/8 - mu) for a thread's NV scores, two at a time, packed to
+// fp16 pairs; returns the fp32 sum (two independent pair sums, added as
+// ((s0 + s1) + (s2 + s3))). mu = 0 stands for a reference of -inf.
+template <int NV>
+__device__ __forceinline__ float exp_tile(const float (&v)[NV], float mref, uint32_t (&own)[NV / 2]) {
+    const float mu = (mref == -INFINITY) ? 0.f : mref;
+    const uint64_t k2 = f2pack(kLog2e8, kLog2e8), nmu2 = f2pack(-mu, -mu);
+    uint64_t sum2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
+#pragma unroll
+    for (int c = 0; c < NV / 2; ++c) {
+        float x0, x1;
+        f2unpack(ffma2(f2pack(v[2 * c], v[2 * c + 1]), k2, nmu2), x0, x1);
+        const float p0 = ex2(x0), p1 = ex2(x1);
+        sum2[c & 1] = fadd2(sum2[c & 1], f2pack(p0, p1));
+        own[c] = pack_h2(p0, p1);
+    }
+    float s4[4];
+    f2unpack(sum2[0], s4[0], s4[1]);
+    f2unpack(sum2[1], s4[2], s4[3]);
+    return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+}
+
 // State of one softmax thread for one unit: query row qi = per*(lane quadrant)
 // + lane sits on TMEM lane quadrant*32 + lane (lanes past `per` hold zero
 // rows). Windows of at most 16 rows (per <= 16) run dual: lanes L and L + 16
@@ -187,7 +211,7 @@ struct SoftState {
     int g0;              // the CTA's running tile count at the unit's first tile
     int T, lim, lim_all;
     bool wact;           // the warp holds at least one real query row
-    float mref, mtrue;   // reference (lazy) and true running max, log2 units
+    float mref;          // reference max (lazy), log2 units: -inf until a tile gives the row a finite score
     float l;             // sum of 2^(s*log2e/8 - mref) over the keys so far
 };
 
@@ -210,8 +234,8 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
         tc_fence_after();
         if (st.wact) {
             const int k0 = j * kKT + half * NV;      // chunk-local key of v[0]
-            float v[NV];
-            {
+            // this thread's scores of the tile, -inf past the row's last key
+            auto load_scores = [&](float (&v)[NV]) {
                 uint32_t r[NV];
                 if constexpr (DUAL)
                     tc_ld16x2_32<KC / 2>(st.trow + colS, r);   // this half's 32 scores of lane L
@@ -220,86 +244,88 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
                 tc_wait_ld();
 #pragma unroll
                 for (int c = 0; c < NV; ++c) v[c] = __uint_as_float(r[c]);
-            }
-            if (j * kKT + kKT > st.lim_all) {   // the causal edge or the chunk's end lies in this tile
+                if (j * kKT + kKT > st.lim_all) {   // the causal edge or the chunk's end lies in this tile
 #pragma unroll
-                for (int c = 0; c < NV; ++c)
-                    if (k0 + c >= st.lim) v[c] = -INFINITY;
-            }
-            float m4[4];   // four independent chains of three-input maxima
-#pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                m4[a] = v[a];
-#pragma unroll
-                for (int c = a + 4; c < NV; c += 8) m4[a] = max3f(m4[a], v[c], c + 4 < NV ? v[c + 4] : v[c]);
-            }
-            float mx = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3]));
-            if (DUAL) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));   // the row's two halves
-            const float mxs = mx * kLog2e8;
-            st.mtrue = fmaxf(st.mtrue, mxs);
-            const bool resc = mxs > st.mref + kTau;
-            if (__any_sync(0xFFFFFFFFu, resc)) {
-                // O holds P.V of the unit's tiles < j; the last of them (j-1) must be done
-                if (j >= 1 && !mbar_wait_warp(su32(&bars->o_done[(gj - 1) % kSBuf]), ((gj - 1) / kSBuf) & 1, st.abortp))
-                    break;
-                tc_fence_after();
-                const float alpha = resc ? ex2(st.mref - mxs) : 1.f;
-                if (resc) {
-                    st.mref = mxs;
-                    st.l *= alpha;
+                    for (int c = 0; c < NV; ++c)
+                        if (k0 + c >= st.lim) v[c] = -INFINITY;
                 }
-                if (j >= 1) {
-                    if constexpr (DUAL) {   // this thread's 32 columns of O
-#pragma unroll 1
-                        for (int h = 0; h < 2; ++h) {
-                            uint32_t o16[16];
-                            tc_ld16x2_16<32>(st.trow + kColO + 16 * h, o16);
-                            tc_wait_ld();
-#pragma unroll
-                            for (int c = 0; c < 16; ++c) o16[c] = __float_as_uint(__uint_as_float(o16[c]) * alpha);
-                            tc_st16x2_16<32>(st.trow + kColO + 16 * h, o16);
-                        }
-                    } else {
-#pragma unroll 1
-                        for (int h = 0; h < 4; ++h) {   // O (64 columns)
-                            uint32_t o16[16];
-                            tc_ld16(st.trow + kColO + 16 * h, o16);
-                            tc_wait_ld();
-                            uint32_t a8[8], b8[8];
-#pragma unroll
-                            for (int c = 0; c < 8; ++c) {
-                                a8[c] = __float_as_uint(__uint_as_float(o16[c]) * alpha);
-                                b8[c] = __float_as_uint(__uint_as_float(o16[8 + c]) * alpha);
-                            }
-                            tc_st8(st.trow + kColO + 16 * h, a8);
-                            tc_st8(st.trow + kColO + 16 * h + 8, b8);
-                        }
-                    }
-                    tc_wait_st();
-                }
-            }
-            const float mu = (st.mref == -INFINITY) ? 0.f : st.mref;
+            };
             uint32_t own[NV / 2];
-            // p = 2^(s*log2e/8 - mu), two at a time; two independent pair sums
-            const uint64_t k2 = f2pack(kLog2e8, kLog2e8), nmu2 = f2pack(-mu, -mu);
-            uint64_t sum2[2] = {f2pack(0.f, 0.f), f2pack(0.f, 0.f)};
-#pragma unroll
-            for (int c = 0; c < NV / 2; ++c) {
-                float x0, x1;
-                f2unpack(ffma2(f2pack(v[2 * c], v[2 * c + 1]), k2, nmu2), x0, x1);
-                const float p0 = ex2(x0), p1 = ex2(x1);
-                sum2[c & 1] = fadd2(sum2[c & 1], f2pack(p0, p1));
-                own[c] = pack_h2(p0, p1);
+            float psum;
+            {
+                float v[NV];
+                load_scores(v);
+                psum = exp_tile<NV>(v, st.mref, own);
             }
-            float s4[4];
-            f2unpack(sum2[0], s4[0], s4[1]);
-            f2unpack(sum2[1], s4[2], s4[3]);
+            // Every p of the tile is at most the tile's sum, so a sum within
+            // kSumMax keeps each within fp16's range and the reference stands
+            // without the tile's max. A row with no reference yet, or a larger
+            // sum (or a NaN), takes the warp through the max: the scores are
+            // loaded again (S is still in tensor memory), a row whose max rose
+            // takes it as the new reference (O rescaled), and p is recomputed.
+            const bool slow = st.mref == -INFINITY || !(psum <= kSumMax);
+            if (__any_sync(0xFFFFFFFFu, slow)) {
+                float v[NV];
+                load_scores(v);
+                float m4[4];   // four independent chains of three-input maxima
+#pragma unroll
+                for (int a = 0; a < 4; ++a) {
+                    m4[a] = v[a];
+#pragma unroll
+                    for (int c = a + 4; c < NV; c += 8) m4[a] = max3f(m4[a], v[c], c + 4 < NV ? v[c + 4] : v[c]);
+                }
+                float mx = max3f(m4[0], m4[1], fmaxf(m4[2], m4[3]));
+                if (DUAL) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 16));   // the row's two halves
+                const float mxs = mx * kLog2e8;
+                const bool resc = mxs > st.mref;
+                if (__any_sync(0xFFFFFFFFu, resc)) {
+                    // O holds P.V of the unit's tiles < j; the last of them (j-1) must be done
+                    if (j >= 1 && !mbar_wait_warp(su32(&bars->o_done[(gj - 1) % kSBuf]), ((gj - 1) / kSBuf) & 1, st.abortp))
+                        break;
+                    tc_fence_after();
+                    const float alpha = resc ? ex2(st.mref - mxs) : 1.f;
+                    if (resc) {
+                        st.mref = mxs;
+                        st.l *= alpha;
+                    }
+                    if (j >= 1) {
+                        if constexpr (DUAL) {   // this thread's 32 columns of O
+#pragma unroll 1
+                            for (int h = 0; h < 2; ++h) {
+                                uint32_t o16[16];
+                                tc_ld16x2_16<32>(st.trow + kColO + 16 * h, o16);
+                                tc_wait_ld();
+#pragma unroll
+                                for (int c = 0; c < 16; ++c) o16[c] = __float_as_uint(__uint_as_float(o16[c]) * alpha);
+                                tc_st16x2_16<32>(st.trow + kColO + 16 * h, o16);
+                            }
+                        } else {
+#pragma unroll 1
+                            for (int h = 0; h < 4; ++h) {   // O (64 columns)
+                                uint32_t o16[16];
+                                tc_ld16(st.trow + kColO + 16 * h, o16);
+                                tc_wait_ld();
+                                uint32_t a8[8], b8[8];
+#pragma unroll
+                                for (int c = 0; c < 8; ++c) {
+                                    a8[c] = __float_as_uint(__uint_as_float(o16[c]) * alpha);
+                                    b8[c] = __float_as_uint(__uint_as_float(o16[8 + c]) * alpha);
+                                }
+                                tc_st8(st.trow + kColO + 16 * h, a8);
+                                tc_st8(st.trow + kColO + 16 * h + 8, b8);
+                            }
+                        }
+                        tc_wait_st();
+                    }
+                }
+                psum = exp_tile<NV>(v, st.mref, own);   // rows that kept their reference get the same values
+            }
             if constexpr (DUAL) {   // P (fp16 pairs) of lane L: keys 0-31 at columns 0-15, 32-63 at 16-31
                 tc_st16x2_16<KC / 4>(st.trow + colS, own);
             } else {
                 tc_st_n<KC / 2>(st.trow + colS, own);
             }
-            st.l += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+            st.l += psum;
             tc_wait_st();
         }
         tc_fence_before();
@@ -653,7 +679,6 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
             ss.lim_all = (full ? st.keys : st.keys - st.rows + 1) - U.c0;
             ss.wact = wact;
             ss.mref = -INFINITY;
-            ss.mtrue = -INFINITY;
             ss.l = 0.f;
             if (dual)
                 softmax_tiles<kKT, true>(ss);
@@ -664,10 +689,11 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
             if (!abortp->flag) mbar_wait(su32(&bars->o_done[(gt - 1) % kSBuf]), ((gt - 1) / kSBuf) & 1, abortp);
             tc_fence_after();
             if (wact) {
-                // (m, l, O) renormalised to the true running max -> the chunk's record
+                // (m, l, O) relative to the row's reference max -> the chunk's record
+                // (the merge weighs each record by 2^(m - M): any reference the
+                // p were taken against gives the same result)
                 const bool aborted = abortp->flag != 0;
-                float f = 1.f;
-                if (ss.mtrue > ss.mref && ss.mref != -INFINITY) f = ex2(ss.mref - ss.mtrue);
+                const float f = 1.f;
                 // this thread's columns of O: all 64 of its lane, or (dual) its
                 // half [d0, d0 + 32) of lane L's row
                 auto finish = [&](auto& ro) {
@@ -707,7 +733,7 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                                                  __uint_as_float(ro[4 * c + 3]) * inv);
                     } else if (qvalid) {
                         const int64_t rec = st.pbase + (int64_t(U.chunk) * TF_NKV + U.g) * nq + qi;
-                        const bool empty = ss.mtrue == -INFINITY;
+                        const bool empty = ss.mref == -INFINITY;
                         float4* dst = reinterpret_cast<float4*>(part_o + rec * TF_D + d0);
 #pragma unroll
                         for (int c = 0; c < ND / 4; ++c) {
@@ -720,7 +746,7 @@ attn_partials_tc_kernel(SegTable t, int layer, const uint16_t* __restrict__ q, f
                         }
                         if (d0 == 0)
                             part_ml[rec] = aborted ? make_float2(NAN, INFINITY)
-                                                   : make_float2(ss.mtrue, empty ? 0.f : lsum * f);
+                                                   : make_float2(ss.mref, empty ? 0.f : lsum * f);
                     }
                 };
                 if (dual) {
