@@ -259,11 +259,14 @@ __device__ __forceinline__ void softmax_tiles(SoftState& st) {
             }
             // Every p of the tile is at most the tile's sum, so a sum within
             // kSumMax keeps each within fp16's range and the reference stands
-            // without the tile's max. A row with no reference yet, or a larger
-            // sum (or a NaN), takes the warp through the max: the scores are
-            // loaded again (S is still in tensor memory), a row whose max rose
-            // takes it as the new reference (O rescaled), and p is recomputed.
-            const bool slow = st.mref == -INFINITY || !(psum <= kSumMax);
+            // without the tile's max. A row that sees a key of the chunk but
+            // has no reference yet, or a larger sum (or a NaN), takes the warp
+            // through the max: the scores are loaded again (S is still in
+            // tensor memory), a row whose max rose takes it as the new
+            // reference (O rescaled), and p is recomputed. (A lane without a
+            // query, or a row that sees no key of the chunk, keeps -inf: its p
+            // are 0.)
+            const bool slow = (st.mref == -INFINITY && st.lim > 0) || !(psum <= kSumMax);
             if (__any_sync(0xFFFFFFFFu, slow)) {
                 float v[NV];
                 load_scores(v);
