@@ -793,8 +793,8 @@ constexpr int kRingMax = 12;
 constexpr int kBaseBufs = 3;      // tiles of base logits staged ahead
 constexpr uint32_t kHoldCols = 512;
 constexpr int kHoldEpi = 256;                     // epilogue threads: two groups of four warps
-constexpr int kHoldMmaWarp = 8, kHoldTmaWarp = 9;
-constexpr int kHoldThreads = kHoldEpi + 64;
+constexpr int kHoldMmaWarp = 8, kHoldTmaWarp = 9, kHoldBaseWarp = 10;
+constexpr int kHoldThreads = kHoldEpi + 96;
 
 struct HoldBars {
     uint64_t full[kRingMax];
@@ -920,12 +920,13 @@ markov_hold_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, const
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == kHoldTmaWarp) {
-        // ------------------------------------------------------------ producer warp
-        // lane 0: W2 (the shared-memory tile once, the streamed tiles' k-blocks
-        // through the ring every step); all lanes: each tile's base logits,
-        // lane l copying streams l and l + 32
-        const uint64_t keep = l2_evict_last();
+        // ------------------------------------------------------------ W2 producer (lane 0)
+        // the shared-memory tile once, the streamed tiles' k-blocks through the
+        // ring every step (a slot frees when the MMAs reading it complete, so
+        // the ring refills across step boundaries). Bounded: no progress for
+        // the wait limit (or another thread's give-up) ends it.
         if (lane == 0) {
+            const uint64_t keep = l2_evict_last();
             {   // the tensor-memory tiles' rows (contiguous in W2) into L2 for the epilogue's loads
                 const int64_t r0 = int64_t(t_begin) * kTileV;
                 const int64_t r1 = min(int64_t(t_begin + nT) * kTileV, int64_t(vocab));
@@ -937,7 +938,43 @@ markov_hold_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, const
                     tma_load_2d_hint(sRes + kb * kSlabB, &w2map, kb * 64, (t_begin + nT) * kTileV,
                                      su32(&bars->res_full), keep);
             }
+            const int per_step_r = ns * kKB, total_r = steps * per_step_r;
+            int gr = 0;
+            bool ok = true;
+            unsigned long long idle0 = gtime();
+            while (ok && gr < total_r) {
+                const int s = gr % C::kRing;
+                if (gr < C::kRing || mbar_test(su32(&bars->empty[s]), ((gr / C::kRing) - 1) & 1)) {
+                    const int il = gr % per_step_r;
+                    const uint32_t bar = su32(&bars->full[s]);
+                    mbar_expect_tx(bar, kSlabB);
+                    tma_load_2d_hint(sRing + s * kSlabB, &w2map, (il % kKB) * 64,
+                                     (t_begin + nR + il / kKB) * kTileV, bar, keep);
+                    ++gr;
+                    idle0 = gtime();
+                } else if (abortp->flag) {
+                    ok = false;
+                } else if (gtime() - idle0 > abortp->limit_ns) {
+                    abortp->flag = 1;
+                    ok = false;
+                } else {
+                    __nanosleep(20);
+                }
+            }
+            if (!ok) {
+                // let the copies in flight land before the CTA exits (bounded waits)
+                for (int i = gr > C::kRing ? gr - C::kRing : 0; i < gr; ++i)
+                    mbar_drain(su32(&bars->full[i % C::kRing]), (i / C::kRing) & 1);
+                if (nR > nT) mbar_drain(su32(&bars->res_full), 0);
+            }
         }
+        __syncwarp();
+    } else if (warp == kHoldBaseWarp) {
+        // ------------------------------------------------------------ base logits producer
+        // each tile's base logits, in step order (a buffer frees when the
+        // epilogue has read it), lane l copying the rows of streams l and
+        // l + 32; a warp of its own, so that W2's ring never waits behind
+        // these copies. Bounded like the W2 producer.
         int rows_s[2] = {0, 0}, off_s[2] = {0, 0};   // streams lane and lane + 32
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -948,71 +985,40 @@ markov_hold_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, const
                 off_s[h] = st.row_offset - s;
             }
         }
-        // Two queues served as their slots free up, so that neither waits
-        // behind the other: base tiles (gb, in step order; a buffer frees when
-        // the epilogue has read it) and ring k-blocks (gr; a slot frees when the
-        // MMAs reading it complete). The ring thus refills across step
-        // boundaries while the epilogue still holds base buffers. Bounded: no
-        // progress for the wait limit (or another thread's give-up) ends it.
-        const int total_b = steps * ntl, per_step_r = ns * kKB, total_r = steps * per_step_r;
-        int gb = 0, gr = 0;
+        const int total_b = steps * ntl;
+        int gb = 0;
         bool ok = true;
         unsigned long long idle0 = gtime();
-        while (ok && (gb < total_b || gr < total_r)) {
-            bool moved = false;
-            if (gb < total_b) {
-                const int q = gb % kBaseBufs;
-                bool free_q = gb < kBaseBufs;
-                if (!free_q && lane == 0) free_q = mbar_test(su32(&bars->bempty[q]), ((gb / kBaseBufs) - 1) & 1);
-                if (__shfl_sync(0xFFFFFFFFu, free_q ? 1 : 0, 0)) {
-                    // 16-byte asynchronous copies through the load path (many small bulk
-                    // copies would queue on the SM's one TMA unit, ahead of W2): lane l
-                    // copies the rows of streams l and l + 32, through L1 so that the two
-                    // halves of each 32-byte sector are fetched from L2 once
-                    const int j = gb / ntl, i = gb - j * ntl;
-                    const int v0 = (t_begin + order(i)) * kTileV;
-                    // 128 logits, or the vocabulary's tail rounded up to 16 bytes (within
-                    // the row: the stride is a multiple of 8 elements and at least the vocabulary)
-                    const int nv = vocab - v0 < kTileV ? vocab - v0 : kTileV;
-                    const int nchunk = (nv + 7) >> 3;
-                    const uint32_t dst = sBase + uint32_t(q * C::kBaseB);
+        while (ok && gb < total_b) {
+            const int q = gb % kBaseBufs;
+            bool free_q = gb < kBaseBufs;
+            if (!free_q && lane == 0) free_q = mbar_test(su32(&bars->bempty[q]), ((gb / kBaseBufs) - 1) & 1);
+            if (__shfl_sync(0xFFFFFFFFu, free_q ? 1 : 0, 0)) {
+                // 16-byte asynchronous copies through the load path (many small bulk
+                // copies would queue on the SM's one TMA unit, ahead of W2), through
+                // L1 so that the two halves of each 32-byte sector are fetched from L2 once
+                const int j = gb / ntl, i = gb - j * ntl;
+                const int v0 = (t_begin + order(i)) * kTileV;
+                // 128 logits, or the vocabulary's tail rounded up to 16 bytes (within
+                // the row: the stride is a multiple of 8 elements and at least the vocabulary)
+                const int nv = vocab - v0 < kTileV ? vocab - v0 : kTileV;
+                const int nchunk = (nv + 7) >> 3;
+                const uint32_t dst = sBase + uint32_t(q * C::kBaseB);
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        if (rows_s[h] - 1 > j) {
-                            const uint16_t* src = base + int64_t(off_s[h] + j) * base_stride + v0;
-                            const uint32_t d = dst + uint32_t((lane + 32 * h) * 256);
+                for (int h = 0; h < 2; ++h) {
+                    if (rows_s[h] - 1 > j) {
+                        const uint16_t* src = base + int64_t(off_s[h] + j) * base_stride + v0;
+                        const uint32_t d = dst + uint32_t((lane + 32 * h) * 256);
 #pragma unroll
-                            for (int c = 0; c < 16; ++c)
-                                if (c < nchunk)
-                                    asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(d + c * 16),
-                                                 "l"(src + c * 8) : "memory");
-                        }
-                    }
-                    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(su32(&bars->bfull[q]))
-                                 : "memory");
-                    ++gb;
-                    moved = true;
-                }
-            }
-            if (gr < total_r) {
-                const int s = gr % C::kRing;
-                bool free_s = gr < C::kRing;
-                if (lane == 0) {
-                    if (!free_s) free_s = mbar_test(su32(&bars->empty[s]), ((gr / C::kRing) - 1) & 1);
-                    if (free_s) {
-                        const int il = gr % per_step_r;
-                        const uint32_t bar = su32(&bars->full[s]);
-                        mbar_expect_tx(bar, kSlabB);
-                        tma_load_2d_hint(sRing + s * kSlabB, &w2map, (il % kKB) * 64,
-                                         (t_begin + nR + il / kKB) * kTileV, bar, keep);
+                        for (int c = 0; c < 16; ++c)
+                            if (c < nchunk)
+                                asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(d + c * 16),
+                                             "l"(src + c * 8) : "memory");
                     }
                 }
-                if (__shfl_sync(0xFFFFFFFFu, free_s ? 1 : 0, 0)) {
-                    ++gr;
-                    moved = true;
-                }
-            }
-            if (moved) {
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(su32(&bars->bfull[q]))
+                             : "memory");
+                ++gb;
                 idle0 = gtime();
             } else {
                 bool give_up = false;
@@ -1029,12 +1035,6 @@ markov_hold_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, const
             }
         }
         asm volatile("cp.async.wait_all;" ::: "memory");   // every lane's base copies have landed
-        if (!ok && lane == 0) {
-            // let the copies in flight land before the CTA exits (bounded waits)
-            for (int i = gr > C::kRing ? gr - C::kRing : 0; i < gr; ++i)
-                mbar_drain(su32(&bars->full[i % C::kRing]), (i / C::kRing) & 1);
-            if (nR > nT) mbar_drain(su32(&bars->res_full), 0);
-        }
         __syncwarp();
     } else if (warp == kHoldMmaWarp) {
         // ------------------------------------------------------------ MMA
