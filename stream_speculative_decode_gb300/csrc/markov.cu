@@ -766,8 +766,9 @@ markov_chain_kernel(SegTable t, int steps, const uint16_t* __restrict__ W1, int 
 // two groups of four warps split the streams (group g takes streams
 // [g*N/2, (g+1)*N/2)). Per tile a thread rounds its dot products to bf16 two
 // streams at a time, adds the base logits (staged per tile in shared memory
-// by the producer warp's 16-byte asynchronous copies: stream s's 128 logits
-// as one 256-byte row), and keeps per stream the largest score with its tile
+// by a producer warp of its own, in 16-byte asynchronous copies: stream s's
+// 128 logits as one 256-byte row; W2's ring has another, so that it never
+// waits behind these copies), and keeps per stream the largest score with its tile
 // (packed bf16 compare and max, the tiles merged in vocabulary order, so a
 // strict compare keeps the first) and a nonfinite bit. The argmax along the vocabulary is then taken once a
 // step: a shuffle reduction over the warp's lanes of (ordered score, lowest
