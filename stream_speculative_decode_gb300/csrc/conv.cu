@@ -5,12 +5,14 @@
 // over every row from the segment table, each row's arithmetic that of the
 // per-stream conv; streams longer than 8 rows are folded into 8-row tiles.
 //
-// Work split: a CTA owns one 8-row tile of one stream and 512 channels; its
-// 256 threads are 64 channel groups (8 consecutive channels, 16-byte loads of
+// Work split: a CTA owns one 8-row tile of one stream and 256 channels; its
+// 128 threads are 32 channel groups (8 consecutive channels, 16-byte loads of
 // B, C, x and the 3 taps) x 4 row slots, slot k taking the tile's rows k and
-// k + 4. A table of few tiles of two rows or more on average takes one row
-// per thread instead (32 groups x 8 slots, 256 channels a CTA: twice the
-// CTAs); the arithmetic of a row is the same either way. Every thread loads its rows at once, gates them (bx = B*x) into
+// k + 4 (128-thread CTAs, up to eight an SM: the next layer's CTAs find free
+// slots sooner than with 256-thread ones, a 1,024-row layer 5.43 -> 5.36 us
+// back to back). A table of few tiles of two rows or more on average takes
+// one row per thread instead (16 groups x 8 slots, 128 channels a CTA: twice
+// the CTAs); the arithmetic of a row is the same either way. Every thread loads its rows at once, gates them (bx = B*x) into
 // shared memory, and after one barrier convolves each row with the two
 // entries before it, so the rows of a tile run in parallel rather than one
 // after the other. The two entries before a tile come from the conv state
@@ -26,15 +28,15 @@ namespace tf {
 namespace {
 
 constexpr int kChan = 8;                        // channels per group
-constexpr int kThreads = 256;
-// The split of a CTA's 256 threads: RPT rows of the tile per thread, so
-// 8 / RPT row slots (slot k takes rows k, k + 8/RPT, ...) and 256 * RPT / 8
+constexpr int kThreads = 128;
+// The split of a CTA's 128 threads: RPT rows of the tile per thread, so
+// 8 / RPT row slots (slot k takes rows k, k + 8/RPT, ...) and 128 * RPT / 8
 // channel groups of 8 channels.
 template <int RPT>
 struct Split {
     static constexpr int kSlots = kConvTileRows / RPT;
     static constexpr int kGroups = kThreads / kSlots;
-    static constexpr int kChanPerCta = kGroups * kChan;   // 512 (RPT 2) or 256 (RPT 1)
+    static constexpr int kChanPerCta = kGroups * kChan;   // 256 (RPT 2) or 128 (RPT 1)
 };
 
 __device__ __forceinline__ void unpack8(const uint4& v, float f[8]) {
@@ -87,12 +89,12 @@ __device__ __forceinline__ void conv8(const uint4 (&w)[3], const uint4& e0, cons
 }
 
 template <int RPT>
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, 8)
 conv_rows_kernel(SegTable t, int layer, const uint16_t* __restrict__ bcx,
                  const uint16_t* __restrict__ w, float* __restrict__ y) {
     constexpr int kSlots = Split<RPT>::kSlots, kGroups = Split<RPT>::kGroups;
     constexpr int kChanPerCta = Split<RPT>::kChanPerCta;
-    __shared__ uint4 sbx[kConvTileRows][kGroups];   // the tile's gated entries (8 or 4 KB)
+    __shared__ uint4 sbx[kConvTileRows][kGroups];   // the tile's gated entries (4 or 2 KB)
     const ConvTile tile = t.tiles[blockIdx.x];
     const SegStream st = t.streams[tile.stream];
     const int grp = threadIdx.x % kGroups, slot = threadIdx.x / kGroups;
@@ -220,9 +222,9 @@ extern "C" int tf_conv_rows(const tf_segments* seg, int conv_layer, const void* 
     const uint16_t* in = static_cast<const uint16_t*>(bcx);
     const uint16_t* wt = static_cast<const uint16_t*>(w);
     // tiles of two rows or more on average, and few of them: one row per
-    // thread over 256 channels a CTA (twice the CTAs, half the serial work;
-    // measured faster while the grid stays within two CTAs per SM); else two
-    // rows per thread over 512 channels
+    // thread over 128 channels a CTA (twice the CTAs, half the serial work;
+    // measured faster while the grid stays within twice the SM count); else
+    // two rows per thread over 256 channels
     if (t.R >= 2 * t.n_tiles && t.n_tiles * (TF_H / Split<1>::kChanPerCta) <= 2 * sm_count())
         return launch_pdl(conv_rows_kernel<1>, dim3(t.n_tiles, TF_H / Split<1>::kChanPerCta), dim3(kThreads), 0,
                           stream, t, conv_layer, in, wt, y);
